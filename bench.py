@@ -1,0 +1,411 @@
+#!/usr/bin/env python3
+"""Benchmark of the KIVI decode hot path on GB300.
+
+One step = one decode step of the whole path for every sequence of the
+batch: kivi_append_flush appends one new K/V token per sequence (quantizing
+and packing a 32-token group whenever the residual window overflows), then
+kivi_decode_attn runs split-K decode attention over the packed 2-bit cache.
+
+Default workload: Llama-3-8B GQA decode layer shape, 64 sequences, 32 query
+heads over 8 kv heads, head_dim 128, 32768 cached tokens per sequence, bf16
+inputs, 2-bit codes, G = 32, R = 128. Inputs are synthetic and seeded; the
+cache (about 1.64 GB) is larger than L2, so no flush is needed between steps.
+
+Prints one JSON line. value = KV tokens attended per second over the timed
+steps (sum over sequences of kv_len, per step, divided by the step time).
+The roofline object is for the decode-attention kernel, from its own CUDA
+event timings inside the timed region.
+
+--impl reference times the CPU oracle on a bounded sample of the same
+workload (the only CPU-side arm; there is no other implementation).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn KV-tokens/s and achieved HBM GB/s (% of GB300 peak), 2-bit KIVI cache"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------- workload
+def workload_spec(args):
+    import synth
+    wl = synth.workload(2)
+    if args.batch:
+        wl = wl.replace(batch=args.batch, lengths=(args.context or wl.lengths[0],) * args.batch)
+    if args.context:
+        wl = wl.replace(lengths=(args.context,) * wl.batch)
+    if args.bits:
+        wl = wl.replace(bits=args.bits)
+    return wl
+
+
+def attn_bytes(wl, lengths, bits):
+    """Algorithmic bytes one decode launch must read: per (token, kv head) 96 B
+    (2-bit: 32 B key codes + 16 B key scale/zero share + 32 B value codes +
+    16 B value scale/zero) or 160 B (4-bit); 512 B per residual token (fp16/bf16 K and V)."""
+    R, G, D, H = wl.residual, wl.group, wl.head_dim, wl.num_kv_heads
+    per_packed = (2 * D * bits // 8) + 2 * 2 * 2 * D // G  # codes K+V, fp16 (s, z) K and V per element/G
+    total = 0
+    for L in lengths:
+        npk = G * (max(L - R, 0) // G)
+        total += H * (npk * per_packed + (L - npk) * 2 * D * 2)
+    return total
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())
+                if any(r[3].replace(".", "").isdigit() for r in rows) else None}
+
+
+# ---------------------------------------------------------------- GPU arm
+def smi_id(device) -> str:
+    """nvidia-smi --id of a torch device: its PCI bus id when torch reports one."""
+    import torch
+    p = torch.cuda.get_device_properties(device)
+    try:
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except AttributeError:
+        return str(device.index or 0)
+
+
+def gen_sequence_kv(wl, b, L, device):
+    """K, V of sequence b for all kv heads, [Hkv][L][D], drawn on the GPU."""
+    import torch
+    import synth
+    K = torch.stack([synth.torch_kv_head_major(wl, b, h, 0, L, "k", device) for h in range(wl.num_kv_heads)])
+    V = torch.stack([synth.torch_kv_head_major(wl, b, h, 0, L, "v", device) for h in range(wl.num_kv_heads)])
+    return K, V
+
+
+def step_inputs(wl, L0, n_steps, device):
+    """New K/V tokens ([steps][B][Hkv][1][D]) at positions L0 + s and queries ([steps][B][Hq][D])."""
+    import torch
+    import synth
+    B, H, D = wl.batch, wl.num_kv_heads, wl.head_dim
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
+    kn = torch.empty((n_steps, B, H, 1, D), dtype=tdt, device=device)
+    vn = torch.empty_like(kn)
+    for b in range(B):
+        for h in range(H):
+            kn[:, b, h, 0] = synth.torch_kv_head_major(wl, b, h, L0, n_steps, "k", device)
+            vn[:, b, h, 0] = synth.torch_kv_head_major(wl, b, h, L0, n_steps, "v", device)
+    q = torch.stack([torch.from_numpy(wl.query(s).view(np.int16)).view(tdt) for s in range(n_steps)]).to(device)
+    return kn, vn, q
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import bit_asymmetric_kv_kivi_gb300 as kivi
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    wl = workload_spec(args)
+    B, Hq, H, D, bits = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.bits
+    L0 = wl.lengths[0]
+    n_steps = args.warmup + args.steps
+    cap = ((L0 + n_steps + args.steps + 31) // 32) * 32   # decode steps of both timed legs
+    cfg = kivi.Config(bits=bits, head_dim=D, num_q_heads=Hq, num_kv_heads=H,
+                      dtype=kivi.BF16 if wl.dtype == "bf16" else kivi.F16)
+    cache = kivi.KVCache(cfg, B, cap, device)
+
+    # prefill (untimed): sequence by sequence, drawn on the GPU
+    for b0 in range(0, B, 8):
+        ks, vs = [], []
+        for b in range(b0, min(B, b0 + 8)):
+            K, V = gen_sequence_kv(wl, b, L0, device)
+            ks.append(K)
+            vs.append(V)
+        sub = list(range(b0, min(B, b0 + 8)))
+        empty = torch.empty((H, 0, D), dtype=ks[0].dtype, device=device)
+        cache.append([ks[sub.index(b)] if b in sub else empty for b in range(B)],
+                     [vs[sub.index(b)] if b in sub else empty for b in range(B)])
+        del ks, vs
+    torch.cuda.synchronize()
+    cache.max_len = L0
+    assert int(cache.status.item()) == 0, cache.status.item()
+
+    kn, vn, q = step_inputs(wl, L0, n_steps, device)
+    ones = torch.ones(B, dtype=torch.int32, device=device)
+    kptr = [torch.tensor([kn[s, b].data_ptr() for b in range(B)], dtype=torch.int64, device=device)
+            for s in range(n_steps)]
+    vptr = [torch.tensor([vn[s, b].data_ptr() for b in range(B)], dtype=torch.int64, device=device)
+            for s in range(n_steps)]
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=device)
+    max_len_final = L0 + n_steps
+    ws = cache.workspace(max_len_final)
+    stream = torch.cuda.current_stream(device)
+
+    def step(s, ev_a=None, ev_b=None):
+        cache.append_ptrs(kptr[s], vptr[s], ones, 1)
+        if ev_a is not None:
+            ev_a.record(stream)
+        cache.decode(q[s], out, wl.softmax_scale, max_kv_len=max_len_final)
+        if ev_b is not None:
+            ev_b.record(stream)
+
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(smi_id(device)) as clk:
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i, *attn_ev[i])
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = ev0.elapsed_time(ev1)
+    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    assert int(cache.status.item()) == 0, cache.status.item()
+
+    lens_per_step = [[L0 + args.warmup + i + 1] * B for i in range(args.steps)]
+    kv_tokens = sum(sum(ls) for ls in lens_per_step)
+    bytes_per_step = [attn_bytes(wl, ls, bits) for ls in lens_per_step]
+
+    # ------------------------------------------------------------ end to end through the public API
+    e2e = run_e2e(args, cache, wl, device, L0 + n_steps, max_len_final + args.steps, out)
+
+    res = {
+        "total_ms": total_ms, "attn_ms": attn_ms, "kv_tokens": kv_tokens, "attn_bytes": bytes_per_step,
+        "clocks": clk.summary(), "e2e": e2e, "launches_per_step": 3, "cap": cap,
+    }
+    return res, wl
+
+
+def run_e2e(args, cache, wl, device, L_start, max_len, out_dev):
+    """Same step, with the step's inputs copied host -> device from pinned memory and the
+    attention output copied back, inside the timed region."""
+    import torch
+    B, Hq, H, D = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
+    n = args.steps
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
+    kn, vn, q = step_inputs(wl, L_start, n, device)
+    kh, vh, qh = kn.cpu().pin_memory(), vn.cpu().pin_memory(), q.cpu().pin_memory()
+    out_h = torch.empty((n, B, Hq, D), dtype=torch.float32).pin_memory()
+    kd = torch.empty((B, H, 1, D), dtype=tdt, device=device)
+    vd = torch.empty_like(kd)
+    qd = torch.empty((B, Hq, D), dtype=tdt, device=device)
+    kptr = torch.tensor([kd[b].data_ptr() for b in range(B)], dtype=torch.int64, device=device)
+    vptr = torch.tensor([vd[b].data_ptr() for b in range(B)], dtype=torch.int64, device=device)
+    ones = torch.ones(B, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(n):
+        kd.copy_(kh[s], non_blocking=True)
+        vd.copy_(vh[s], non_blocking=True)
+        qd.copy_(qh[s], non_blocking=True)
+        cache.append_ptrs(kptr, vptr, ones, 1)
+        cache.decode(qd, out_dev, wl.softmax_scale, max_kv_len=max_len)
+        out_h[s].copy_(out_dev, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    kv_tokens = sum(B * (L_start + s + 1) for s in range(n))
+    h2d = (kd.numel() + vd.numel() + qd.numel()) * 2
+    d2h = out_dev.numel() * 4
+    return {"value": kv_tokens / (ms / 1e3), "unit": "KV-tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms / n}
+
+
+# ---------------------------------------------------------------- CPU oracle arm
+def oracle_sample(wl, n_steps, budget_s=20.0):
+    """The oracle on a bounded sample of the workload: one sequence (all kv and query
+    heads) prefilled to the workload's context, then n_steps decode steps of
+    append + attention. Returns (KV-tokens/s, threads, description)."""
+    import oracle
+    oracle.build()
+    L0 = wl.lengths[0]
+    ocfg = oracle.Cfg(bits=wl.bits, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
+                      dtype=oracle.BF16 if wl.dtype == "bf16" else oracle.F16)
+    cap = ((L0 + n_steps + 31) // 32) * 32
+    seq = oracle.SeqCache(ocfg, cap)
+    K, V = wl.kv_seq(0, 0, L0)
+    assert seq.append(K, V) == oracle.OK
+    Kn, Vn = wl.kv_seq(0, L0, n_steps)
+    t0 = time.perf_counter()
+    tokens = 0
+    done = 0
+    for s in range(n_steps):
+        assert seq.append(np.ascontiguousarray(Kn[:, s:s + 1]), np.ascontiguousarray(Vn[:, s:s + 1])) == oracle.OK
+        seq.decode(wl.query(s, 0), wl.softmax_scale)
+        tokens += seq.L
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    desc = (f"oracle (C, fp32 codec + fp64 attention, OpenMP over query heads) on sequence 0 of the workload: "
+            f"prefill {L0} tokens untimed, then {done} timed decode steps of append + attention "
+            f"({wl.num_q_heads} query heads over {wl.num_kv_heads} kv heads)")
+    return tokens / dt, threads, desc, dt
+
+
+# ---------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kivi", choices=["kivi", "reference"])
+    ap.add_argument("--batch", type=int, default=0)
+    ap.add_argument("--context", type=int, default=0)
+    ap.add_argument("--bits", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    wl = workload_spec(args)
+    config = {
+        "workload": (f"Llama-3-8B GQA decode step: {wl.batch} sequences x {wl.lengths[0]} cached tokens, "
+                     f"{wl.num_q_heads} query / {wl.num_kv_heads} kv heads, head_dim {wl.head_dim}, "
+                     f"{wl.bits}-bit KIVI (G=32, R=128), {wl.dtype} inputs"),
+        "batch": wl.batch, "context": wl.lengths[0], "q_heads": wl.num_q_heads, "kv_heads": wl.num_kv_heads,
+        "head_dim": wl.head_dim, "bits": wl.bits, "group": wl.group, "residual": wl.residual,
+        "input_dtype": wl.dtype, "step": "append 1 token/sequence (+ group flush every 32 steps) + decode attention",
+        "l2": "no flush: the packed cache (>1.6 GB) is larger than L2 (129 MB)",
+        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+    }
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        v, threads, desc, dt = oracle_sample(wl, args.warmup + args.steps, budget_s=60.0)
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "KV-tokens/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": v, "unit": "KV-tokens/s", "cores": threads, "kind": "oracle",
+                                 "sample": desc},
+                "e2e": {"value": v, "unit": "KV-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res, wl = run_gpu(args, rank, world, local_rank)
+
+    total_ms = res["total_ms"]
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=torch.device("cuda", local_rank))
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+        e = torch.tensor([res["e2e"]["ms_per_step"]], dtype=torch.float64, device=torch.device("cuda", local_rank))
+        torch.distributed.all_reduce(e, op=torch.distributed.ReduceOp.MAX)
+        res["e2e"]["value"] = res["e2e"]["value"] * res["e2e"]["ms_per_step"] / float(e.item()) * world
+        res["e2e"]["ms_per_step"] = float(e.item())
+    if rank != 0:
+        torch.distributed.destroy_process_group()
+        return
+
+    value = res["kv_tokens"] * world / (total_ms / 1e3)
+    attn_ms = res["attn_ms"]
+    avg_attn_ms = sum(attn_ms) / len(attn_ms)
+    avg_bytes = sum(res["attn_bytes"]) / len(res["attn_bytes"])
+    achieved = avg_bytes / (avg_attn_ms / 1e3) / 1e9
+    peak, peak_kind = measured_hbm_peak()
+    line = {
+        "metric": METRIC, "value": value, "unit": "KV-tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config,
+        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel", "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+                     "algorithmic_bytes_per_launch": avg_bytes, "avg_launch_ms": avg_attn_ms,
+                     "traffic": None},
+        "attn_kv_tokens_per_s": (res["kv_tokens"] / args.steps) / (avg_attn_ms / 1e3),
+        "e2e": {k: res["e2e"][k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")},
+        "gpu_launches": res["launches_per_step"] * args.steps,
+        "clocks": res["clocks"],
+    }
+    if not args.no_cpu_baseline:
+        v, threads, desc, dt = oracle_sample(wl, 4, budget_s=20.0)
+        line["cpu_baseline"] = {"value": v, "unit": "KV-tokens/s", "cores": threads, "kind": "oracle",
+                                "sample": desc}
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

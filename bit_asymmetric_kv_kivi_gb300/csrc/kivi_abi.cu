@@ -1,0 +1,179 @@
+// The extern "C" boundary of the KIVI library: argument validation on the
+// host, sizes and workspace planning, and the launches. Every entry point
+// checks its arguments before anything is enqueued, so an invalid call
+// launches nothing and returns an error code.
+#include <math.h>
+#include <string.h>
+
+#include "kivi_internal.cuh"
+
+namespace {
+
+using kivi::kGroup;
+
+bool cfg_ok(const kivi_cfg* c) {
+    if (c == nullptr) return false;
+    if (c->bits != 2 && c->bits != 4) return false;
+    if (c->group != kGroup) return false;
+    if (c->residual <= 0 || c->residual % kGroup != 0) return false;
+    if (c->head_dim <= 0 || c->head_dim % 32 != 0 || c->head_dim > kivi::kMaxHeadDim) return false;
+    if (c->num_kv_heads <= 0 || c->num_kv_heads > 65535) return false;
+    if (c->num_q_heads <= 0 || c->num_q_heads % c->num_kv_heads != 0) return false;
+    if (c->dtype != KIVI_F16 && c->dtype != KIVI_BF16) return false;
+    return true;
+}
+
+kivi_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KIVI_OK : KIVI_ERR_CUDA; }
+
+kivi_status codec_common(const kivi_cfg* cfg, int32_t n_streams, int32_t n_tokens, const void* x,
+                         uint8_t* codes, uint16_t* scale, uint16_t* zero, kivi::CodecArgs* a) {
+    if (!cfg_ok(cfg)) return KIVI_ERR_ARG;
+    if (n_streams < 0 || n_tokens < 0 || n_streams > 65535) return KIVI_ERR_ARG;
+    if (n_streams > 0 && n_tokens > 0 &&
+        (x == nullptr || codes == nullptr || scale == nullptr || zero == nullptr))
+        return KIVI_ERR_ARG;
+    a->bits = cfg->bits;
+    a->D = cfg->head_dim;
+    a->dtype = cfg->dtype;
+    a->n_streams = n_streams;
+    a->n_tokens = n_tokens;
+    a->x = x;
+    a->codes = codes;
+    a->scale = scale;
+    a->zero = zero;
+    return KIVI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kivi_status kivi_quant_keys(const kivi_cfg* cfg, int32_t n_streams, int32_t n_tokens, const void* x_dev,
+                            uint8_t* codes_dev, uint16_t* scale_dev, uint16_t* zero_dev, void* stream) {
+    kivi::CodecArgs a;
+    const kivi_status st = codec_common(cfg, n_streams, n_tokens, x_dev, codes_dev, scale_dev, zero_dev, &a);
+    if (st != KIVI_OK) return st;
+    if (n_tokens % kGroup != 0) return KIVI_ERR_ARG;
+    return from_cuda(kivi::launch_quant_keys(a, static_cast<cudaStream_t>(stream)));
+}
+
+kivi_status kivi_quant_values(const kivi_cfg* cfg, int32_t n_streams, int32_t n_tokens, const void* x_dev,
+                              uint8_t* codes_dev, uint16_t* scale_dev, uint16_t* zero_dev, void* stream) {
+    kivi::CodecArgs a;
+    const kivi_status st = codec_common(cfg, n_streams, n_tokens, x_dev, codes_dev, scale_dev, zero_dev, &a);
+    if (st != KIVI_OK) return st;
+    return from_cuda(kivi::launch_quant_values(a, static_cast<cudaStream_t>(stream)));
+}
+
+kivi_status kivi_append_flush(const kivi_cfg* cfg, int32_t nseq, const kivi_seq* seqs_dev, int32_t* kv_len_dev,
+                              const void* const* k_new_dev, const void* const* v_new_dev,
+                              const int32_t* n_new_dev, int32_t max_new, int32_t* status_dev, void* stream) {
+    if (!cfg_ok(cfg)) return KIVI_ERR_ARG;
+    if (nseq < 0 || nseq > 65535 || max_new < 0) return KIVI_ERR_ARG;
+    if (nseq == 0) return KIVI_OK;
+    if (seqs_dev == nullptr || kv_len_dev == nullptr || k_new_dev == nullptr || v_new_dev == nullptr ||
+        n_new_dev == nullptr || status_dev == nullptr)
+        return KIVI_ERR_ARG;
+    kivi::AppendArgs a;
+    a.bits = cfg->bits;
+    a.D = cfg->head_dim;
+    a.R = cfg->residual;
+    a.H = cfg->num_kv_heads;
+    a.dtype = cfg->dtype;
+    a.nseq = nseq;
+    a.max_new = max_new;
+    a.seqs = seqs_dev;
+    a.kv_len = kv_len_dev;
+    a.k_new = k_new_dev;
+    a.v_new = v_new_dev;
+    a.n_new = n_new_dev;
+    a.status = status_dev;
+    return from_cuda(kivi::launch_append_flush(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t kivi_decode_workspace_bytes(const kivi_cfg* cfg, int32_t nseq, int32_t max_kv_len) {
+    if (!cfg_ok(cfg) || nseq < 0 || max_kv_len < 0) return 0;
+    int chunk, max_splits;
+    size_t cb, pb;
+    kivi::decode_plan(nseq, cfg->num_kv_heads, cfg->num_q_heads, cfg->head_dim, max_kv_len, &chunk,
+                      &max_splits, &cb, &pb);
+    return cb + pb;
+}
+
+kivi_status kivi_decode_attn(const kivi_cfg* cfg, int32_t nseq, const kivi_seq* seqs_dev,
+                             const int32_t* kv_len_dev, const void* q_dev, float* out_dev, float softmax_scale,
+                             int32_t max_kv_len, void* workspace_dev, size_t workspace_bytes,
+                             int32_t* status_dev, void* stream) {
+    if (!cfg_ok(cfg)) return KIVI_ERR_ARG;
+    if (nseq < 0 || nseq > 65535 || max_kv_len < 0 || !isfinite(softmax_scale)) return KIVI_ERR_ARG;
+    const int g = cfg->num_q_heads / cfg->num_kv_heads;
+    if (cfg->head_dim != 128 || (g != 1 && g != 2 && g != 4 && g != 8)) return KIVI_ERR_UNSUPPORTED;
+    if (nseq == 0) return KIVI_OK;
+    if (seqs_dev == nullptr || kv_len_dev == nullptr || q_dev == nullptr || out_dev == nullptr)
+        return KIVI_ERR_ARG;
+    kivi::DecodeArgs a;
+    size_t cb, pb;
+    kivi::decode_plan(nseq, cfg->num_kv_heads, cfg->num_q_heads, cfg->head_dim, max_kv_len, &a.chunk,
+                      &a.max_splits, &cb, &pb);
+    if (workspace_dev == nullptr || workspace_bytes < cb + pb) return KIVI_ERR_WORKSPACE;
+    a.bits = cfg->bits;
+    a.D = cfg->head_dim;
+    a.R = cfg->residual;
+    a.Hq = cfg->num_q_heads;
+    a.H = cfg->num_kv_heads;
+    a.dtype = cfg->dtype;
+    a.nseq = nseq;
+    a.max_kv_len = max_kv_len;
+    a.seqs = seqs_dev;
+    a.kv_len = kv_len_dev;
+    a.q = q_dev;
+    a.out = out_dev;
+    a.scale_log2 = softmax_scale * 1.4426950408889634f;
+    a.counters = static_cast<int32_t*>(workspace_dev);
+    a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace_dev) + cb);
+    a.status = status_dev;
+    return from_cuda(kivi::launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+kivi_status kivi_seq_buffer_bytes(const kivi_cfg* cfg, int32_t cap_tokens, size_t bytes_out[8]) {
+    if (!cfg_ok(cfg) || cap_tokens < 0 || cap_tokens % kGroup != 0 || bytes_out == nullptr) return KIVI_ERR_ARG;
+    const size_t H = cfg->num_kv_heads, D = cfg->head_dim, cap = cap_tokens;
+    const size_t esz = 2;  // fp16 and bf16
+    const size_t codes = H * cap * D * cfg->bits / 8;
+    const size_t kmeta = H * (cap / kGroup) * D * 2;
+    const size_t vmeta = H * cap * (D / kGroup) * 2;
+    const size_t ring = H * (cfg->residual + kGroup) * D * esz;
+    const size_t sizes[8] = {codes, kmeta, kmeta, codes, vmeta, vmeta, ring, ring};
+    memcpy(bytes_out, sizes, sizeof(sizes));
+    return KIVI_OK;
+}
+
+int64_t kivi_seq_bytes(const kivi_cfg* cfg, int32_t cap_tokens) {
+    size_t b[8];
+    if (kivi_seq_buffer_bytes(cfg, cap_tokens, b) != KIVI_OK) return -1;
+    int64_t total = 0;
+    for (int i = 0; i < 8; ++i) total += static_cast<int64_t>(b[i]);
+    return total;
+}
+
+int64_t kivi_n_packed(const kivi_cfg* cfg, int64_t kv_len) {
+    if (!cfg_ok(cfg) || kv_len < 0) return -1;
+    return kivi::n_packed(kv_len, cfg->residual);
+}
+
+const char* kivi_status_string(int32_t status) {
+    switch (status) {
+        case KIVI_OK: return "ok";
+        case KIVI_ERR_ARG: return "invalid argument or configuration";
+        case KIVI_ERR_UNSUPPORTED: return "configuration not supported by this build";
+        case KIVI_ERR_CAPACITY: return "append exceeds the packed capacity of a sequence";
+        case KIVI_ERR_WORKSPACE: return "workspace missing or too small";
+        case KIVI_ERR_CUDA: return "CUDA launch or runtime error";
+        case KIVI_ERR_LENGTH: return "sequence length or new-token count out of range";
+        default: return "unknown status";
+    }
+}
+
+int32_t kivi_abi_version(void) { return KIVI_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,122 @@
+// Internal declarations shared by the CUDA translation units of the KIVI
+// library: device helpers for the storage formats, the quantizer of one
+// min/max group, and the internal launchers called by the C ABI layer.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kivi.h"
+
+namespace kivi {
+
+constexpr int kGroup = 32;          // G: tokens per key group, channels per value group
+constexpr int kMaxHeadDim = 256;
+
+// ---------------------------------------------------------------- formats
+
+template <int DT>
+__device__ __forceinline__ float widen(uint16_t v) {
+    if constexpr (DT == KIVI_BF16) {
+        return __uint_as_float(static_cast<uint32_t>(v) << 16);
+    } else {
+        return __half2float(__ushort_as_half(v));
+    }
+}
+
+__device__ __forceinline__ float f16_bits_to_float(uint16_t v) {
+    return __half2float(__ushort_as_half(v));
+}
+
+// ---------------------------------------------------------------- quantizer
+
+// Scale and zero of one group from its min and max: s = fp16(fp32(mx - mn) / qmax),
+// z = fp16(mn), both round-to-nearest-even, with one IEEE fp32 subtraction and one
+// IEEE fp32 division. Returns the stored fp16 patterns and their fp32 widening.
+struct GroupParams {
+    uint16_t s16, z16;
+    float s, z;
+};
+
+__device__ __forceinline__ GroupParams group_params(float mn, float mx, int qmax) {
+    const float s32 = __fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(qmax));
+    const __half hs = __float2half_rn(s32);
+    const __half hz = __float2half_rn(mn);
+    GroupParams p;
+    p.s16 = __half_as_ushort(hs);
+    p.z16 = __half_as_ushort(hz);
+    p.s = __half2float(hs);
+    p.z = __half2float(hz);
+    return p;
+}
+
+// Code of one element: clamp(rint((x - z) / s), 0, qmax), IEEE fp32 subtraction and
+// division, round half to even; 0 when s == 0.
+__device__ __forceinline__ uint32_t encode(float x, float z, float s, int qmax) {
+    if (s == 0.0f) return 0u;
+    float t = rintf(__fdiv_rn(__fsub_rn(x, z), s));
+    t = fminf(fmaxf(t, 0.0f), static_cast<float>(qmax));
+    return static_cast<uint32_t>(t);
+}
+
+// ---------------------------------------------------------------- cache state
+
+__host__ __device__ __forceinline__ int64_t n_packed(int64_t L, int R) {
+    const int64_t over = L - R;
+    return over <= 0 ? 0 : (over / kGroup) * kGroup;
+}
+
+__device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
+    if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+// ---------------------------------------------------------------- launchers
+
+struct CodecArgs {
+    int bits, D, dtype;
+    int n_streams, n_tokens;
+    const void* x;
+    uint8_t* codes;
+    uint16_t* scale;
+    uint16_t* zero;
+};
+
+cudaError_t launch_quant_keys(const CodecArgs& a, cudaStream_t stream);
+cudaError_t launch_quant_values(const CodecArgs& a, cudaStream_t stream);
+
+struct AppendArgs {
+    int bits, D, R, H, dtype;
+    int nseq, max_new;
+    const kivi_seq* seqs;
+    int32_t* kv_len;
+    const void* const* k_new;
+    const void* const* v_new;
+    const int32_t* n_new;
+    int32_t* status;
+};
+
+cudaError_t launch_append_flush(const AppendArgs& a, cudaStream_t stream);
+
+struct DecodeArgs {
+    int bits, D, R, Hq, H, dtype;
+    int nseq, max_kv_len;
+    int chunk, max_splits;          // tokens per split (multiple of 32), splits per sequence
+    const kivi_seq* seqs;
+    const int32_t* kv_len;
+    const void* q;
+    float* out;
+    float scale_log2;               // softmax_scale * log2(e)
+    int32_t* counters;              // [nseq][H] split tickets (workspace)
+    float* partials;                // [nseq][Hq][max_splits][D + 4] (workspace)
+    int32_t* status;
+};
+
+// Split policy and workspace layout shared by kivi_decode_workspace_bytes and the launch.
+void decode_plan(int nseq, int H, int Hq, int D, int max_kv_len, int* chunk, int* max_splits,
+                 size_t* counter_bytes, size_t* partial_bytes);
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+}  // namespace kivi

@@ -1,0 +1,97 @@
+"""The C-ABI library on a host without a GPU: it loads, exports every symbol that
+include/kivi.h declares, and its host-only logic (sizes, n_packed, argument
+validation, status strings) behaves as documented. No compute call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_asymmetric_kv_kivi_gb300 as kivi
+from bit_asymmetric_kv_kivi_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "kivi.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return kivi.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kivi_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "kivi_decode_attn" in names and len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    assert lib.kivi_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert kivi.status_string(s) and kivi.status_string(s) != "unknown status"
+    assert kivi.status_string(99) == "unknown status"
+
+
+def test_seq_bytes_and_n_packed(lib):
+    import oracle
+    for bits in (2, 4):
+        for dt in (kivi.F16, kivi.BF16):
+            cfg = kivi.Config(bits=bits, num_q_heads=32, num_kv_heads=8, dtype=dt)
+            ocfg = oracle.Cfg(bits=bits, num_q_heads=32, num_kv_heads=8, dtype=dt)
+            for cap in (0, 32, 4096, 32768):
+                assert cfg.seq_bytes(cap) == oracle.seq_bytes(ocfg, cap)
+                assert sum(cfg.seq_buffer_bytes(cap)) == cfg.seq_bytes(cap)
+            for L in (0, 1, 127, 128, 159, 160, 161, 1024, 16384 + 511):
+                assert cfg.n_packed(L) == oracle.n_packed(ocfg, L)
+    assert kivi.Config(group=16).seq_bytes(64) == -1
+    assert kivi.Config().n_packed(-1) == -1
+
+
+@pytest.mark.parametrize("bad", [dict(bits=3), dict(group=64), dict(residual=100), dict(head_dim=96 + 1),
+                                 dict(head_dim=512), dict(num_q_heads=6, num_kv_heads=4), dict(dtype=7),
+                                 dict(residual=0), dict(num_kv_heads=0)])
+def test_bad_config_rejected_before_launch(lib, bad):
+    cfg = kivi.Config(**bad).c()
+    P = ctypes.c_void_p
+    one = P(16)
+    assert lib.kivi_quant_keys(cfg, 1, 32, one, one, one, one, None) == kivi.ERR_ARG
+    assert lib.kivi_quant_values(cfg, 1, 32, one, one, one, one, None) == kivi.ERR_ARG
+    assert lib.kivi_append_flush(cfg, 1, one, one, one, one, one, 1, one, None) == kivi.ERR_ARG
+    assert lib.kivi_decode_attn(cfg, 1, one, one, one, one, 0.1, 10, one, 1 << 20, one, None) == kivi.ERR_ARG
+    assert lib.kivi_decode_workspace_bytes(cfg, 1, 100) == 0
+
+
+def test_bad_arguments_rejected_before_launch(lib):
+    cfg = kivi.Config(num_q_heads=4, num_kv_heads=1).c()
+    P = ctypes.c_void_p
+    one, null = P(16), None
+    # NULL pointers, negative sizes, tokens not a multiple of G
+    assert lib.kivi_quant_keys(cfg, 1, 32, null, one, one, one, None) == kivi.ERR_ARG
+    assert lib.kivi_quant_keys(cfg, 1, 48, one, one, one, one, None) == kivi.ERR_ARG
+    assert lib.kivi_quant_values(cfg, -1, 32, one, one, one, one, None) == kivi.ERR_ARG
+    assert lib.kivi_append_flush(cfg, 2, null, one, one, one, one, 1, one, None) == kivi.ERR_ARG
+    assert lib.kivi_append_flush(cfg, 2, one, one, one, one, one, -1, one, None) == kivi.ERR_ARG
+    assert lib.kivi_append_flush(cfg, 2, one, one, one, one, one, 1, null, None) == kivi.ERR_ARG
+    assert lib.kivi_decode_attn(cfg, 2, one, one, null, one, 0.1, 10, one, 1 << 20, one, None) == kivi.ERR_ARG
+    assert lib.kivi_decode_attn(cfg, 2, one, one, one, one, float("nan"), 10, one, 1 << 20, one, None) == kivi.ERR_ARG
+    # workspace too small
+    need = lib.kivi_decode_workspace_bytes(cfg, 2, 5000)
+    assert need > 0
+    assert lib.kivi_decode_attn(cfg, 2, one, one, one, one, 0.1, 5000, one, need - 1, one, None) == kivi.ERR_WORKSPACE
+    assert lib.kivi_decode_attn(cfg, 2, one, one, one, one, 0.1, 5000, null, need, one, None) == kivi.ERR_WORKSPACE
+    # decode supports head_dim 128 and Hq/Hkv in {1, 2, 4, 8} only
+    assert lib.kivi_decode_attn(kivi.Config(head_dim=64).c(), 1, one, one, one, one, 0.1, 10, one, 1 << 20,
+                                one, None) == kivi.ERR_UNSUPPORTED
+    assert lib.kivi_decode_attn(kivi.Config(num_q_heads=3).c(), 1, one, one, one, one, 0.1, 10, one, 1 << 20,
+                                one, None) == kivi.ERR_UNSUPPORTED
+    # zero-sized calls are no-ops that touch nothing
+    assert lib.kivi_quant_keys(cfg, 0, 32, null, null, null, null, None) == kivi.OK
+    assert lib.kivi_append_flush(cfg, 0, null, null, null, null, null, 0, null, None) == kivi.OK
+    assert lib.kivi_decode_attn(cfg, 0, null, null, null, null, 0.1, 0, null, 0, null, None) == kivi.OK

@@ -1,0 +1,82 @@
+"""GPU parity of the codec entry points (kivi_quant_keys, kivi_quant_values):
+codes, scales and zeros bit-exact against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import bit_asymmetric_kv_kivi_gb300 as kivi
+import oracle
+from gpu_util import configs, dev_tensor, host_bits
+from synth import to_dtype_bits
+from test_oracle_codec import planted_codes
+
+pytestmark = pytest.mark.gpu
+
+
+def structured(rng, S, T, D, dtype):
+    x = rng.standard_normal((S, T, D))
+    x[:, :, rng.choice(D, max(1, D // 32), replace=False)] *= 20.0
+    x[:, rng.random(T) < 0.05, :] *= 10.0
+    x[0, :3, :] = 0.0                       # exact zeros
+    x[-1, 5, :] = 1.5                       # a constant value row (value groups with s = 0)
+    return to_dtype_bits(x, dtype)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
+def test_quant_keys_bitexact(bits, dtype, D):
+    rng = np.random.default_rng(100 + bits + D)
+    S, T = 3, 160
+    kcfg, ocfg = configs(bits, dtype, 1, 1, D)
+    xb = structured(rng, S, T, D, dtype)
+    xb[1, 32:64, :] = xb[1, 32, :]          # a group of identical tokens: every channel constant
+    codes, scale, zero = kivi.quant_keys(kcfg, dev_tensor(xb, dtype))
+    rc, rs, rz = oracle.quant_keys(ocfg, xb)
+    np.testing.assert_array_equal(codes.cpu().numpy(), rc)
+    np.testing.assert_array_equal(host_bits(scale), rs)
+    np.testing.assert_array_equal(host_bits(zero), rz)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("D,T", [(32, 1), (64, 45), (128, 97), (256, 33)])
+def test_quant_values_bitexact(bits, dtype, D, T):
+    rng = np.random.default_rng(200 + bits + D)
+    S = 4
+    kcfg, ocfg = configs(bits, dtype, 1, 1, D)
+    xb = structured(rng, S, max(T, 6), D, dtype)[:, :T].copy()
+    codes, scale, zero = kivi.quant_values(kcfg, dev_tensor(xb, dtype))
+    rc, rs, rz = oracle.quant_values(ocfg, xb)
+    np.testing.assert_array_equal(codes.cpu().numpy(), rc)
+    np.testing.assert_array_equal(host_bits(scale), rs)
+    np.testing.assert_array_equal(host_bits(zero), rz)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_planted_grid_recovered_exactly(bits):
+    """x = z + c*s on exact grids: the kernel must return (c, s, z) themselves."""
+    rng = np.random.default_rng(300 + bits)
+    S, T, D, G = 2, 64, 128, 32
+    qmax = (1 << bits) - 1
+    kcfg, _ = configs(bits, "f16", 1, 1, D)
+    s = np.ldexp(1.0, rng.integers(-6, 3, size=(S, T // G, D)))
+    z = rng.integers(-48, 48, size=s.shape) * s
+    c = planted_codes(rng, (S, T // G, G, D), qmax, axis=2).reshape(S, T, D)
+    x = np.repeat(z, G, axis=1) + c * np.repeat(s, G, axis=1)
+    codes, scale, zero = kivi.quant_keys(kcfg, dev_tensor(to_dtype_bits(x, "f16"), "f16"))
+    d = np.arange(D)
+    got_c = (codes.cpu().numpy()[..., (d * bits) // 8].astype(np.int64) >> ((d * bits) % 8)) & qmax
+    np.testing.assert_array_equal(got_c, c)
+    np.testing.assert_array_equal(host_bits(scale).view(np.float16).astype(np.float64), s)
+    np.testing.assert_array_equal(host_bits(zero).view(np.float16).astype(np.float64), z)
+
+
+def test_empty_inputs_are_noops():
+    kcfg, _ = configs(2, "f16", 1, 1, 128)
+    x = torch.empty((0, 32, 128), dtype=torch.float16, device="cuda")
+    codes, scale, zero = kivi.quant_keys(kcfg, x)
+    assert codes.numel() == 0
+    x = torch.empty((2, 0, 128), dtype=torch.float16, device="cuda")
+    codes, scale, zero = kivi.quant_values(kcfg, x)
+    assert codes.numel() == 0

@@ -1,0 +1,130 @@
+"""GPU parity of kivi_decode_attn against the oracle's fp64 attention over the
+same cache: max |out - oracle| <= 2e-3 over every output element, for both code
+widths, both dtypes, GQA groups 1/2/4/8, the length edge cases of the packed /
+residual split, varlen batches and the split-K combine."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import bit_asymmetric_kv_kivi_gb300 as kivi
+import oracle
+import synth
+from gpu_util import ATTN_TOL, assert_state_equal, configs, dev_tensor
+
+pytestmark = pytest.mark.gpu
+
+
+def build(wl: synth.Workload, bits: int, cap: int):
+    """Library and oracle caches of workload `wl` (every sequence prefilled to its length)."""
+    kcfg, ocfg = configs(bits, wl.dtype, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.residual)
+    cache = kivi.KVCache(kcfg, wl.batch, cap)
+    refs, ks, vs = [], [], []
+    for b in range(wl.batch):
+        K, V = wl.kv_seq(b, 0, wl.lengths[b])
+        ks.append(dev_tensor(K, wl.dtype))
+        vs.append(dev_tensor(V, wl.dtype))
+        r = oracle.SeqCache(ocfg, cap)
+        assert r.append(K, V) == oracle.OK
+        refs.append(r)
+    cache.append(ks, vs)
+    return cache, refs
+
+
+def check_decode(wl, cache, refs, step=0, max_kv_len=None, heads=None):
+    q = wl.query(step)
+    out = cache.decode(dev_tensor(q, wl.dtype), softmax_scale=wl.softmax_scale, max_kv_len=max_kv_len)
+    out = out.cpu().numpy()
+    assert int(cache.status.item()) == 0
+    worst = 0.0
+    for b, r in enumerate(refs):
+        if heads is None:
+            want = r.decode(q[b], wl.softmax_scale)
+            err = np.max(np.abs(out[b] - want))
+        else:
+            want = r.decode(q[b], wl.softmax_scale, heads[0], heads[1])
+            err = np.max(np.abs(out[b, heads[0]:heads[0] + heads[1]] - want[heads[0]:heads[0] + heads[1]]))
+        worst = max(worst, float(err))
+    assert worst <= ATTN_TOL, worst
+    return out, worst
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+def test_decode_edge_lengths(bits, dtype, g):
+    """One batch holding the edge lengths of the packed/residual split."""
+    lengths = (1, 5, 31, 32, 33, 127, 128, 129, 159, 160, 161, 191, 300, 1000)
+    H = 2
+    wl = synth.Workload("edges", len(lengths), H * g, H, 128, lengths, dtype, bits=bits,
+                        seed=500 + g + bits)
+    cache, refs = build(wl, bits, 1024)
+    for b, r in enumerate(refs):
+        assert_state_equal(cache, b, r)
+    check_decode(wl, cache, refs)
+
+
+def test_decode_empty_sequence_gives_zeros():
+    wl = synth.Workload("empty", 3, 4, 2, 128, (0, 200, 0), "f16", seed=7)
+    cache, refs = build(wl, 2, 256)
+    out, _ = check_decode(wl, cache, refs)
+    assert np.all(out[0] == 0) and np.all(out[2] == 0)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_split_count_invariance(dtype):
+    """The split size follows max_kv_len; one split and many splits agree to 1e-5."""
+    wl = synth.Workload("splits", 2, 8, 2, 128, (9000, 5000), dtype, seed=8)
+    cache, refs = build(wl, 2, 9024)
+    a, _ = check_decode(wl, cache, refs, max_kv_len=9000)          # several splits
+    b, _ = check_decode(wl, cache, refs, max_kv_len=400000)        # 8192-token splits
+    c, _ = check_decode(wl, cache, refs, max_kv_len=4096 + 9000)   # another split size
+    assert np.max(np.abs(a - b)) <= 1e-5 and np.max(np.abs(a - c)) <= 1e-5
+
+
+def test_gqa_equals_repeated_mha():
+    """Hq/Hkv = 4 over a cache equals MHA over the same cache with each kv head repeated 4 times."""
+    wl = synth.Workload("gqa", 2, 8, 2, 128, (700, 450), "f16", seed=9)
+    cache, refs = build(wl, 2, 640)
+    q = dev_tensor(wl.query(0), "f16")
+    out_gqa = cache.decode(q, softmax_scale=wl.softmax_scale)
+    kcfg = kivi.Config(bits=2, num_q_heads=8, num_kv_heads=8, dtype=kivi.F16)
+    mha = kivi.KVCache(kcfg, 2, 640)
+    ks, vs = [], []
+    for b in range(2):
+        K, V = wl.kv_seq(b, 0, wl.lengths[b])
+        ks.append(dev_tensor(np.repeat(K, 4, axis=0), "f16"))
+        vs.append(dev_tensor(np.repeat(V, 4, axis=0), "f16"))
+    mha.append(ks, vs)
+    out_mha = mha.decode(q, softmax_scale=wl.softmax_scale)
+    assert torch.equal(out_gqa, out_mha)
+
+
+def test_bad_length_gives_nan_and_status():
+    wl = synth.Workload("bad", 2, 2, 1, 128, (300, 100), "f16", seed=10)
+    cache, refs = build(wl, 2, 256)
+    q = dev_tensor(wl.query(0), "f16")
+    out = cache.decode(q, softmax_scale=wl.softmax_scale, max_kv_len=200).cpu().numpy()
+    assert int(cache.status.item()) == kivi.ERR_LENGTH
+    assert np.all(np.isnan(out[0]))
+    want = refs[1].decode(wl.query(0)[1], wl.softmax_scale)
+    assert np.max(np.abs(out[1] - want)) <= ATTN_TOL
+
+
+def test_workload_tiny_decode():
+    """Workload 0 (one sequence, one head, 1024 tokens: 28 key groups + 128 residual)."""
+    wl = synth.workload(0)
+    cache, refs = build(wl, 2, 1024)
+    assert oracle.n_packed(refs[0].cfg, 1024) == 896
+    assert_state_equal(cache, 0, refs[0])
+    check_decode(wl, cache, refs)
+
+
+def test_workload_llama2_7b_mha():
+    """Workload 1 at full size: 8 sequences, 32 heads (MHA), 4096 tokens, fp16."""
+    wl = synth.workload(1)
+    cache, refs = build(wl, 2, 4096)
+    for b in (0, 7):
+        assert_state_equal(cache, b, refs[b])
+    check_decode(wl, cache, refs)
