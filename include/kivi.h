@@ -18,7 +18,8 @@
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream). All work is enqueued on it; no entry point synchronizes, and
  *    the library allocates no device memory, keeps no global state between
- *    calls and is safe to call from several host threads.
+ *    calls and is safe to call from several host threads (the one exception,
+ *    kivi_decode_attn_static, is described at its declaration).
  *  - Argument errors are found on the host before anything is launched and
  *    returned synchronously (KIVI_ERR_ARG, KIVI_ERR_UNSUPPORTED,
  *    KIVI_ERR_WORKSPACE). A failed launch returns KIVI_ERR_CUDA.
@@ -198,6 +199,32 @@ kivi_status kivi_decode_attn(const kivi_cfg* cfg, int32_t nseq, const kivi_seq* 
 
 /* Workspace bytes kivi_decode_attn needs for (nseq, max_kv_len); 0 on a bad config. */
 size_t kivi_decode_workspace_bytes(const kivi_cfg* cfg, int32_t nseq, int32_t max_kv_len);
+
+/*
+ * Decode attention that allocates nothing and takes no workspace argument.
+ * The pages that describe KIVI have no counterpart of this entry point; it
+ * exists for callers that cannot call cudaMalloc: processes whose device
+ * memory is already reserved by another allocator (a serving framework's
+ * memory pool), latency-critical paths that must not allocate or free
+ * (cudaFree synchronizes the whole device), and plugin hosts whose interface
+ * passes only input and output buffers.
+ * Same arguments, results and errors as kivi_decode_attn, except that the
+ * workspace is a fixed array of KIVI_STATIC_WORKSPACE_BYTES bytes in the
+ * library's own device memory: every GPU that loads the library holds it
+ * until the process exits. Calls whose kivi_decode_workspace_bytes(cfg, nseq,
+ * max_kv_len) exceeds that size return KIVI_ERR_WORKSPACE and launch nothing.
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any stream
+ * capture. The entry point calls no cudaMalloc, cudaFree or other allocating
+ * routine. All calls on a device share the array: each call clears the part
+ * that must start at zero (with an asynchronous memset on `stream`), and calls
+ * that overlap on the GPU race and give wrong results.
+ */
+#define KIVI_STATIC_WORKSPACE_BYTES (16u << 20)
+kivi_status kivi_decode_attn_static(const kivi_cfg* cfg, int32_t nseq, const kivi_seq* seqs_dev,
+                                    const int32_t* kv_len_dev, const void* q_dev, float* out_dev,
+                                    float softmax_scale, int32_t max_kv_len, int32_t* status_dev,
+                                    void* stream);
 
 /* ---------------------------------------------------------------- sizes and helpers */
 
