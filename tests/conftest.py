@@ -18,3 +18,14 @@ def oracle_lib():
     import oracle
     oracle.build()
     return oracle
+
+
+def pytest_terminal_summary(terminalreporter):
+    try:
+        from gpu_util import ERRORS
+    except Exception:
+        return
+    if ERRORS:
+        terminalreporter.write_line("max |out - oracle| per attention test:")
+        for k, v in sorted(ERRORS.items()):
+            terminalreporter.write_line(f"  {v:.3e}  {k}")

@@ -10,6 +10,13 @@ TORCH_DT = {"f16": torch.float16, "bf16": torch.bfloat16}
 KIVI_DT = {"f16": kivi.F16, "bf16": kivi.BF16}
 ORC_DT = {"f16": oracle.F16, "bf16": oracle.BF16}
 ATTN_TOL = 2e-3   # max |out - oracle| over every output element (fp32 accumulation vs fp64)
+ERRORS: dict = {}  # test id -> largest attention error seen (printed in the terminal summary)
+
+
+def record_error(err: float) -> None:
+    import os
+    name = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    ERRORS[name] = max(ERRORS.get(name, 0.0), float(err))
 
 
 def dev_tensor(bits: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:

@@ -11,7 +11,7 @@ import torch
 import bit_asymmetric_kv_kivi_gb300 as kivi
 import oracle
 import synth
-from gpu_util import ATTN_TOL, assert_state_equal, configs, dev_tensor
+from gpu_util import ATTN_TOL, assert_state_equal, configs, dev_tensor, record_error
 
 pytestmark = pytest.mark.gpu
 
@@ -46,6 +46,7 @@ def check_decode(wl, cache, refs, step=0, max_kv_len=None, heads=None):
             want = r.decode(q[b], wl.softmax_scale, heads[0], heads[1])
             err = np.max(np.abs(out[b, heads[0]:heads[0] + heads[1]] - want[heads[0]:heads[0] + heads[1]]))
         worst = max(worst, float(err))
+    record_error(worst)
     assert worst <= ATTN_TOL, worst
     return out, worst
 
@@ -74,13 +75,16 @@ def test_decode_empty_sequence_gives_zeros():
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_split_count_invariance(dtype):
-    """The split size follows max_kv_len; one split and many splits agree to 1e-5."""
+    """The split size follows max_kv_len; different split counts agree to 1e-4. (The
+    tensor-core path carries ~22 bits on normal f16 hi+lo operands with an absolute
+    floor of 2^-25 on subnormal low parts; each split's running max changes which
+    terms sit at that floor.)"""
     wl = synth.Workload("splits", 2, 8, 2, 128, (9000, 5000), dtype, seed=8)
     cache, refs = build(wl, 2, 9024)
     a, _ = check_decode(wl, cache, refs, max_kv_len=9000)          # several splits
     b, _ = check_decode(wl, cache, refs, max_kv_len=400000)        # 8192-token splits
     c, _ = check_decode(wl, cache, refs, max_kv_len=4096 + 9000)   # another split size
-    assert np.max(np.abs(a - b)) <= 1e-5 and np.max(np.abs(a - c)) <= 1e-5
+    assert np.max(np.abs(a - b)) <= 1e-4 and np.max(np.abs(a - c)) <= 1e-4
 
 
 def test_gqa_equals_repeated_mha():
@@ -98,7 +102,8 @@ def test_gqa_equals_repeated_mha():
         vs.append(dev_tensor(np.repeat(V, 4, axis=0), "f16"))
     mha.append(ks, vs)
     out_mha = mha.decode(q, softmax_scale=wl.softmax_scale)
-    assert torch.equal(out_gqa, out_mha)
+    # the same arithmetic per head, up to the power-of-two q prescale chosen per CTA
+    assert float((out_gqa - out_mha).abs().max()) <= 2e-5
 
 
 def test_bad_length_gives_nan_and_status():
