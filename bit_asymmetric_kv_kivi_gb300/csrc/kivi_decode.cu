@@ -430,8 +430,11 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
 template <int BITS>
 struct MmaLayout {
     static constexpr int kRowBytes = kD * BITS / 8;                      // packed row: 32 or 64 bytes
-    static constexpr int kStage = 2 * kGroup * kRowBytes + 4 * 256;      // kc, vc, ks, kz, vs, vz
-    static constexpr int kChunks = kStage / 16;                          // 16-byte cp.async pieces
+    // kc, vc, ks, kz, vs, vz; each 64-byte channel span of ks and kz is padded to 80 bytes so
+    // that the four spans read together fall on distinct shared-memory banks
+    static constexpr int kMetaPad = 320;
+    static constexpr int kStage = 2 * kGroup * kRowBytes + 2 * kMetaPad + 2 * 256;
+    static constexpr int kChunks = (2 * kGroup * kRowBytes + 4 * 256) / 16;   // 16-byte cp.async pieces
     static constexpr int kNslot = 16 / BITS;                             // code pairs per 32-bit word
     static constexpr int kStageBytes = kWarps * kStages * kStage;
     static constexpr int kSmemBytes(int gq) {
@@ -573,18 +576,24 @@ __global__ void __launch_bounds__(kThreads, BITS == 2 ? 3 : 2) decode_mma_kernel
         for (int k = 0; k < Lay::kChunks / 32; ++k) {
             const int c = lane + 32 * k;
             const unsigned char* src;
+            int d;
             if (c < 2 * RB) {
                 src = kc_base + j * kGroup * RB + c * 16;
+                d = c * 16;
             } else if (c < 4 * RB) {
                 src = vc_base + j * kGroup * RB + (c - 2 * RB) * 16;
+                d = c * 16;
             } else {
                 const int r = c - 4 * RB, reg = r >> 4, off = (r & 15) * 16;
                 src = reg == 0 ? ks_base + j * 256 + off
                     : reg == 1 ? kz_base + j * 256 + off
                     : reg == 2 ? vs_base + j * 256 + off
                                : vz_base + j * 256 + off;
+                d = 2 * kGroup * RB +
+                    (reg < 2 ? reg * Lay::kMetaPad + (off >> 6) * 80 + (off & 63)
+                             : 2 * Lay::kMetaPad + (reg - 2) * 256 + off);
             }
-            cp_async16(dst + c * 16, src);
+            cp_async16(dst + d, src);
         }
     };
 
@@ -606,8 +615,8 @@ __global__ void __launch_bounds__(kThreads, BITS == 2 ? 3 : 2) decode_mma_kernel
         const unsigned char* kc = st;
         const unsigned char* vc = st + kGroup * RB;
         const unsigned char* ksm = st + 2 * kGroup * RB;
-        const unsigned char* kzm = ksm + 256;
-        const unsigned char* vsm = kzm + 256;    // [32 tokens][4] fp16
+        const unsigned char* kzm = ksm + Lay::kMetaPad;
+        const unsigned char* vsm = kzm + Lay::kMetaPad;    // [32 tokens][4] fp16
         const unsigned char* vzm = vsm + 256;
 
         // ---- key scale / zero pairs of this thread's span
@@ -616,8 +625,8 @@ __global__ void __launch_bounds__(kThreads, BITS == 2 ? 3 : 2) decode_mma_kernel
             uint32_t R[16], Z[16];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const uint4 r4 = *reinterpret_cast<const uint4*>(ksm + 64 * t + 16 * i);
-                const uint4 z4 = *reinterpret_cast<const uint4*>(kzm + 64 * t + 16 * i);
+                const uint4 r4 = *reinterpret_cast<const uint4*>(ksm + 80 * t + 16 * i);
+                const uint4 z4 = *reinterpret_cast<const uint4*>(kzm + 80 * t + 16 * i);
                 R[4 * i] = r4.x; R[4 * i + 1] = r4.y; R[4 * i + 2] = r4.z; R[4 * i + 3] = r4.w;
                 Z[4 * i] = z4.x; Z[4 * i + 1] = z4.y; Z[4 * i + 2] = z4.z; Z[4 * i + 3] = z4.w;
             }
@@ -707,7 +716,9 @@ a0 = code_slot<BITS>(cw[0][w0], cws[0][w0], s0);
         for (int r = 0; r < 4; ++r) p[r] = t < GQ ? exp2f(S[r] - m_run) : 0.0f;
         l_run += (p[0] + p[1]) + (p[2] + p[3]);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) pt[t * kPtLd + gid + 8 * r] = p[r];
+        // token 8r + j goes to column 8r + 2 (j % 4) + j / 4: the value side pairs tokens
+        // (8r + t', 8r + t' + 4), which then sit side by side
+        for (int r = 0; r < 4; ++r) pt[t * kPtLd + 8 * r + 2 * (gid & 3) + (gid >> 2)] = p[r];
         __syncwarp();
 
         // ---- value side B operands: P' = p * s_v (hi / lo), and p (hi / lo) for the z_v term
@@ -716,15 +727,15 @@ a0 = code_slot<BITS>(cw[0][w0], cws[0][w0], s0);
         for (int k2 = 0; k2 < 2; ++k2) {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const int tau0 = 16 * k2 + 2 * t + 8 * e;
-                const float2 pp = hv ? *reinterpret_cast<const float2*>(pt + (hv ? hh : 0) * kPtLd + tau0)
+                const int tau0 = 16 * k2 + 8 * e + t;      // pair (tau0, tau0 + 4)
+                const float2 pp = hv ? *reinterpret_cast<const float2*>(pt + (hv ? hh : 0) * kPtLd + 16 * k2 + 8 * e + 2 * t)
                                      : make_float2(0.0f, 0.0f);
                 const uint32_t ph = pack_h2(pp.x, pp.y);
                 const uint32_t pl = pack_h2(pp.x - h2_lo(ph), pp.y - h2_hi(ph));
                 const uint32_t xp = part ? pl : 0u, zn = part ? (ph ^ 0x80008000u) : 0u;
                 bp[k2][e] = part ? pl : ph;
                 const uint2 s0w = *reinterpret_cast<const uint2*>(vsm + tau0 * 8);
-                const uint2 s1w = *reinterpret_cast<const uint2*>(vsm + (tau0 + 1) * 8);
+                const uint2 s1w = *reinterpret_cast<const uint2*>(vsm + (tau0 + 4) * 8);
 #pragma unroll
                 for (int kg = 0; kg < 4; ++kg) {
                     const uint32_t a_w = kg < 2 ? s0w.x : s0w.y, b_w = kg < 2 ? s1w.x : s1w.y;
@@ -732,7 +743,7 @@ a0 = code_slot<BITS>(cw[0][w0], cws[0][w0], s0);
                     vb[k2][e][kg] = hfma2(xp, svp, hfma2(ph, svp, hmul2(zn, svp)));
                 }
                 const uint32_t zw0 = *reinterpret_cast<const uint32_t*>(vzm + tau0 * 8 + 4 * ((gid & 3) >> 1));
-                const uint32_t zw1 = *reinterpret_cast<const uint32_t*>(vzm + (tau0 + 1) * 8 + 4 * ((gid & 3) >> 1));
+                const uint32_t zw1 = *reinterpret_cast<const uint32_t*>(vzm + (tau0 + 4) * 8 + 4 * ((gid & 3) >> 1));
                 za[k2][e] = gid < 4 ? prmt(zw0, zw1, sel_z) : 0u;
             }
         }
@@ -747,10 +758,10 @@ a0 = code_slot<BITS>(cw[0][w0], cws[0][w0], s0);
                 uint32_t wv[2], wvs[2];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const int tau0 = 16 * k2 + 2 * t + 8 * e;
+                    const int tau0 = 16 * k2 + 8 * e + t;
                     const int off = kg * (RB / 4) + vbyte;
                     const uint32_t x0 = *reinterpret_cast<const uint32_t*>(vc + tau0 * RB + off);
-                    const uint32_t x1 = *reinterpret_cast<const uint32_t*>(vc + (tau0 + 1) * RB + off);
+                    const uint32_t x1 = *reinterpret_cast<const uint32_t*>(vc + (tau0 + 4) * RB + off);
                     wv[e] = prmt(x0, x1, sel_v);
                     wvs[e] = wv[e] >> SHIFT;
                 }
