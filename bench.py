@@ -75,6 +75,22 @@ def attn_bytes(wl, lengths, bits):
     return total
 
 
+def reduce_max(x: float, device=None) -> float:
+    """Max of x over the ranks of the default process group (x itself without one)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, max_ms: float) -> float:
+    """Whole-job rate under weak scaling: every rank processed units_per_rank in at most max_ms."""
+    return units_per_rank * world / (max_ms / 1e3)
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
 
@@ -283,7 +299,7 @@ def run_e2e(args, cache, wl, device, L_start, max_len, out_dev):
     h2d = (kd.numel() + vd.numel() + qd.numel()) * 2
     d2h = out_dev.numel() * 4
     return {"value": kv_tokens / (ms / 1e3), "unit": "KV-tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms / n}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms / n, "kv_tokens": kv_tokens, "steps": n}
 
 
 # ---------------------------------------------------------------- CPU oracle arm
@@ -352,7 +368,7 @@ def main():
             return
         v, threads, desc, dt = oracle_sample(wl, args.warmup + args.steps, budget_s=60.0)
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "KV-tokens/s", "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / (args.warmup + args.steps), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
                 "cpu_baseline": {"value": v, "unit": "KV-tokens/s", "cores": threads, "kind": "oracle",
                                  "sample": desc},
@@ -365,20 +381,15 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     res, wl = run_gpu(args, rank, world, local_rank)
 
-    total_ms = res["total_ms"]
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=torch.device("cuda", local_rank))
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-        e = torch.tensor([res["e2e"]["ms_per_step"]], dtype=torch.float64, device=torch.device("cuda", local_rank))
-        torch.distributed.all_reduce(e, op=torch.distributed.ReduceOp.MAX)
-        res["e2e"]["value"] = res["e2e"]["value"] * res["e2e"]["ms_per_step"] / float(e.item()) * world
-        res["e2e"]["ms_per_step"] = float(e.item())
+    dev = torch.device("cuda", local_rank)
+    total_ms = reduce_max(res["total_ms"], dev)
+    e2e_ms = reduce_max(res["e2e"]["ms_per_step"], dev)
+    res["e2e"]["value"] = job_throughput(res["e2e"]["kv_tokens"], world, e2e_ms * res["e2e"]["steps"])
     if rank != 0:
         torch.distributed.destroy_process_group()
         return
 
-    value = res["kv_tokens"] * world / (total_ms / 1e3)
+    value = job_throughput(res["kv_tokens"], world, total_ms)
     attn_ms = res["attn_ms"]
     avg_attn_ms = sum(attn_ms) / len(attn_ms)
     avg_bytes = sum(res["attn_bytes"]) / len(res["attn_bytes"])

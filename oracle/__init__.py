@@ -24,6 +24,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kivi_oracle.c")
 _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "libkivi_oracle.so")
+# A test may point the wrapper at a deliberately broken build of the oracle (a
+# "mutant") to check that the pins catch the mistake; nothing else sets this.
+_LIB_OVERRIDE = os.environ.get("KIVI_ORACLE_LIB")
 _CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
            "-shared", "-fPIC", "-Wall", "-Wno-unused-function"]
 
@@ -34,8 +37,16 @@ _lock = threading.Lock()
 _lib = None
 
 
+def compile_source(src: str, out: str) -> str:
+    """Compile a C source with the oracle's flags into a shared library at `out`."""
+    subprocess.run(["gcc", *_CFLAGS, src, "-o", out, "-lm"], check=True)
+    return out
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc into oracle/_build/ (rebuilt when the source is newer)."""
+    if _LIB_OVERRIDE:
+        return _LIB_OVERRIDE
     os.makedirs(_OUT_DIR, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):

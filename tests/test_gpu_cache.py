@@ -116,3 +116,26 @@ def test_count_above_max_new_is_a_length_error():
     torch.cuda.synchronize()
     assert int(cache.status.item()) == kivi.ERR_LENGTH
     assert int(cache.kv_len.item()) == 0
+
+
+def test_nothing_packed_beyond_n_packed():
+    """The library packs a group exactly when the residual reaches R+G: after every
+    append the packed buffers past n_packed(L) keep a sentinel."""
+    H, dtype = 2, "f16"
+    kcfg, ocfg = configs(2, dtype, 2, H)
+    rng = np.random.default_rng(14)
+    cache = kivi.KVCache(kcfg, 1, 256)
+    for name in ("k_codes", "v_codes"):
+        getattr(cache, name).fill_(0xAB)
+    for name in ("k_scale", "k_zero", "v_scale", "v_zero"):
+        getattr(cache, name).fill_(-21555)          # 0xABCD
+    K, V = rand_kv(rng, H, 330, 128, dtype)
+    Kd, Vd = dev_tensor(K, dtype), dev_tensor(V, dtype)
+    L = 0
+    for n in [100, 27, 1, 30, 2] + [1] * 120 + [50]:
+        cache.append(Kd[:, L:L + n].contiguous()[None], Vd[:, L:L + n].contiguous()[None])
+        L += n
+        P = ocfg and oracle.n_packed(ocfg, L)
+        got = cache.seq_numpy(0)
+        assert np.all(got["k_codes"][:, P:] == 0xAB) and np.all(got["v_codes"][:, P:] == 0xAB), L
+        assert np.all(got["k_scale"][:, P // 32:] == 0xABCD) and np.all(got["v_zero"][:, P:] == 0xABCD), L

@@ -48,6 +48,29 @@ def test_flush_schedule_closed_form(oracle_lib):
 
 
 @pytest.mark.parametrize("bits", [2, 4])
+def test_nothing_packed_beyond_n_packed(oracle_lib, bits):
+    """Groups are packed exactly when the residual reaches R+G: after every append the
+    packed buffers hold nothing past n_packed(L) (they keep a sentinel there)."""
+    cfg = oracle.Cfg(bits=bits, num_kv_heads=2, head_dim=64)
+    G = cfg.group
+    rng = np.random.default_rng(30 + bits)
+    s = oracle.SeqCache(cfg, 512)
+    for name in ("k_codes", "v_codes"):
+        getattr(s, name)[...] = 0xAB
+    for name in ("k_scale", "k_zero", "v_scale", "v_zero"):
+        getattr(s, name)[...] = 0xABCD
+    L = 0
+    for n in [100, 27, 1, 1, 1, 3, 30, 31, 32, 33, 1, 64, 5, 40] + [1] * 100:
+        K, V = _rand_kv(rng, 2, n, 64)
+        assert s.append(K, V) == oracle.OK
+        L += n
+        P = oracle.n_packed(cfg, L)
+        assert np.all(s.k_codes[:, P:] == 0xAB) and np.all(s.v_codes[:, P:] == 0xAB)
+        assert np.all(s.k_scale[:, P // G:] == 0xABCD) and np.all(s.v_scale[:, P:] == 0xABCD)
+        assert not np.all(s.k_codes[:, :P] == 0xAB) or P == 0
+
+
+@pytest.mark.parametrize("bits", [2, 4])
 def test_streaming_equals_bulk(oracle_lib, bits):
     cfg = oracle.Cfg(bits=bits, num_q_heads=4, num_kv_heads=2, head_dim=64)
     rng = np.random.default_rng(2 + bits)
