@@ -50,9 +50,13 @@ def measured_hbm_peak():
 
 
 # ---------------------------------------------------------------- workload
+WORKLOAD_NAMES = {0: "tiny decode", 1: "Llama-2-7B MHA decode step", 2: "Llama-3-8B GQA decode step",
+                  3: "streaming append + decode step", 4: "long varlen (Mistral-7B shape) decode step"}
+
+
 def workload_spec(args):
     import synth
-    wl = synth.workload(2)
+    wl = synth.workload(getattr(args, "workload", 2))
     if args.batch:
         wl = wl.replace(batch=args.batch, lengths=(args.context or wl.lengths[0],) * args.batch)
     if args.context:
@@ -92,7 +96,7 @@ def job_throughput(units_per_rank: float, world: int, max_ms: float) -> float:
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms during the timed region."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -107,7 +111,7 @@ class ClockSampler:
         try:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.file, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -164,8 +168,8 @@ def gen_sequence_kv(wl, b, L, device):
     return K, V
 
 
-def step_inputs(wl, L0, n_steps, device):
-    """New K/V tokens ([steps][B][Hkv][1][D]) at positions L0 + s and queries ([steps][B][Hq][D])."""
+def step_inputs(wl, L0s, n_steps, device):
+    """New K/V tokens ([steps][B][Hkv][1][D]) at positions L0s[b] + s and queries ([steps][B][Hq][D])."""
     import torch
     import synth
     B, H, D = wl.batch, wl.num_kv_heads, wl.head_dim
@@ -174,8 +178,8 @@ def step_inputs(wl, L0, n_steps, device):
     vn = torch.empty_like(kn)
     for b in range(B):
         for h in range(H):
-            kn[:, b, h, 0] = synth.torch_kv_head_major(wl, b, h, L0, n_steps, "k", device)
-            vn[:, b, h, 0] = synth.torch_kv_head_major(wl, b, h, L0, n_steps, "v", device)
+            kn[:, b, h, 0] = synth.torch_kv_head_major(wl, b, h, L0s[b], n_steps, "k", device)
+            vn[:, b, h, 0] = synth.torch_kv_head_major(wl, b, h, L0s[b], n_steps, "v", device)
     q = torch.stack([torch.from_numpy(wl.query(s).view(np.int16)).view(tdt) for s in range(n_steps)]).to(device)
     return kn, vn, q
 
@@ -188,7 +192,8 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.set_device(device)
     wl = workload_spec(args)
     B, Hq, H, D, bits = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.bits
-    L0 = wl.lengths[0]
+    L0s = list(wl.lengths)
+    L0 = max(L0s)
     n_steps = args.warmup + args.steps
     cap = ((L0 + n_steps + args.steps + 31) // 32) * 32   # decode steps of both timed legs
     cfg = kivi.Config(bits=bits, head_dim=D, num_q_heads=Hq, num_kv_heads=H,
@@ -199,7 +204,7 @@ def run_gpu(args, rank, world, local_rank):
     for b0 in range(0, B, 8):
         ks, vs = [], []
         for b in range(b0, min(B, b0 + 8)):
-            K, V = gen_sequence_kv(wl, b, L0, device)
+            K, V = gen_sequence_kv(wl, b, L0s[b], device)
             ks.append(K)
             vs.append(V)
         sub = list(range(b0, min(B, b0 + 8)))
@@ -211,7 +216,7 @@ def run_gpu(args, rank, world, local_rank):
     cache.max_len = L0
     assert int(cache.status.item()) == 0, cache.status.item()
 
-    kn, vn, q = step_inputs(wl, L0, n_steps, device)
+    kn, vn, q = step_inputs(wl, L0s, n_steps, device)
     ones = torch.ones(B, dtype=torch.int32, device=device)
     kptr = [torch.tensor([kn[s, b].data_ptr() for b in range(B)], dtype=torch.int64, device=device)
             for s in range(n_steps)]
@@ -221,6 +226,14 @@ def run_gpu(args, rank, world, local_rank):
     max_len_final = L0 + n_steps
     ws = cache.workspace(max_len_final)
     stream = torch.cuda.current_stream(device)
+
+    # caches smaller than twice the 129 MB L2 are flushed (a 512 MB write) before every
+    # step, outside the per-step timing
+    cache_bytes = attn_bytes(wl, L0s, bits)
+    flush = cache_bytes < 256 << 20
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=device) if flush else None
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
 
     def step(s, ev_a=None, ev_b=None):
         cache.append_ptrs(kptr[s], vptr[s], ones, 1)
@@ -242,25 +255,29 @@ def run_gpu(args, rank, world, local_rank):
     with ClockSampler(smi_id(device)) as clk:
         ev0.record(stream)
         for i in range(args.steps):
+            if flush:
+                flush_buf.zero_()
+            step_ev[i][0].record(stream)
             step(args.warmup + i, *attn_ev[i])
+            step_ev[i][1].record(stream)
         ev1.record(stream)
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    total_ms = ev0.elapsed_time(ev1)
+    total_ms = sum(a.elapsed_time(b) for a, b in step_ev) if flush else ev0.elapsed_time(ev1)
     attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
     assert int(cache.status.item()) == 0, cache.status.item()
 
-    lens_per_step = [[L0 + args.warmup + i + 1] * B for i in range(args.steps)]
+    lens_per_step = [[L + args.warmup + i + 1 for L in L0s] for i in range(args.steps)]
     kv_tokens = sum(sum(ls) for ls in lens_per_step)
     bytes_per_step = [attn_bytes(wl, ls, bits) for ls in lens_per_step]
 
     # ------------------------------------------------------------ end to end through the public API
-    e2e = run_e2e(args, cache, wl, device, L0 + n_steps, max_len_final + args.steps, out)
+    e2e = run_e2e(args, cache, wl, device, [L + n_steps for L in L0s], max_len_final + args.steps, out)
 
     res = {
         "total_ms": total_ms, "attn_ms": attn_ms, "kv_tokens": kv_tokens, "attn_bytes": bytes_per_step,
-        "clocks": clk.summary(), "e2e": e2e, "launches_per_step": 3, "cap": cap,
+        "clocks": clk.summary(), "e2e": e2e, "launches_per_step": 3, "cap": cap, "flush": flush,
     }
     return res, wl
 
@@ -295,7 +312,7 @@ def run_e2e(args, cache, wl, device, L_start, max_len, out_dev):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
-    kv_tokens = sum(B * (L_start + s + 1) for s in range(n))
+    kv_tokens = sum(sum(L + s + 1 for L in L_start) for s in range(n))
     h2d = (kd.numel() + vd.numel() + qd.numel()) * 2
     d2h = out_dev.numel() * 4
     return {"value": kv_tokens / (ms / 1e3), "unit": "KV-tokens/s", "h2d_bytes_per_step": h2d,
@@ -339,12 +356,14 @@ def oracle_sample(wl, n_steps, budget_s=20.0):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kivi", choices=["kivi", "reference"])
     ap.add_argument("--batch", type=int, default=0)
     ap.add_argument("--context", type=int, default=0)
     ap.add_argument("--bits", type=int, default=0)
+    ap.add_argument("--workload", type=int, default=2, choices=[0, 1, 2, 3, 4],
+                    help="0 tiny, 1 Llama-2-7B MHA, 2 Llama-3-8B GQA (default), 3 streaming, 4 long varlen")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
 
@@ -352,17 +371,21 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
     wl = workload_spec(args)
+    ctx = (f"{wl.lengths[0]} cached tokens" if len(set(wl.lengths)) == 1 else
+           f"{min(wl.lengths)}..{max(wl.lengths)} cached tokens (mean {sum(wl.lengths) / len(wl.lengths):.0f})")
     config = {
-        "workload": (f"Llama-3-8B GQA decode step: {wl.batch} sequences x {wl.lengths[0]} cached tokens, "
+        "workload": (f"{WORKLOAD_NAMES[args.workload]}: {wl.batch} sequences x {ctx}, "
                      f"{wl.num_q_heads} query / {wl.num_kv_heads} kv heads, head_dim {wl.head_dim}, "
                      f"{wl.bits}-bit KIVI (G=32, R=128), {wl.dtype} inputs"),
-        "batch": wl.batch, "context": wl.lengths[0], "q_heads": wl.num_q_heads, "kv_heads": wl.num_kv_heads,
+        "batch": wl.batch, "context": wl.lengths[0] if len(set(wl.lengths)) == 1 else "varlen",
+        "q_heads": wl.num_q_heads, "kv_heads": wl.num_kv_heads,
         "head_dim": wl.head_dim, "bits": wl.bits, "group": wl.group, "residual": wl.residual,
         "input_dtype": wl.dtype, "step": "append 1 token/sequence (+ group flush every 32 steps) + decode attention",
-        "l2": "no flush: the packed cache (>1.6 GB) is larger than L2 (129 MB)",
+        "l2": ("flushed before every step (512 MB write, outside the step timing): the cache is smaller than L2"
+               if attn_bytes(wl, list(wl.lengths), wl.bits) < 256 << 20 else
+               "no flush: the packed cache is larger than L2 (129 MB)"),
         "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
     }
-
     if args.impl == "reference":
         if rank != 0:
             return

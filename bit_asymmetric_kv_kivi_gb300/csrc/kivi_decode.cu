@@ -515,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, BITS == 2 ? 3 : 2) decode_mma_kernel
     // ---------------- packed split: key groups [g0, g1)
     const int gid = lane >> 2, t = lane & 3;
     const int hh = gid >> 1, part = gid & 1;     // B column gid = (head hh, hi/lo part)
-    const bool hv = hh < GQ;
+    const bool hv = GQ >= 4 || hh < GQ;   // this thread's B column belongs to a real head
 
     // q prescale: a power of two putting max |q| in (1/2, 1]
     float qmax_abs = 0.0f;
@@ -570,31 +570,26 @@ __global__ void __launch_bounds__(kThreads, BITS == 2 ? 3 : 2) decode_mma_kernel
     const unsigned char* vs_base = reinterpret_cast<const unsigned char*>(sq.v_scale + static_cast<int64_t>(h) * cap * (kD / kGroup));
     const unsigned char* vz_base = reinterpret_cast<const unsigned char*>(sq.v_zero + static_cast<int64_t>(h) * cap * (kD / kGroup));
 
+    // Per-lane cp.async plan of one group: code rows as 16-byte chunks (lane + 32k), then one
+    // chunk of key scale / zero (lanes 0-15 / 16-31) and one of value scale / zero.
+    constexpr int kCodeChunks = 2 * RB / 32;                // per lane, per code block
+    const int half = lane >> 4, off16 = (lane & 15) * 16;
+    const unsigned char* kc_lane = kc_base + lane * 16;
+    const unsigned char* vc_lane = vc_base + lane * 16;
+    const unsigned char* km_lane = (half ? kz_base : ks_base) + off16;
+    const unsigned char* vm_lane = (half ? vz_base : vs_base) + off16;
+    const int km_dst = 2 * kGroup * RB + half * Lay::kMetaPad + (off16 >> 6) * 80 + (off16 & 63);
+    const int vm_dst = 2 * kGroup * RB + 2 * Lay::kMetaPad + half * 256 + off16;
     auto issue = [&](int slot, int64_t j) {
         unsigned char* dst = my_st + slot * STAGE;
+        const int64_t code_off = j * kGroup * RB, meta_off = j * 256;
 #pragma unroll
-        for (int k = 0; k < Lay::kChunks / 32; ++k) {
-            const int c = lane + 32 * k;
-            const unsigned char* src;
-            int d;
-            if (c < 2 * RB) {
-                src = kc_base + j * kGroup * RB + c * 16;
-                d = c * 16;
-            } else if (c < 4 * RB) {
-                src = vc_base + j * kGroup * RB + (c - 2 * RB) * 16;
-                d = c * 16;
-            } else {
-                const int r = c - 4 * RB, reg = r >> 4, off = (r & 15) * 16;
-                src = reg == 0 ? ks_base + j * 256 + off
-                    : reg == 1 ? kz_base + j * 256 + off
-                    : reg == 2 ? vs_base + j * 256 + off
-                               : vz_base + j * 256 + off;
-                d = 2 * kGroup * RB +
-                    (reg < 2 ? reg * Lay::kMetaPad + (off >> 6) * 80 + (off & 63)
-                             : 2 * Lay::kMetaPad + (reg - 2) * 256 + off);
-            }
-            cp_async16(dst + d, src);
+        for (int k = 0; k < kCodeChunks; ++k) {
+            cp_async16(dst + lane * 16 + 512 * k, kc_lane + code_off + 512 * k);
+            cp_async16(dst + kGroup * RB + lane * 16 + 512 * k, vc_lane + code_off + 512 * k);
         }
+        cp_async16(dst + km_dst, km_lane + meta_off);
+        cp_async16(dst + vm_dst, vm_lane + meta_off);
     };
 
 #pragma unroll
@@ -713,7 +708,7 @@ a0 = code_slot<BITS>(cw[0][w0], cws[0][w0], s0);
         }
         float p[4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) p[r] = t < GQ ? exp2f(S[r] - m_run) : 0.0f;
+        for (int r = 0; r < 4; ++r) p[r] = (GQ >= 4 || t < GQ) ? exp2f(S[r] - m_run) : 0.0f;
         l_run += (p[0] + p[1]) + (p[2] + p[3]);
 #pragma unroll
         // token 8r + j goes to column 8r + 2 (j % 4) + j / 4: the value side pairs tokens
@@ -788,7 +783,7 @@ a0 = code_slot<BITS>(cw[0][w0], cws[0][w0], s0);
 #pragma unroll
     for (int kg = 0; kg < 4; ++kg) zk[kg] = __shfl_sync(kFull, zmine, 4 * kg + t);
     __syncthreads();
-    if (t < GQ) {
+    if (GQ >= 4 || t < GQ) {
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
             const int kg = mt >> 1;

@@ -135,7 +135,7 @@ def test_nothing_packed_beyond_n_packed():
     for n in [100, 27, 1, 30, 2] + [1] * 120 + [50]:
         cache.append(Kd[:, L:L + n].contiguous()[None], Vd[:, L:L + n].contiguous()[None])
         L += n
-        P = ocfg and oracle.n_packed(ocfg, L)
+        P = oracle.n_packed(ocfg, L)
         got = cache.seq_numpy(0)
         assert np.all(got["k_codes"][:, P:] == 0xAB) and np.all(got["v_codes"][:, P:] == 0xAB), L
         assert np.all(got["k_scale"][:, P // 32:] == 0xABCD) and np.all(got["v_zero"][:, P:] == 0xABCD), L
