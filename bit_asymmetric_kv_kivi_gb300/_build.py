@@ -19,7 +19,7 @@ LIB = os.path.join(OUT_DIR, "libkivi.so")
 OBJ_DIR = os.path.join(PKG, "_build")
 SOURCES = ["kivi_abi.cu", "kivi_codec.cu", "kivi_decode.cu", "kivi_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
+NVCC_FLAGS = ["-O3", "-std=c++20", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
               "--expt-relaxed-constexpr", f"-I{ROOT}/include"]
 
 

@@ -9,140 +9,417 @@
 // group and window sizes from "KV cache quantization with KIVI INT2 setup
 // guide 2026" (G = 32, R = 128).
 //
-// Design. One CTA of 128 threads quantizes one 32-token group tile of one
-// kv head: the tile (32 x D, 16-bit) is staged into shared memory with
-// 16-byte loads, per-group min/max and the fp16 scale/zero are computed
-// there, and every thread then emits whole 32-bit words of packed codes, so
-// the code rows leave the SM as coalesced word stores. These kernels stream
-// 16 bits in and 3 (2-bit) bits out per element; they are HBM-bound.
+// Design. One warp quantizes one 32-token group tile (or, for values, up to
+// 32 tokens) over a slice of up to 128 channels, entirely in registers: no
+// shared memory and no block barriers. For keys a lane owns four channels and
+// loads them from every token row (each load instruction reads whole rows,
+// coalesced); for values a lane owns one token row. Minimum and maximum run on
+// packed pairs (min/max.f16x2 or .bf16x2); the codes come from one fused
+// multiply-add with a rounding constant and reach their bit position through the
+// accumulating add, so that an element costs about nine instructions. These
+// kernels stream 16 bits in and 2.5 (2-bit) bits out per element and are meant
+// to run at the HBM bound.
 #include "kivi_internal.cuh"
 
 namespace kivi {
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kPad = 8;  // row padding of the shared tile, in 16-bit elements (keeps 16-byte rows)
+constexpr int kThreads = 256;   // 8 warps per CTA, one tile slice per warp
+constexpr int kWarps = kThreads / 32;
 
-// Copies rows [0, nrows) of a 32 x D tile of 16-bit elements into shared memory.
-// row_src(t) returns the global address of row t (16-byte aligned).
-template <typename RowSrc>
-__device__ __forceinline__ void stage_tile(uint16_t* tile, int D, int nrows, RowSrc row_src) {
-    const int chunks_per_row = D / 8;  // 16-byte chunks
-    for (int c = threadIdx.x; c < nrows * chunks_per_row; c += kThreads) {
-        const int t = c / chunks_per_row, part = c - t * chunks_per_row;
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(row_src(t)) + part);
-        *reinterpret_cast<uint4*>(tile + t * (D + kPad) + part * 8) = v;
+// Channels one warp covers of a D-channel tile: 64 where that divides D, else 32. A
+// 64-channel slice holds 32 registers of elements per lane, so that three CTAs of eight
+// warps fit on an SM.
+__host__ __device__ constexpr int slice_width(int D) { return D % 64 == 0 ? 64 : 32; }
+
+template <int DT>
+__device__ __forceinline__ uint32_t hmin2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    if constexpr (DT == KIVI_F16) asm("min.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    else asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+template <int DT>
+__device__ __forceinline__ uint32_t hmax2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    if constexpr (DT == KIVI_F16) asm("max.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    else asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t lo16(uint32_t w) { return w & 0xffffu; }
+__device__ __forceinline__ uint32_t hi16(uint32_t w) { return w >> 16; }
+__device__ __forceinline__ bool is_zero16(uint32_t h) { return (h & 0x7fffu) == 0; }
+
+// Smaller / larger of two 16-bit floats of the same group (either one when equal).
+template <int DT>
+__device__ __forceinline__ uint32_t pick_min(uint32_t a, uint32_t b) {
+    return widen<DT>(static_cast<uint16_t>(b)) < widen<DT>(static_cast<uint16_t>(a)) ? b : a;
+}
+template <int DT>
+__device__ __forceinline__ uint32_t pick_max(uint32_t a, uint32_t b) {
+    return widen<DT>(static_cast<uint16_t>(b)) > widen<DT>(static_cast<uint16_t>(a)) ? b : a;
+}
+
+// The fp32 quantizer of one group: zero z, scale s and r = 1/s (0 when s is 0 or inf).
+struct Quantizer {
+    float z, r, s;
+};
+
+__device__ __forceinline__ Quantizer make_quantizer(const GroupParams& gp) {
+    Quantizer q;
+    q.z = gp.z;
+    q.s = gp.s;
+    q.r = gp.s != 0.0f ? __frcp_rn(gp.s) : 0.0f;
+    return q;
+}
+
+// Adding 1.5 * 2^23 to an fp32 value t with |t| < 2^22 rounds it to the integer
+// rint(t) (half to even) in the low mantissa bits.
+constexpr float kMagic = 12582912.0f;
+constexpr uint32_t kMagicBits = 0x4B400000u;
+// What n encodings of kMagic + code, shifted to bit offsets 0, B, 2B, ..., sum to
+// beyond the codes themselves; subtracted up front, so the sum is the packed codes.
+__host__ __device__ constexpr uint32_t magic_offset(int n, int bits) {
+    uint32_t o = 0;
+    for (int e = 0; e < n; ++e) o += kMagicBits << (e * bits);
+    return 0u - o;
+}
+
+// The code of encode() as kMagic + code (an fp32 bit pattern), with the IEEE division
+// replaced by r = 1/s, plus a flag set when that may give a different code.
+// y = fma(d, r, kMagic) is kMagic + rint(d r) for the exact product d r, and f is
+// d r - rint(d r). The exact product is within 2^-23 |t| of the correctly rounded
+// quotient t = d / s (r is 1/s correctly rounded). Only the half-integers 0.5 ..
+// qmax - 0.5 (|t| < 16) can change a clamped code, and there the two differ by at
+// most 2e-6: the codes agree unless |f| > 0.5 - 1e-5, which sets near_tie (the caller
+// then recomputes with the exact division). There is no clamp: the caller checks with
+// codes_in_range() that every element of the group lands in [0, qmax] and otherwise
+// recomputes the group exactly. r == 0 (s == 0 or s = inf) gives code 0, as the
+// division does.
+template <int BITS>
+__device__ __forceinline__ uint32_t code_bits(float x, const Quantizer& q, bool& near_tie) {
+    const float d = __fsub_rn(x, q.z);
+    const float y = __fmaf_rn(d, q.r, kMagic);
+    const float f = __fmaf_rn(d, q.r, -__fsub_rn(y, kMagic));
+    near_tie |= fabsf(f) > 0.5f - 1e-5f;
+    return __float_as_uint(y);
+}
+
+// Whether code_bits() gives codes in [0, qmax] for every element of a group with this
+// minimum and maximum: x -> fma(x - z, r, kMagic) is monotone (r >= 0), so checking the
+// two ends suffices. False only where the fp16 rounding of z or s pushes an end more
+// than half a step out (for instance inputs below the fp16 normal range).
+template <int BITS>
+__device__ __forceinline__ bool codes_in_range(float mn, float mx, const Quantizer& q) {
+    constexpr float qmax = static_cast<float>((1 << BITS) - 1);
+    const float ylo = __fmaf_rn(__fsub_rn(mn, q.z), q.r, kMagic);
+    const float yhi = __fmaf_rn(__fsub_rn(mx, q.z), q.r, kMagic);
+    return ylo >= kMagic && yhi <= kMagic + qmax;
+}
+
+template <int DT>
+__device__ __forceinline__ float half_at(uint32_t w, int hi) {
+    return widen<DT>(static_cast<uint16_t>(hi ? w >> 16 : w & 0xffffu));
+}
+
+__device__ __forceinline__ uint2 ld_nc_u2(const uint16_t* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint4 ld_nc_u4(const uint16_t* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Rare paths, kept out of line so that the unrolled main loops stay small in the
+// instruction cache; they re-read their inputs from global memory.
+
+// Codes of four consecutive key channels at p (one per channel quantizer), with the
+// IEEE division: the product path found one of them near a rounding tie.
+template <int BITS, int DT>
+__device__ __noinline__ uint32_t keys_exact4(const uint16_t* p, float z0, float z1, float z2, float z3, float s0,
+                                             float s1, float s2, float s3) {
+    constexpr int qmax = (1 << BITS) - 1;
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    return encode(half_at<DT>(v.x, 0), z0, s0, qmax) | encode(half_at<DT>(v.x, 1), z1, s1, qmax) << BITS |
+           encode(half_at<DT>(v.y, 0), z2, s2, qmax) << (2 * BITS) | encode(half_at<DT>(v.y, 1), z3, s3, qmax) << (3 * BITS);
+}
+
+// Code words of one 32-channel value group at p with the IEEE division.
+template <int BITS, int DT>
+__device__ __noinline__ uint4 values_exact(const uint16_t* p, float z, float s) {
+    constexpr int qmax = (1 << BITS) - 1, CPW = 32 / BITS;
+    uint32_t out[4] = {0, 0, 0, 0};
+#pragma unroll 1
+    for (int c = 0; c < kGroup; ++c) out[c / CPW] |= encode(widen<DT>(p[c]), z, s, qmax) << ((c % CPW) * BITS);
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// One lane's share of a 32-row x DS-channel tile of 16-bit elements, in registers.
+// Keys: lane l owns channels 4 (l mod DS/4) .. +3 of the slice and the tokens j,
+// j + TS, ... (j = l / (DS/4), TS = 128 / DS): w[2 i], w[2 i + 1] hold token i TS + j.
+// Values: lane l owns token l, w[c] holding channels 2 c and 2 c + 1 of the slice.
+template <int DS>
+struct Tile {
+    uint32_t w[DS / 2];
+};
+
+// Loads a key tile. row(t) is token t's row at the slice's first channel; where
+// `contiguous` is set (the same on every lane) the rows are known to be row(0) + t * D.
+template <int DS, typename RowFn>
+__device__ __forceinline__ void keys_load(RowFn row, bool contiguous, int D, Tile<DS>& x) {
+    constexpr int LPR = DS / 4, TS = 32 / LPR, NT = 32 / TS;
+    const int lane = threadIdx.x & 31, cq = lane % LPR, j = lane / LPR;
+    if (contiguous) {
+        const uint16_t* p = row(j) + 4 * cq;
+        const int64_t step = static_cast<int64_t>(TS) * D;
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+            const uint2 v = ld_nc_u2(p + i * step);
+            x.w[2 * i] = v.x;
+            x.w[2 * i + 1] = v.y;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+            const uint2 v = ld_nc_u2(row(i * TS + j) + 4 * cq);
+            x.w[2 * i] = v.x;
+            x.w[2 * i + 1] = v.y;
+        }
     }
 }
 
-// Keys of one group (32 tokens x D channels in `tile`): per channel min/max
-// over the 32 tokens, fp16 scale and zero into scale[d], zero[d], and the 32
-// packed code rows into codes (row stride D*BITS/8 bytes).
-template <int BITS, int DT>
-__device__ void quantize_key_group(const uint16_t* tile, int D, uint8_t* codes, uint16_t* scale,
-                                   uint16_t* zero, float* s_s, float* s_z) {
-    constexpr int qmax = (1 << BITS) - 1;
-    const int ld = D + kPad;
-    for (int d = threadIdx.x; d < D; d += kThreads) {
-        float mn = widen<DT>(tile[d]), mx = mn;
-#pragma unroll 8
-        for (int t = 1; t < kGroup; ++t) {
-            const float v = widen<DT>(tile[t * ld + d]);
-            mn = v < mn ? v : mn;   // first-seen wins on ties (+0 / -0), in token order
-            mx = v > mx ? v : mx;
-        }
-        const GroupParams p = group_params(mn, mx, qmax);
-        scale[d] = p.s16;
-        zero[d] = p.z16;
-        s_s[d] = p.s;
-        s_z[d] = p.z;
-    }
-    __syncthreads();
-    constexpr int per_word = 32 / BITS;
-    const int wpr = D / per_word;  // 32-bit words per code row
-    uint32_t* out = reinterpret_cast<uint32_t*>(codes);
-    for (int w = threadIdx.x; w < kGroup * wpr; w += kThreads) {
-        const int t = w / wpr, k = w - t * wpr;
-        const int d0 = k * per_word;
-        uint32_t word = 0;
+// Keys of one 32-token group over one DS-channel slice, by one warp, from a tile that
+// keys_load() filled; row() as there (used again only on the rare exact paths). codes,
+// scale and zero point at the slice's first channel of token 0's code row and of the
+// group's scale and zero rows. The minimum and maximum come from packed min/max over
+// token pairs and a shuffle across token subsets; where one is a zero, the rule "the
+// first value seen wins" is applied by finding the sign of the first zero in token order.
+template <int BITS, int DT, int DS, typename RowFn>
+__device__ __forceinline__ void keys_compute(const Tile<DS>& x, RowFn row, uint8_t* codes, int code_ld, uint16_t* scale,
+                                             uint16_t* zero) {
+    constexpr int LPR = DS / 4, TS = 32 / LPR, NT = 32 / TS;
+    const int lane = threadIdx.x & 31, cq = lane % LPR, j = lane / LPR;
+    uint32_t mn0 = x.w[0], mx0 = x.w[0], mn1 = x.w[1], mx1 = x.w[1];
 #pragma unroll
-        for (int i = 0; i < per_word; ++i) {
-            const int d = d0 + i;
-            word |= encode(widen<DT>(tile[t * ld + d]), s_z[d], s_s[d], qmax) << (i * BITS);
+    for (int i = 1; i < NT; ++i) {
+        mn0 = hmin2<DT>(mn0, x.w[2 * i]);
+        mx0 = hmax2<DT>(mx0, x.w[2 * i]);
+        mn1 = hmin2<DT>(mn1, x.w[2 * i + 1]);
+        mx1 = hmax2<DT>(mx1, x.w[2 * i + 1]);
+    }
+#pragma unroll
+    for (int o = LPR; o < 32; o <<= 1) {
+        mn0 = hmin2<DT>(mn0, __shfl_xor_sync(0xffffffffu, mn0, o));
+        mx0 = hmax2<DT>(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mn1 = hmin2<DT>(mn1, __shfl_xor_sync(0xffffffffu, mn1, o));
+        mx1 = hmax2<DT>(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    uint32_t mn[4] = {lo16(mn0), hi16(mn0), lo16(mn1), hi16(mn1)};
+    uint32_t mx[4] = {lo16(mx0), hi16(mx0), lo16(mx1), hi16(mx1)};
+    bool fix = false;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) fix |= is_zero16(mn[e]) || is_zero16(mx[e]);
+    if (__any_sync(0xffffffffu, fix)) {
+        // 2 t + sign of this lane's first zero, per channel
+        uint32_t first[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+#pragma unroll 1
+        for (int i = NT - 1; i >= 0; --i) {
+            const uint2 v = *reinterpret_cast<const uint2*>(row(i * TS + j) + 4 * cq);
+            const uint32_t hv[4] = {lo16(v.x), hi16(v.x), lo16(v.y), hi16(v.y)};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (is_zero16(hv[e])) first[e] = 2u * (i * TS + j) + (hv[e] >> 15);
         }
-        out[w] = word;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+#pragma unroll
+            for (int o = LPR; o < 32; o <<= 1) first[e] = min(first[e], __shfl_xor_sync(0xffffffffu, first[e], o));
+            const uint32_t zs = (first[e] & 1u) ? 0x8000u : 0u;
+            if (is_zero16(mn[e])) mn[e] = zs;
+            if (is_zero16(mx[e])) mx[e] = zs;
+        }
+    }
+    constexpr int qmax = (1 << BITS) - 1;
+    Quantizer qz[4];
+    uint32_t s16[4], z16[4];
+    bool in_range = true;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float fmn = widen<DT>(static_cast<uint16_t>(mn[e])), fmx = widen<DT>(static_cast<uint16_t>(mx[e]));
+        const GroupParams gp = group_params(fmn, fmx, qmax);
+        s16[e] = gp.s16;
+        z16[e] = gp.z16;
+        qz[e] = make_quantizer(gp);
+        in_range &= codes_in_range<BITS>(fmn, fmx, qz[e]);
+    }
+    if (j == 0) {
+        *reinterpret_cast<uint2*>(scale + 4 * cq) = make_uint2(s16[0] | (s16[1] << 16), s16[2] | (s16[3] << 16));
+        *reinterpret_cast<uint2*>(zero + 4 * cq) = make_uint2(z16[0] | (z16[1] << 16), z16[2] | (z16[3] << 16));
+    }
+    uint32_t tie_rows = in_range ? 0u : 0xffffffffu >> (32 - NT);   // rows to redo with the exact division
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+        bool tie = false;
+        uint32_t acc = magic_offset(4, BITS);
+        acc += code_bits<BITS>(half_at<DT>(x.w[2 * i], 0), qz[0], tie);
+        acc += code_bits<BITS>(half_at<DT>(x.w[2 * i], 1), qz[1], tie) << BITS;
+        acc += code_bits<BITS>(half_at<DT>(x.w[2 * i + 1], 0), qz[2], tie) << (2 * BITS);
+        acc += code_bits<BITS>(half_at<DT>(x.w[2 * i + 1], 1), qz[3], tie) << (3 * BITS);
+        tie_rows |= static_cast<uint32_t>(tie) << i;
+        uint8_t* dst = codes + static_cast<int64_t>(i * TS + j) * code_ld;
+        if constexpr (BITS == 2) dst[cq] = static_cast<uint8_t>(acc);
+        else reinterpret_cast<uint16_t*>(dst)[cq] = static_cast<uint16_t>(acc);
+    }
+#pragma unroll 1
+    while (tie_rows != 0) {
+        const int i = __ffs(tie_rows) - 1;
+        tie_rows &= tie_rows - 1;
+        const uint32_t acc = keys_exact4<BITS, DT>(row(i * TS + j) + 4 * cq, qz[0].z, qz[1].z, qz[2].z, qz[3].z, qz[0].s,
+                                                   qz[1].s, qz[2].s, qz[3].s);
+        uint8_t* dst = codes + static_cast<int64_t>(i * TS + j) * code_ld;
+        if constexpr (BITS == 2) dst[cq] = static_cast<uint8_t>(acc);
+        else reinterpret_cast<uint16_t*>(dst)[cq] = static_cast<uint16_t>(acc);
     }
 }
 
-// Values of up to 32 tokens (rows [0, ntok) of `tile`): per token and per
-// group of 32 channels, min/max, fp16 scale and zero into scale/zero
-// [ntok][D/32], and the packed code rows.
-template <int BITS, int DT>
-__device__ void quantize_value_rows(const uint16_t* tile, int D, int ntok, uint8_t* codes,
-                                    uint16_t* scale, uint16_t* zero, float* s_s, float* s_z) {
-    constexpr int qmax = (1 << BITS) - 1;
-    const int ld = D + kPad, ng = D / kGroup;
-    for (int i = threadIdx.x; i < ntok * ng; i += kThreads) {
-        const int t = i / ng, k = i - t * ng;
-        const uint16_t* x = tile + t * ld + k * kGroup;
-        float mn = widen<DT>(x[0]), mx = mn;
-#pragma unroll 8
-        for (int c = 1; c < kGroup; ++c) {
-            const float v = widen<DT>(x[c]);
-            mn = v < mn ? v : mn;   // first-seen wins on ties, in channel order
-            mx = v > mx ? v : mx;
-        }
-        const GroupParams p = group_params(mn, mx, qmax);
-        scale[i] = p.s16;
-        zero[i] = p.z16;
-        s_s[i] = p.s;
-        s_z[i] = p.z;
-    }
-    __syncthreads();
-    constexpr int per_word = 32 / BITS;
-    const int wpr = D / per_word;
-    uint32_t* out = reinterpret_cast<uint32_t*>(codes);
-    for (int w = threadIdx.x; w < ntok * wpr; w += kThreads) {
-        const int t = w / wpr, k = w - t * wpr;
-        const int d0 = k * per_word;
-        const float s = s_s[t * ng + d0 / kGroup], z = s_z[t * ng + d0 / kGroup];
-        uint32_t word = 0;
+// Loads one lane's value row: src is the token's row at the slice's first channel
+// (null: this lane has no token).
+template <int DS>
+__device__ __forceinline__ void values_load(const uint16_t* src, Tile<DS>& x) {
+    if (src == nullptr) return;
 #pragma unroll
-        for (int i = 0; i < per_word; ++i)
-            word |= encode(widen<DT>(tile[t * ld + d0 + i]), z, s, qmax) << (i * BITS);
-        out[w] = word;
+    for (int c = 0; c < DS / 8; ++c) {
+        const uint4 v = ld_nc_u4(src + 8 * c);
+        x.w[4 * c] = v.x;
+        x.w[4 * c + 1] = v.y;
+        x.w[4 * c + 2] = v.z;
+        x.w[4 * c + 3] = v.w;
+    }
+}
+
+// Values of one token over one DS-channel slice (DS / 32 channel groups), by one lane,
+// from the row values_load() read from src; codes, scale and zero point at the slice's
+// first code byte and first group of the token's rows. Packed min/max over channel
+// pairs, then the pair's two halves; a zero minimum or maximum takes the sign of the
+// first zero in channel order.
+template <int BITS, int DT, int DS>
+__device__ __forceinline__ void values_compute(const Tile<DS>& x, const uint16_t* src, uint8_t* codes, uint16_t* scale,
+                                               uint16_t* zero) {
+    if (src == nullptr) return;
+    constexpr int NKG = DS / kGroup, qmax = (1 << BITS) - 1;
+    constexpr int WPG = kGroup * BITS / 32;   // code words per channel group
+    uint32_t code_w[NKG][WPG];
+    uint32_t s16[NKG], z16[NKG];
+    float zq[NKG], sq[NKG];   // fp32 zero and scale per group, for the exact redo
+    uint32_t tie_groups = 0;  // groups to redo with the exact division
+#pragma unroll
+    for (int k = 0; k < NKG; ++k) {
+        const uint32_t* w = x.w + 16 * k;
+        uint32_t mn2 = w[0], mx2 = w[0];
+#pragma unroll
+        for (int c = 1; c < 16; ++c) {
+            mn2 = hmin2<DT>(mn2, w[c]);
+            mx2 = hmax2<DT>(mx2, w[c]);
+        }
+        uint32_t mn = pick_min<DT>(lo16(mn2), hi16(mn2));
+        uint32_t mx = pick_max<DT>(lo16(mx2), hi16(mx2));
+        if (is_zero16(mn) || is_zero16(mx)) {   // sign of the first zero in channel order
+            uint32_t zs = 0;
+#pragma unroll 1
+            for (int c = kGroup - 1; c >= 0; --c) {
+                const uint32_t hv = src[k * kGroup + c];
+                zs = is_zero16(hv) ? hv & 0x8000u : zs;
+            }
+            if (is_zero16(mn)) mn = zs;
+            if (is_zero16(mx)) mx = zs;
+        }
+        const float fmn = widen<DT>(static_cast<uint16_t>(mn)), fmx = widen<DT>(static_cast<uint16_t>(mx));
+        const GroupParams gp = group_params(fmn, fmx, qmax);
+        s16[k] = gp.s16;
+        z16[k] = gp.z16;
+        const Quantizer q = make_quantizer(gp);
+        zq[k] = q.z;
+        sq[k] = q.s;
+        bool tie = !codes_in_range<BITS>(fmn, fmx, q);
+#pragma unroll
+        for (int ww = 0; ww < WPG; ++ww) {
+            constexpr int CPW = 32 / BITS;   // codes per word
+            uint32_t acc = magic_offset(CPW, BITS);
+#pragma unroll
+            for (int e = 0; e < CPW; ++e) {
+                const int c = ww * CPW + e;
+                acc += code_bits<BITS>(half_at<DT>(w[c >> 1], c & 1), q, tie) << (e * BITS);
+            }
+            code_w[k][ww] = acc;
+        }
+        tie_groups |= static_cast<uint32_t>(tie) << k;
+    }
+    // code row: NKG * WPG words (8 bytes per 32 channels at 2 bits, 16 at 4 bits)
+    uint32_t* cw = reinterpret_cast<uint32_t*>(codes);
+    if constexpr (NKG * WPG % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < NKG * WPG / 4; ++i)
+            reinterpret_cast<uint4*>(cw)[i] = make_uint4(code_w[(4 * i) / WPG][(4 * i) % WPG], code_w[(4 * i + 1) / WPG][(4 * i + 1) % WPG],
+                                                         code_w[(4 * i + 2) / WPG][(4 * i + 2) % WPG], code_w[(4 * i + 3) / WPG][(4 * i + 3) % WPG]);
+    } else {
+        reinterpret_cast<uint2*>(cw)[0] = make_uint2(code_w[0][0], code_w[0][1]);   // NKG * WPG == 2
+    }
+#pragma unroll
+    for (int k = 0; k < NKG; ++k) {
+        scale[k] = static_cast<uint16_t>(s16[k]);
+        zero[k] = static_cast<uint16_t>(z16[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < NKG; ++k) {
+        if (tie_groups & (1u << k)) {
+            const uint4 ex = values_exact<BITS, DT>(src + k * kGroup, zq[k], sq[k]);
+            if constexpr (WPG == 4) reinterpret_cast<uint4*>(cw)[k] = ex;
+            else reinterpret_cast<uint2*>(cw)[k] = make_uint2(ex.x, ex.y);
+        }
     }
 }
 
 // ---------------------------------------------------------------- standalone codec
 
-template <int BITS, int DT>
-__global__ void __launch_bounds__(kThreads) quant_keys_kernel(CodecArgs a) {
-    __shared__ __align__(16) uint16_t tile[kGroup * (kMaxHeadDim + kPad)];
-    __shared__ float s_s[kMaxHeadDim], s_z[kMaxHeadDim];
-    const int j = blockIdx.x, st = blockIdx.y, D = a.D;
-    const int64_t tok0 = static_cast<int64_t>(st) * a.n_tokens + static_cast<int64_t>(j) * kGroup;
-    const uint16_t* x = static_cast<const uint16_t*>(a.x);
-    stage_tile(tile, D, kGroup, [&](int t) { return x + (tok0 + t) * D; });
-    __syncthreads();
-    const int64_t g = static_cast<int64_t>(st) * (a.n_tokens / kGroup) + j;
-    quantize_key_group<BITS, DT>(tile, D, a.codes + tok0 * (D * BITS / 8), a.scale + g * D, a.zero + g * D,
-                                 s_s, s_z);
+// One warp per (stream, 32-token group, channel slice).
+template <int BITS, int DT, int DS>
+__global__ void __launch_bounds__(kThreads, 3) quant_keys_kernel(CodecArgs a) {
+    const int D = a.D, nsl = D / DS, groups = a.n_tokens / kGroup;
+    const int64_t unit = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    if (unit >= static_cast<int64_t>(a.n_streams) * groups * nsl) return;
+    const int sl = static_cast<int>(unit % nsl);
+    const int64_t g = unit / nsl;   // stream * groups + group
+    const int64_t tok0 = g * kGroup;
+    const uint16_t* x = static_cast<const uint16_t*>(a.x) + tok0 * D + sl * DS;
+    const int row_bytes = D * BITS / 8;
+    auto row = [&](int t) { return x + static_cast<int64_t>(t) * D; };
+    Tile<DS> tile;
+    keys_load<DS>(row, true, D, tile);
+    keys_compute<BITS, DT, DS>(tile, row, a.codes + tok0 * row_bytes + sl * (DS * BITS / 8), row_bytes,
+                               a.scale + g * D + sl * DS, a.zero + g * D + sl * DS);
 }
 
-template <int BITS, int DT>
-__global__ void __launch_bounds__(kThreads) quant_values_kernel(CodecArgs a) {
-    __shared__ __align__(16) uint16_t tile[kGroup * (kMaxHeadDim + kPad)];
-    __shared__ float s_s[kGroup * (kMaxHeadDim / kGroup)], s_z[kGroup * (kMaxHeadDim / kGroup)];
-    const int j = blockIdx.x, st = blockIdx.y, D = a.D;
-    const int t_begin = j * kGroup;
-    const int ntok = min(kGroup, a.n_tokens - t_begin);
-    const int64_t tok0 = static_cast<int64_t>(st) * a.n_tokens + t_begin;
-    const uint16_t* x = static_cast<const uint16_t*>(a.x);
-    stage_tile(tile, D, ntok, [&](int t) { return x + (tok0 + t) * D; });
-    __syncthreads();
-    quantize_value_rows<BITS, DT>(tile, D, ntok, a.codes + tok0 * (D * BITS / 8),
-                                  a.scale + tok0 * (D / kGroup), a.zero + tok0 * (D / kGroup), s_s, s_z);
+// One warp per (stream, run of 32 tokens, channel slice); lane t takes token t.
+template <int BITS, int DT, int DS>
+__global__ void __launch_bounds__(kThreads, 3) quant_values_kernel(CodecArgs a) {
+    const int D = a.D, nsl = D / DS, runs = (a.n_tokens + kGroup - 1) / kGroup;
+    const int64_t unit = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    if (unit >= static_cast<int64_t>(a.n_streams) * runs * nsl) return;
+    const int sl = static_cast<int>(unit % nsl);
+    const int64_t sr = unit / nsl;
+    const int st = static_cast<int>(sr / runs);
+    const int t = static_cast<int>(sr % runs) * kGroup + (threadIdx.x & 31);
+    const int64_t tok = static_cast<int64_t>(st) * a.n_tokens + t;
+    const uint16_t* src = t < a.n_tokens ? static_cast<const uint16_t*>(a.x) + tok * D + sl * DS : nullptr;
+    Tile<DS> tile;
+    values_load<DS>(src, tile);
+    values_compute<BITS, DT, DS>(tile, src, a.codes + tok * (D * BITS / 8) + sl * (DS * BITS / 8),
+                                 a.scale + tok * (D / kGroup) + sl * (DS / kGroup), a.zero + tok * (D / kGroup) + sl * (DS / kGroup));
 }
 
 // ---------------------------------------------------------------- append + flush
@@ -164,49 +441,76 @@ __device__ __forceinline__ SeqState seq_state(const AppendArgs& a, int b, int ca
     return s;
 }
 
-// One CTA per (group slot, kv head, sequence): quantizes the gi-th group that
-// this append makes leave the residual window. Tokens older than kv_len come
-// from the ring, newer ones straight from the caller's new-token buffers.
-template <int BITS, int DT>
-__global__ void __launch_bounds__(kThreads) append_pack_kernel(AppendArgs a) {
-    __shared__ __align__(16) uint16_t tk[kGroup * (kMaxHeadDim + kPad)];
-    __shared__ __align__(16) uint16_t tv[kGroup * (kMaxHeadDim + kPad)];
-    __shared__ float s_s[kMaxHeadDim], s_z[kMaxHeadDim];
-    const int gi = blockIdx.x, h = blockIdx.y, b = blockIdx.z, D = a.D;
+// Work units of append_pack_kernel: (group that this append makes leave the residual
+// window, keys or values, channel slice); grid (warp runs, kv head, sequence), each warp
+// taking every (gridDim.x * kWarps)-th unit of its (head, sequence). Tokens older than
+// kv_len come from the ring, newer ones straight from the caller's buffers.
+constexpr int kUnitsPerWarp = 32;
+
+template <int BITS, int DT, int DS>
+__global__ void __launch_bounds__(kThreads, 3) append_pack_kernel(AppendArgs a) {
+    const int h = blockIdx.y, b = blockIdx.z, D = a.D, nsl = D / DS;
     const kivi_seq& sq = a.seqs[b];
     const int cap = sq.cap_tokens;
     const SeqState st = seq_state(a, b, cap);
     if (!st.ok) {
-        if (gi == 0 && h == 0 && threadIdx.x == 0) {
+        if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) {
             const bool len_bad = st.L < 0 || st.L1 < st.L || st.L1 - st.L > a.max_new;
             set_status(a.status, len_bad ? KIVI_ERR_LENGTH : KIVI_ERR_CAPACITY);
         }
         return;
     }
-    const int64_t p0 = st.np0 + static_cast<int64_t>(gi) * kGroup;  // first token of the group
-    if (p0 >= st.np1) return;
+    const int64_t n_units = (st.np1 - st.np0) / kGroup * 2 * nsl;
     const int ring = a.R + kGroup;
     const int64_t n = st.L1 - st.L;
-    const uint16_t* kres = static_cast<const uint16_t*>(sq.k_res) + static_cast<int64_t>(h) * ring * D;
-    const uint16_t* vres = static_cast<const uint16_t*>(sq.v_res) + static_cast<int64_t>(h) * ring * D;
-    const uint16_t* knew = static_cast<const uint16_t*>(a.k_new[b]);
-    const uint16_t* vnew = static_cast<const uint16_t*>(a.v_new[b]);
-    auto src = [&](const uint16_t* res, const uint16_t* nw, int t) -> const uint16_t* {
-        const int64_t p = p0 + t;
-        if (p < st.L) return res + (p % ring) * D;
-        return nw + (static_cast<int64_t>(h) * n + (p - st.L)) * D;
-    };
-    stage_tile(tk, D, kGroup, [&](int t) { return src(kres, knew, t); });
-    stage_tile(tv, D, kGroup, [&](int t) { return src(vres, vnew, t); });
-    __syncthreads();
     const int row_bytes = D * BITS / 8;
-    const int64_t tok = static_cast<int64_t>(h) * cap + p0;
-    const int64_t kg = static_cast<int64_t>(h) * (cap / kGroup) + p0 / kGroup;
-    quantize_key_group<BITS, DT>(tk, D, sq.k_codes + tok * row_bytes, sq.k_scale + kg * D, sq.k_zero + kg * D,
-                                 s_s, s_z);
-    __syncthreads();
-    quantize_value_rows<BITS, DT>(tv, D, kGroup, sq.v_codes + tok * row_bytes, sq.v_scale + tok * (D / kGroup),
-                                  sq.v_zero + tok * (D / kGroup), s_s, s_z);
+    const int lane = threadIdx.x & 31;
+    // unit -> (group, keys or values, slice); a warp's units all have the same side,
+    // since the stride between them is a multiple of 2 * nsl only in the group index
+    auto slice_of = [&](int64_t unit) { return static_cast<int>(unit % nsl); };
+    auto group_pos = [&](int64_t unit) { return st.np0 + (unit / (2 * nsl)) * kGroup; };
+    // row of position p0 + t at the slice's first channel
+    auto row_at = [&](const void* res, const void* nw, int64_t p0, int sl, int t) -> const uint16_t* {
+        const int64_t p = p0 + t;
+        if (p < st.L) {
+            int slot = static_cast<int>(p0 % ring) + t;
+            slot = slot >= ring ? slot - ring : slot;
+            return static_cast<const uint16_t*>(res) + (static_cast<int64_t>(h) * ring + slot) * D + sl * DS;
+        }
+        return static_cast<const uint16_t*>(nw) + (static_cast<int64_t>(h) * n + (p - st.L)) * D + sl * DS;
+    };
+    auto load = [&](int64_t unit, bool is_v, Tile<DS>& tile) {
+        const int sl = slice_of(unit);
+        const int64_t p0 = group_pos(unit);
+        if (is_v) values_load<DS>(row_at(sq.v_res, a.v_new[b], p0, sl, lane), tile);
+        else keys_load<DS>([&](int t) { return row_at(sq.k_res, a.k_new[b], p0, sl, t); }, p0 >= st.L, D, tile);
+    };
+    auto compute = [&](int64_t unit, bool is_v, const Tile<DS>& tile) {
+        const int sl = slice_of(unit);
+        const int64_t p0 = group_pos(unit);
+        const int64_t tok = static_cast<int64_t>(h) * cap + p0;
+        if (!is_v) {
+            const int64_t kg = static_cast<int64_t>(h) * (cap / kGroup) + p0 / kGroup;
+            keys_compute<BITS, DT, DS>(tile, [&](int t) { return row_at(sq.k_res, a.k_new[b], p0, sl, t); },
+                                       sq.k_codes + tok * row_bytes + sl * (DS * BITS / 8), row_bytes,
+                                       sq.k_scale + kg * D + sl * DS, sq.k_zero + kg * D + sl * DS);
+        } else {
+            const int64_t tt = tok + lane;
+            values_compute<BITS, DT, DS>(tile, row_at(sq.v_res, a.v_new[b], p0, sl, lane),
+                                         sq.v_codes + tt * row_bytes + sl * (DS * BITS / 8),
+                                         sq.v_scale + tt * (D / kGroup) + sl * (DS / kGroup),
+                                         sq.v_zero + tt * (D / kGroup) + sl * (DS / kGroup));
+        }
+    };
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarps;
+    int64_t unit = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    if (unit >= n_units) return;
+    for (; unit < n_units; unit += stride) {
+        Tile<DS> cur;
+        const bool is_v = (unit / nsl) % 2 != 0;
+        load(unit, is_v, cur);
+        compute(unit, is_v, cur);
+    }
 }
 
 // One CTA per sequence: writes the new tokens that stay in the residual window
@@ -244,38 +548,52 @@ __global__ void __launch_bounds__(256) append_ring_kernel(AppendArgs a) {
     if (threadIdx.x == 0) a.kv_len[b] = static_cast<int32_t>(st.L1);
 }
 
+// Calls f.template operator()<BITS, DT, DS>() for the runtime bit width, input type and slice width.
+template <typename F>
+cudaError_t dispatch(int bits, int dtype, int D, F f) {
+    const int ds = slice_width(D);
+#define KIVI_DS(B, T) \
+    return ds == 64 ? f.template operator()<B, T, 64>() : f.template operator()<B, T, 32>();
+    if (bits == 2 && dtype == KIVI_F16) { KIVI_DS(2, KIVI_F16) }
+    if (bits == 2) { KIVI_DS(2, KIVI_BF16) }
+    if (dtype == KIVI_F16) { KIVI_DS(4, KIVI_F16) }
+    KIVI_DS(4, KIVI_BF16)
+#undef KIVI_DS
+}
+
+int64_t blocks_for(int64_t warps) { return (warps + kWarps - 1) / kWarps; }
+
 }  // namespace
 
 cudaError_t launch_quant_keys(const CodecArgs& a, cudaStream_t stream) {
     if (a.n_streams == 0 || a.n_tokens == 0) return cudaSuccess;
-    const dim3 grid(a.n_tokens / kGroup, a.n_streams);
-    if (a.bits == 2 && a.dtype == KIVI_F16) quant_keys_kernel<2, KIVI_F16><<<grid, kThreads, 0, stream>>>(a);
-    else if (a.bits == 2) quant_keys_kernel<2, KIVI_BF16><<<grid, kThreads, 0, stream>>>(a);
-    else if (a.dtype == KIVI_F16) quant_keys_kernel<4, KIVI_F16><<<grid, kThreads, 0, stream>>>(a);
-    else quant_keys_kernel<4, KIVI_BF16><<<grid, kThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    const int64_t units = static_cast<int64_t>(a.n_streams) * (a.n_tokens / kGroup) * (a.D / slice_width(a.D));
+    return dispatch(a.bits, a.dtype, a.D, [&]<int B, int T, int DS>() {
+        quant_keys_kernel<B, T, DS><<<static_cast<unsigned>(blocks_for(units)), kThreads, 0, stream>>>(a);
+        return cudaGetLastError();
+    });
 }
 
 cudaError_t launch_quant_values(const CodecArgs& a, cudaStream_t stream) {
     if (a.n_streams == 0 || a.n_tokens == 0) return cudaSuccess;
-    const dim3 grid((a.n_tokens + kGroup - 1) / kGroup, a.n_streams);
-    if (a.bits == 2 && a.dtype == KIVI_F16) quant_values_kernel<2, KIVI_F16><<<grid, kThreads, 0, stream>>>(a);
-    else if (a.bits == 2) quant_values_kernel<2, KIVI_BF16><<<grid, kThreads, 0, stream>>>(a);
-    else if (a.dtype == KIVI_F16) quant_values_kernel<4, KIVI_F16><<<grid, kThreads, 0, stream>>>(a);
-    else quant_values_kernel<4, KIVI_BF16><<<grid, kThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    const int64_t runs = (a.n_tokens + kGroup - 1) / kGroup;
+    const int64_t units = static_cast<int64_t>(a.n_streams) * runs * (a.D / slice_width(a.D));
+    return dispatch(a.bits, a.dtype, a.D, [&]<int B, int T, int DS>() {
+        quant_values_kernel<B, T, DS><<<static_cast<unsigned>(blocks_for(units)), kThreads, 0, stream>>>(a);
+        return cudaGetLastError();
+    });
 }
 
 cudaError_t launch_append_flush(const AppendArgs& a, cudaStream_t stream) {
     if (a.nseq == 0) return cudaSuccess;
     const int max_groups = (a.max_new + kGroup - 1) / kGroup;
     if (max_groups > 0) {
-        const dim3 grid(max_groups, a.H, a.nseq);
-        if (a.bits == 2 && a.dtype == KIVI_F16) append_pack_kernel<2, KIVI_F16><<<grid, kThreads, 0, stream>>>(a);
-        else if (a.bits == 2) append_pack_kernel<2, KIVI_BF16><<<grid, kThreads, 0, stream>>>(a);
-        else if (a.dtype == KIVI_F16) append_pack_kernel<4, KIVI_F16><<<grid, kThreads, 0, stream>>>(a);
-        else append_pack_kernel<4, KIVI_BF16><<<grid, kThreads, 0, stream>>>(a);
-        const cudaError_t e = cudaGetLastError();
+        const int64_t units = static_cast<int64_t>(max_groups) * 2 * (a.D / slice_width(a.D));
+        const dim3 grid(static_cast<unsigned>(blocks_for((units + kUnitsPerWarp - 1) / kUnitsPerWarp)), a.H, a.nseq);
+        const cudaError_t e = dispatch(a.bits, a.dtype, a.D, [&]<int B, int T, int DS>() {
+            append_pack_kernel<B, T, DS><<<grid, kThreads, 0, stream>>>(a);
+            return cudaGetLastError();
+        });
         if (e != cudaSuccess) return e;
     }
     append_ring_kernel<<<a.nseq, 256, 0, stream>>>(a);

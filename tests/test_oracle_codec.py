@@ -190,3 +190,42 @@ def test_packing_layout_2bit(oracle_lib):
     # byte 0 holds channels 0..3 = codes (0, 3, 1, 1) -> 0b01_01_11_00
     assert codes[0, 0, 0] == 0b01011100
     assert np.all(codes[0, 0, 1:] == 0b01010101)
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+def test_signed_zero_extreme_takes_first_seen(oracle_lib, dtype):
+    """Where a group's minimum (or maximum) is a zero, z (or s) follows the zero seen
+    first in scan order: tokens for keys, channels for values (the reading that
+    ties keep the first value seen)."""
+    name = "bf16" if dtype == BF16 else "f16"
+    D = 32
+    cfg = oracle.Cfg(bits=2, head_dim=D, dtype=dtype)
+    x = np.abs(np.linspace(0.5, 3.0, 32))[:, None] * np.ones((1, D))    # [T=32][D], all > 0
+    x[4, :] = -0.0
+    x[9, :] = 0.0
+    x[4, 1] = 0.0            # channel 1: +0 first (token 4), -0 never
+    x[9, 2] = -0.0           # channel 2: -0 at token 4 and token 9
+    xb = to_dtype_bits(x[None], name)
+    _, _, zb = oracle.quant_keys(cfg, xb)
+    zbits = np.asarray(zb, np.uint16)[0, 0]
+    assert zbits[0] == 0x8000 and zbits[1] == 0x0000 and zbits[2] == 0x8000
+    # values: channel order within a 32-channel group; all <= 0, so the maximum is a zero
+    v = -np.abs(np.linspace(0.5, 3.0, 32))[None, :] * np.ones((3, 1))   # [T=3][D]
+    v[0, 7], v[0, 20] = 0.0, -0.0
+    v[1, 7], v[1, 20] = -0.0, 0.0
+    v[2, 3] = -0.0
+    vb = to_dtype_bits(v[None], name)
+    _, sb, zb = oracle.quant_values(cfg, vb)
+    mx_minus_mn = f16(sb)[0, :, 0] * 3
+    assert np.allclose(mx_minus_mn, 3.0, rtol=2.0 ** -9)
+    # min is -3 in every row; the stored zero is the fp16 of the minimum, the sign of the
+    # maximum zero shows only through s, which is the same for either sign
+    assert np.all(f16(zb)[0, :, 0] == -3.0)
+    # keys again with every token of a channel a zero: the first token's sign wins
+    y = np.zeros((32, D))
+    y[0, :D // 2] = -0.0
+    y[1:, D // 2:] = -0.0
+    _, sb, zb = oracle.quant_keys(cfg, to_dtype_bits(y[None], name))
+    zbits = np.asarray(zb, np.uint16)[0, 0]
+    assert np.all(zbits[:D // 2] == 0x8000) and np.all(zbits[D // 2:] == 0x0000)
+    assert np.all(np.asarray(sb, np.uint16) == 0)
