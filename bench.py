@@ -79,6 +79,14 @@ def attn_bytes(wl, lengths, bits):
     return total
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per (token, kv head) of one
+# decode launch, from an ncu capture of the kernel in its current version on the 8-sequence
+# case of the Llama-3-8B GQA workload (2-bit, bf16): 208.69 MB for 8 x 8 x 32772 units.
+# Keyed by (kernel, bits, query group, input dtype); a configuration without an entry
+# reports traffic as null. Profile summary: profiles/decode_kernels_llama3-8b-gqa_b8_ctx32768.md.
+NCU_TRAFFIC_BYTES_PER_UNIT = {("decode_mma_kernel", 2, 4, "bf16"): 208_691_456 / (8 * 8 * 32772)}
+
+
 def reduce_max(x: float, device=None) -> float:
     """Max of x over the ranks of the default process group (x itself without one)."""
     import torch
@@ -292,12 +300,14 @@ def run_gpu(args, rank, world, local_rank):
     lens_per_step = [[L + args.warmup + i + 1 for L in L0s] for i in range(args.steps)]
     kv_tokens = sum(sum(ls) for ls in lens_per_step)
     bytes_per_step = [attn_bytes(wl, ls, bits) for ls in lens_per_step]
+    units_per_step = [wl.num_kv_heads * sum(ls) for ls in lens_per_step]
 
     # ------------------------------------------------------------ end to end through the public API
     e2e = run_e2e(args, cache, wl, device, [L + n_steps for L in L0s], max_len_final + args.steps, out)
 
     res = {
         "total_ms": total_ms, "attn_ms": attn_ms, "kv_tokens": kv_tokens, "attn_bytes": bytes_per_step,
+        "attn_units": units_per_step,
         "clocks": clk.summary(), "e2e": e2e, "launches_per_step": 3, "cap": cap, "flush": flush,
         "prefill": {"ms": prefill_ms, "algorithmic_bytes": prefill_bytes,
                     "GBps": prefill_bytes / (prefill_ms / 1e3) / 1e9 if prefill_ms > 0 else None},
@@ -442,7 +452,10 @@ def main():
     achieved = avg_bytes / (avg_attn_ms / 1e3) / 1e9
     peak, peak_kind = measured_hbm_peak()
     # the decode kernel the library picks: tensor-core path for query groups of 1, 2 or 4
-    kernel = "decode_mma_kernel" if config["q_heads"] // config["kv_heads"] in (1, 2, 4) else "decode_split_kernel"
+    group = config["q_heads"] // config["kv_heads"]
+    kernel = "decode_mma_kernel" if group in (1, 2, 4) else "decode_split_kernel"
+    per_unit = NCU_TRAFFIC_BYTES_PER_UNIT.get((kernel, config["bits"], group, config["input_dtype"]))
+    traffic = per_unit * sum(res["attn_units"]) / len(res["attn_units"]) if per_unit else None
     line = {
         "metric": METRIC, "value": value, "unit": "KV-tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -451,7 +464,8 @@ def main():
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
                      "algorithmic_bytes_per_launch": avg_bytes, "avg_launch_ms": avg_attn_ms,
-                     "traffic": None},
+                     "traffic": traffic,
+                     "traffic_source": "ncu capture at 8 sequences, scaled by (token, kv head) units" if per_unit else None},
         "attn_kv_tokens_per_s": (res["kv_tokens"] / args.steps) / (avg_attn_ms / 1e3),
         "e2e": {k: res["e2e"][k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")},
         "gpu_launches": res["launches_per_step"] * args.steps,
