@@ -81,9 +81,9 @@ def test_split_count_invariance(dtype):
     terms sit at that floor.)"""
     wl = synth.Workload("splits", 2, 8, 2, 128, (9000, 5000), dtype, seed=8)
     cache, refs = build(wl, 2, 9024)
-    a, _ = check_decode(wl, cache, refs, max_kv_len=9000)          # several splits
-    b, _ = check_decode(wl, cache, refs, max_kv_len=400000)        # 8192-token splits
-    c, _ = check_decode(wl, cache, refs, max_kv_len=4096 + 9000)   # another split size
+    a, _ = check_decode(wl, cache, refs, max_kv_len=9000)          # 2048-token splits (5 packed)
+    b, _ = check_decode(wl, cache, refs, max_kv_len=400000)        # 4096-token splits (3 packed)
+    c, _ = check_decode(wl, cache, refs, max_kv_len=24000)         # 3072-token splits (3 packed)
     assert np.max(np.abs(a - b)) <= 1e-4 and np.max(np.abs(a - c)) <= 1e-4
 
 
