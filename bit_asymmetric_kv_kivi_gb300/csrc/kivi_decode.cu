@@ -148,22 +148,29 @@ struct CodeShift {
 
 // One 32-token tile of residual tokens [ts, min(ts+32, t1)) for one warp, lane = token:
 // scores against the widened stored keys, online-softmax update and value accumulation
-// into the lane-layout state (lane owns channels [4 lane, 4 lane + 4)).
+// into the lane-layout state (lane owns channels [4 lane, 4 lane + 4)). Every global
+// load of the tile is issued before its first use (the key row, then the lane's value
+// slices of all 32 tokens), so a tile waits for memory twice, not once per token.
 template <int DT, int GQ>
 __device__ __forceinline__ void residual_tile(const uint16_t* kres, const uint16_t* vres, int ring, int64_t ts,
                                               int64_t t1, const float* qs, int lane, float (&m)[GQ], float (&l)[GQ],
                                               float (&acc)[GQ][kCpl]) {
     const int64_t p = ts + lane;
     const bool valid = p < t1;
+    const int ntok = static_cast<int>(t1 - ts < 32 ? t1 - ts : 32);
+    const int slot0 = static_cast<int>(ts % ring);
     float sc[GQ];
 #pragma unroll
     for (int hh = 0; hh < GQ; ++hh) sc[hh] = 0.0f;
-    if (valid) {
-        const uint4* krow = reinterpret_cast<const uint4*>(kres + (p % ring) * kD);
-#pragma unroll 4
+    {
+        uint4 kr[kD / 8];
+        const int slot = slot0 + lane >= ring ? slot0 + lane - ring : slot0 + lane;
+        const uint4* krow = reinterpret_cast<const uint4*>(kres + static_cast<int64_t>(slot) * kD);
+#pragma unroll
+        for (int w = 0; w < kD / 8; ++w) kr[w] = valid ? __ldg(krow + w) : make_uint4(0, 0, 0, 0);
+#pragma unroll
         for (int w = 0; w < kD / 8; ++w) {
-            const uint4 v4 = __ldg(krow + w);
-            const uint32_t words[4] = {v4.x, v4.y, v4.z, v4.w};
+            const uint32_t words[4] = {kr[w].x, kr[w].y, kr[w].z, kr[w].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float k0 = widen<DT>(static_cast<uint16_t>(words[e] & 0xffffu));
@@ -173,6 +180,13 @@ __device__ __forceinline__ void residual_tile(const uint16_t* kres, const uint16
                 for (int hh = 0; hh < GQ; ++hh) sc[hh] = fmaf(qs[hh * kD + d + 1], k1, fmaf(qs[hh * kD + d], k0, sc[hh]));
             }
         }
+    }
+    uint2 vr[32];
+#pragma unroll
+    for (int tau = 0; tau < 32; ++tau) {
+        const int slot = slot0 + tau >= ring ? slot0 + tau - ring : slot0 + tau;
+        vr[tau] = tau < ntok ? __ldg(reinterpret_cast<const uint2*>(vres + static_cast<int64_t>(slot) * kD + lane * kCpl))
+                             : make_uint2(0, 0);
     }
     float pr[GQ];
 #pragma unroll
@@ -186,16 +200,15 @@ __device__ __forceinline__ void residual_tile(const uint16_t* kres, const uint16
         for (int c = 0; c < kCpl; ++c) acc[hh][c] *= alpha;
         m[hh] = mnew;
     }
-    const int ntok = static_cast<int>(t1 - ts < 32 ? t1 - ts : 32);
-    for (int tau = 0; tau < ntok; ++tau) {
-        const uint2 raw = __ldg(reinterpret_cast<const uint2*>(vres + ((ts + tau) % ring) * kD + lane * kCpl));
-        const float v[kCpl] = {widen<DT>(static_cast<uint16_t>(raw.x & 0xffffu)),
-                               widen<DT>(static_cast<uint16_t>(raw.x >> 16)),
-                               widen<DT>(static_cast<uint16_t>(raw.y & 0xffffu)),
-                               widen<DT>(static_cast<uint16_t>(raw.y >> 16))};
+#pragma unroll
+    for (int tau = 0; tau < 32; ++tau) {
+        const float v[kCpl] = {widen<DT>(static_cast<uint16_t>(vr[tau].x & 0xffffu)),
+                               widen<DT>(static_cast<uint16_t>(vr[tau].x >> 16)),
+                               widen<DT>(static_cast<uint16_t>(vr[tau].y & 0xffffu)),
+                               widen<DT>(static_cast<uint16_t>(vr[tau].y >> 16))};
 #pragma unroll
         for (int hh = 0; hh < GQ; ++hh) {
-            const float pt = __shfl_sync(kFull, pr[hh], tau);
+            const float pt = __shfl_sync(kFull, pr[hh], tau);   // 0 for tokens past t1
 #pragma unroll
             for (int c = 0; c < kCpl; ++c) acc[hh][c] = fmaf(pt, v[c], acc[hh][c]);
         }
@@ -277,6 +290,129 @@ __device__ __forceinline__ void finish_split(const DecodeArgs& a, int b, int h, 
         out_bh[i] = num / den;
     }
     if (tid == 0) a.counters[static_cast<int64_t>(b) * a.H + h] = 0;
+}
+
+// ---------------------------------------------------------------- persistent schedule
+
+// decode_mma_kernel runs one CTA per resident slot. The work of all (sequence, kv head)
+// streams, sequence-major, is a row of units: a stream's packed key groups (one unit
+// each) then its residual tokens in 32-token tiles (kResidualWeight units each, about
+// their cost relative to a group). CTA c takes units [c U / Ceff, (c+1) U / Ceff), which
+// may span streams; each stream is charged kStreamOverhead units ahead of its groups for its
+// setup and merge, which no segment holds. The part of a stream's groups (or of its tiles) that one CTA holds is
+// a segment; its partial record sits at index 2 s + part + c (s the stream, part 0 for
+// groups and 1 for tiles), unique because each step to the next segment raises the
+// stream, the part or the CTA, and below 2 S + Ceff. The last CTA to finish a segment of
+// a stream (an atomic ticket, no waiting) merges the stream's records.
+constexpr int kResidualWeight = 4;
+constexpr int kStreamOverhead = 32;      // units charged per stream for its setup and merge
+constexpr int kMinUnitsPerCta = 8;
+constexpr int kMaxCtas = 1024;           // bound on the grid, sizes the workspace
+
+struct SeqWork {
+    int64_t L, np, ng, rt, u;   // tokens, packed tokens, packed groups, residual tiles, units
+    bool bad;
+};
+
+__device__ __forceinline__ SeqWork seq_work(const DecodeArgs& a, int b) {
+    SeqWork w;
+    w.L = a.kv_len[b];
+    w.bad = w.L < 0 || w.L > a.max_kv_len || n_packed(w.L, a.R) > a.seqs[b].cap_tokens;
+    w.np = w.ng = w.rt = w.u = 0;
+    if (w.bad || w.L == 0) return w;
+    w.np = n_packed(w.L, a.R);
+    w.ng = w.np / kGroup;
+    w.rt = (w.L - w.np + kGroup - 1) / kGroup;
+    w.u = kStreamOverhead + w.ng + kResidualWeight * w.rt;
+    return w;
+}
+
+// The CTA whose range holds unit x: the largest c with c U / Ceff <= x.
+__device__ __forceinline__ int64_t owner(int64_t x, int64_t U, int64_t Ceff) { return ((x + 1) * Ceff - 1) / U; }
+
+// The segments of one stream: CTAs [cg0, cg1] hold its groups, [cr0, cr1] its tiles
+// (empty ranges when first > last).
+struct StreamSegs {
+    int64_t s, cg0, cg1, cr0, cr1;
+    int nseg;
+};
+
+// Merges the four warps' states of one segment (red_* in shared memory, filled and
+// synchronized by the caller), then writes the output (the stream's only segment) or
+// the segment's partial record; the last CTA of the stream to arrive merges them all.
+// An empty state (m = -inf, l = 0) contributes nothing. scratch: shared memory for
+// GQ * nseg floats from scratch[0] and GQ before it, free once red_* have been read.
+template <int GQ>
+__device__ __forceinline__ void finish_segment(const DecodeArgs& a, const StreamSegs& ss, int64_t seg, float* out_s,
+                                               const float* red_m, const float* red_l, const float* red_acc,
+                                               int* s_last, float* scratch) {
+    const int tid = threadIdx.x;
+    constexpr int64_t rec = kD + 4;
+    for (int i = tid; i < GQ * kD; i += kThreads) {
+        const int hh = i / kD, d = i - hh * kD;
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w * GQ + hh]);
+        float den = 0.0f, num = 0.0f;
+        if (M != -CUDART_INF_F) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float f = exp2f(red_m[w * GQ + hh] - M);
+                den = fmaf(red_l[w * GQ + hh], f, den);
+                num = fmaf(red_acc[(w * GQ + hh) * kD + d], f, num);
+            }
+        }
+        if (ss.nseg == 1) {
+            out_s[i] = num / den;
+        } else {
+            float* r = a.partials + (seg * GQ + hh) * rec;
+            r[d] = num;
+            if (d == 0) {
+                r[kD] = M;
+                r[kD + 1] = den;
+            }
+        }
+    }
+    if (ss.nseg == 1) return;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) *s_last = atomicAdd(&a.counters[ss.s], 1) == ss.nseg - 1;
+    __syncthreads();
+    if (!*s_last) return;
+    __threadfence();
+    // the stream's records: k-th segment -> record index; one warp per head finds the
+    // running max and the weights exp2(m - M) of all records at once (loads in parallel),
+    // then every output sums its records with independent loads
+    const int ng_cnt = static_cast<int>(ss.cg1 - ss.cg0 + 1);
+    auto rec_at = [&](int k, int hh) {
+        const int64_t idx = k < ng_cnt ? 2 * ss.s + ss.cg0 + k : 2 * ss.s + 1 + ss.cr0 + (k - ng_cnt);
+        return a.partials + (idx * GQ + hh) * rec;
+    };
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int hh = warp; hh < GQ; hh += kWarps) {
+        float M = -CUDART_INF_F;
+        for (int k = lane; k < ss.nseg; k += 32) M = fmaxf(M, __ldcg(rec_at(k, hh) + kD));
+        M = warp_max(M);
+        float den = 0.0f;
+        for (int k = lane; k < ss.nseg; k += 32) {
+            const float* r = rec_at(k, hh);
+            const float ms = __ldcg(r + kD);
+            const float f = ms == -CUDART_INF_F ? 0.0f : exp2f(ms - M);
+            scratch[k * GQ + hh] = f;
+            den = fmaf(__ldcg(r + kD + 1), f, den);
+        }
+        den = warp_sum(den);
+        if (lane == 0) scratch[-GQ + hh] = den;
+    }
+    __syncthreads();
+    for (int i = tid; i < GQ * kD; i += kThreads) {
+        const int hh = i / kD, d = i - hh * kD;
+        float num = 0.0f;
+#pragma unroll 8
+        for (int k = 0; k < ss.nseg; ++k) num = fmaf(scratch[k * GQ + hh], __ldcg(rec_at(k, hh) + d), num);
+        out_s[i] = num / scratch[-GQ + hh];
+    }
+    if (tid == 0) a.counters[ss.s] = 0;
 }
 
 // ---------------------------------------------------------------- CUDA-core kernel
@@ -434,7 +570,6 @@ struct MmaLayout {
     // that the four spans read together fall on distinct shared-memory banks
     static constexpr int kMetaPad = 320;
     static constexpr int kStage = 2 * kGroup * kRowBytes + 2 * kMetaPad + 2 * 256;
-    static constexpr int kChunks = (2 * kGroup * kRowBytes + 4 * 256) / 16;   // 16-byte cp.async pieces
     static constexpr int kNslot = 16 / BITS;                             // code pairs per 32-bit word
     static constexpr int kStageBytes = kWarps * kStages * kStage;
     static constexpr int kSmemBytes(int gq) {
@@ -442,77 +577,82 @@ struct MmaLayout {
     }
 };
 
-// Splits: ceil(n_packed / chunk) ranges of whole key groups, then one split for the
-// residual tokens. Thread (gid = lane / 4, t = lane % 4) follows the mma.sync
+// Thread (gid = lane / 4, t = lane % 4) follows the mma.sync
 // m16n8k16 fragment layout. Logical k index 2t+8e+{0,1} of key k-step ks maps to
 // the code pair of slot s = 2 ks + e in thread t's 32-channel span of the row:
 // channels 32t + m*2*NSLOT + i and + NSLOT, with m = s / NSLOT, i = s % NSLOT.
+struct MmaSmem {
+    unsigned char* stages;   // [warp][stage][STAGE]
+    float* qs;               // [GQ][kD]
+    float* pt_all;           // [warp][4][kPtLd]
+    float* red_m;            // [warp][GQ]
+    float* red_l;            // [warp][GQ]
+    int* s_misc;             // [8]
+    float* red_acc;          // [warp][GQ][kD], aliases the stages once they are drained
+    __device__ MmaSmem(unsigned char* smem, int stage_bytes, int gq) {
+        stages = smem;
+        qs = reinterpret_cast<float*>(smem + stage_bytes);
+        pt_all = qs + gq * kD;
+        red_m = pt_all + kWarps * 4 * kPtLd;
+        red_l = red_m + kWarps * gq;
+        s_misc = reinterpret_cast<int*>(red_l + kWarps * gq);
+        red_acc = reinterpret_cast<float*>(smem);
+    }
+};
+
+// q of stream (b, h) into shared memory, scaled by softmax_scale * log2(e); the caller's
+// earlier use of qs must be over (a CTA barrier) before this runs.
+template <int DT, int GQ>
+__device__ __forceinline__ void load_q(const DecodeArgs& a, float* qs, int b, int h) {
+    const uint16_t* q = static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(b) * a.Hq + h * GQ) * kD;
+    for (int i = threadIdx.x; i < GQ * kD; i += kThreads) qs[i] = widen<DT>(q[i]) * a.scale_log2;
+}
+
+// Residual tiles [t0, t1) of stream (b, h) (tile i = tokens np + 32 i ..), lane-layout
+// CUDA-core path; leaves the merged warp states in red_* (synchronized).
+template <int DT, int GQ>
+__device__ __forceinline__ void residual_segment(const DecodeArgs& a, const MmaSmem& sm, int b, int h,
+                                                 const SeqWork& w, int64_t t0, int64_t t1) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, ring = a.R + kGroup;
+    const kivi_seq& sq = a.seqs[b];
+    float m[GQ], l[GQ], acc[GQ][kCpl];
+#pragma unroll
+    for (int hh = 0; hh < GQ; ++hh) {
+        m[hh] = -CUDART_INF_F;
+        l[hh] = 0.0f;
+#pragma unroll
+        for (int c = 0; c < kCpl; ++c) acc[hh][c] = 0.0f;
+    }
+    const uint16_t* kres = static_cast<const uint16_t*>(sq.k_res) + static_cast<int64_t>(h) * ring * kD;
+    const uint16_t* vres = static_cast<const uint16_t*>(sq.v_res) + static_cast<int64_t>(h) * ring * kD;
+    for (int64_t i = t0 + warp; i < t1; i += kWarps) {
+        residual_tile<DT, GQ>(kres, vres, ring, w.np + kGroup * i, w.L, sm.qs, lane, m, l, acc);
+        __syncwarp();
+    }
+    store_lane_state<GQ>(warp, lane, m, l, acc, sm.red_m, sm.red_l, sm.red_acc);
+    __syncthreads();
+}
+
+// Key groups [ga, gb) of stream (b, h) on the tensor cores; leaves the merged warp states
+// in red_* (synchronized). qs holds the stream's q.
 template <int BITS, int DT, int GQ>
-__global__ void __launch_bounds__(kThreads, BITS == 2 ? 3 : 2) decode_mma_kernel(DecodeArgs a) {
-    static_assert(GQ == 1 || GQ == 2 || GQ == 4, "one n8 tile holds hi and lo of up to four heads");
+__device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem& sm, int b, int h, int64_t ga,
+                                              int64_t gb) {
     using Lay = MmaLayout<BITS>;
     constexpr int RB = Lay::kRowBytes;
     constexpr int STAGE = Lay::kStage;
     constexpr int NSLOT = Lay::kNslot;
     constexpr int SHIFT = CodeShift<BITS>::kValue;
-
-    extern __shared__ __align__(16) unsigned char smem[];
-    unsigned char* stages = smem;                                               // [warp][stage][STAGE]
-    float* qs = reinterpret_cast<float*>(smem + Lay::kStageBytes);             // [GQ][kD]
-    float* pt_all = qs + GQ * kD;                                               // [warp][4][kPtLd]
-    float* red_m = pt_all + kWarps * 4 * kPtLd;                                 // [warp][GQ]
-    float* red_l = red_m + kWarps * GQ;                                         // [warp][GQ]
-    int* s_misc = reinterpret_cast<int*>(red_l + kWarps * GQ);                 // [8]
-    float* red_acc = reinterpret_cast<float*>(smem);                           // [warp][GQ][kD], after the loop
-
-    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int Hq = a.Hq, ring = a.R + kGroup;
     const kivi_seq& sq = a.seqs[b];
     const int cap = sq.cap_tokens;
-    const int64_t L = a.kv_len[b];
-    float* out_bh = a.out + (static_cast<int64_t>(b) * Hq + static_cast<int64_t>(h) * GQ) * kD;
-
-    const bool bad = L < 0 || L > a.max_kv_len || n_packed(L, a.R) > cap;
-    if (bad || L == 0) {
-        if (split == 0) {
-            for (int i = tid; i < GQ * kD; i += kThreads) out_bh[i] = bad ? CUDART_NAN_F : 0.0f;
-            if (bad && h == 0 && tid == 0) set_status(a.status, KIVI_ERR_LENGTH);
-        }
-        return;
-    }
-    const int64_t np = n_packed(L, a.R);
-    const int nsp = static_cast<int>((np + a.chunk - 1) / a.chunk);   // packed splits
-    const int nsplit = nsp + 1;                                         // + the residual split
-    if (split >= nsplit) return;
-
-    const uint16_t* q = static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(b) * Hq + h * GQ) * kD;
-    for (int i = tid; i < GQ * kD; i += kThreads) qs[i] = widen<DT>(q[i]) * a.scale_log2;
-    __syncthreads();
-
-    if (split == nsp) {
-        // ---------------- residual split: tokens [np, L), lane-layout CUDA-core path
-        float m[GQ], l[GQ], acc[GQ][kCpl];
-#pragma unroll
-        for (int hh = 0; hh < GQ; ++hh) {
-            m[hh] = -CUDART_INF_F;
-            l[hh] = 0.0f;
-#pragma unroll
-            for (int c = 0; c < kCpl; ++c) acc[hh][c] = 0.0f;
-        }
-        const uint16_t* kres = static_cast<const uint16_t*>(sq.k_res) + static_cast<int64_t>(h) * ring * kD;
-        const uint16_t* vres = static_cast<const uint16_t*>(sq.v_res) + static_cast<int64_t>(h) * ring * kD;
-        for (int64_t ts = np + 32 * warp; ts < L; ts += 32 * kWarps) {
-            residual_tile<DT, GQ>(kres, vres, ring, ts, L, qs, lane, m, l, acc);
-            __syncwarp();
-        }
-        store_lane_state<GQ>(warp, lane, m, l, acc, red_m, red_l, red_acc);
-        __syncthreads();
-        finish_split<GQ>(a, b, h, split, nsplit, out_bh, red_m, red_l, red_acc, &s_misc[0]);
-        return;
-    }
-
-    // ---------------- packed split: key groups [g0, g1)
+    unsigned char* stages = sm.stages;
+    float* qs = sm.qs;
+    float* pt_all = sm.pt_all;
+    float* red_m = sm.red_m;
+    float* red_l = sm.red_l;
+    int* s_misc = sm.s_misc;
+    float* red_acc = sm.red_acc;
     const int gid = lane >> 2, t = lane & 3;
     const int hh = gid >> 1, part = gid & 1;     // B column gid = (head hh, hi/lo part)
     const bool hv = GQ >= 4 || hh < GQ;   // this thread's B column belongs to a real head
@@ -556,8 +696,7 @@ __global__ void __launch_bounds__(kThreads, BITS == 2 ? 3 : 2) decode_mma_kernel
     for (int i = 0; i < 8; ++i) cv[i][0] = cv[i][1] = cv[i][2] = cv[i][3] = 0.0f;
     cz[0] = cz[1] = cz[2] = cz[3] = 0.0f;
 
-    const int64_t g0 = static_cast<int64_t>(split) * a.chunk / kGroup;
-    const int64_t g1 = min(static_cast<int64_t>(split + 1) * a.chunk, np) / kGroup;
+    const int64_t g0 = ga, g1 = gb;
     const int64_t gfirst = g0 + warp;
     const int n_my = gfirst < g1 ? static_cast<int>((g1 - gfirst + kWarps - 1) / kWarps) : 0;
     unsigned char* my_st = stages + warp * kStages * STAGE;
@@ -797,26 +936,187 @@ a0 = code_slot<BITS>(cw[0][w0], cws[0][w0], s0);
         }
     }
     __syncthreads();
-    finish_split<GQ>(a, b, h, split, nsplit, out_bh, red_m, red_l, red_acc, &s_misc[0]);
 }
 
 template <int BITS, int DT, int GQ>
-cudaError_t launch_mma(const DecodeArgs& a, dim3 grid, cudaStream_t stream) {
+__global__ void __launch_bounds__(kThreads, BITS == 2 ? 3 : 2) decode_mma_kernel(DecodeArgs a) {
+    static_assert(GQ == 1 || GQ == 2 || GQ == 4, "one n8 tile holds hi and lo of up to four heads");
+    extern __shared__ __align__(16) unsigned char smem[];
+    const MmaSmem sm(smem, MmaLayout<BITS>::kStageBytes, GQ);
+    int64_t* sched = reinterpret_cast<int64_t*>(smem);   // scan scratch: the stages are idle until the walk
+    const int tid = threadIdx.x;
+    const int C = gridDim.x, c = blockIdx.x, H = a.H;
+
+    // sequences without work: zeros for an empty one, NaN and a status for a bad length
+    for (int b = c; b < a.nseq; b += C) {
+        const SeqWork w = seq_work(a, b);
+        if (w.u != 0) continue;
+        float* o = a.out + static_cast<int64_t>(b) * a.Hq * kD;
+        for (int i = tid; i < a.Hq * kD; i += kThreads) o[i] = w.bad ? CUDART_NAN_F : 0.0f;
+        if (w.bad && tid == 0) set_status(a.status, KIVI_ERR_LENGTH);
+    }
+
+    // units before each thread's run of sequences (exclusive scan), the total U, and this
+    // CTA's range [lo, hi)
+    const int per = (a.nseq + kThreads - 1) / kThreads;
+    const int b_lo = tid * per < a.nseq ? tid * per : a.nseq;
+    const int b_hi = b_lo + per < a.nseq ? b_lo + per : a.nseq;
+    int64_t mine = 0;
+    for (int b = b_lo; b < b_hi; ++b) mine += static_cast<int64_t>(H) * seq_work(a, b).u;
+    // the walk state lives in shared memory and is read back (volatile) around each
+    // segment, so that the hot loops do not hold it in registers: lo, hi, U, Ceff, the
+    // first unit of sequence b, b, h (b = nseq ends the walk)
+    __shared__ int64_t walk[7];
+    volatile int64_t* vw = walk;
+    sched[tid] = mine;
+    __syncthreads();
+    if (tid == 0) {
+        vw[5] = a.nseq;
+        int64_t run = 0;
+        for (int i = 0; i < kThreads; ++i) {
+            const int64_t v = sched[i];
+            sched[i] = run;
+            run += v;
+        }
+        sched[kThreads] = run;
+    }
+    __syncthreads();
+    const int64_t U = sched[kThreads];
+    const int64_t by_size = U / kMinUnitsPerCta > 1 ? U / kMinUnitsPerCta : 1;
+    const int64_t Ceff = C < by_size ? C : by_size;
+    if (U == 0 || c >= Ceff) return;
+    const int64_t lo = c * U / Ceff, hi = (c + 1) * U / Ceff;
+    const int64_t start = sched[tid];
+    if (mine > 0 && lo >= start && lo < start + mine) {
+        int64_t p = start;
+        for (int b = b_lo; b < b_hi; ++b) {
+            const int64_t ub = static_cast<int64_t>(H) * seq_work(a, b).u;
+            if (lo < p + ub) {
+                vw[0] = lo;
+                vw[1] = hi;
+                vw[2] = U;
+                vw[3] = Ceff;
+                vw[4] = p;
+                vw[5] = b;
+                vw[6] = 0;
+                break;
+            }
+            p += ub;
+        }
+    }
+    __syncthreads();
+
+    // stream (vw[5], vw[6]) and the part of it this CTA holds: [x0, x1) in its units
+    // (x0, x1 count from the stream's first group; x1 <= x0: no work here)
+    struct Cur {
+        int b, h;
+        int64_t Ps, Ws, x0, x1;   // first unit of the stream and of its groups
+        SeqWork w;
+    };
+    auto current = [&]() {
+        Cur k;
+        k.b = static_cast<int>(vw[5]);
+        k.h = static_cast<int>(vw[6]);
+        k.w = seq_work(a, k.b);
+        k.Ps = vw[4] + k.h * k.w.u;
+        k.Ws = k.Ps + kStreamOverhead;
+        const int64_t lo_ = vw[0], hi_ = vw[1];
+        k.x0 = (lo_ > k.Ws ? lo_ : k.Ws) - k.Ws;
+        k.x1 = (hi_ < k.Ps + k.w.u ? hi_ : k.Ps + k.w.u) - k.Ws;
+        return k;
+    };
+    auto finish = [&](int part) {
+        const Cur k = current();
+        const int64_t U_ = vw[2], Ceff_ = vw[3];
+        StreamSegs ss;
+        ss.s = static_cast<int64_t>(k.b) * H + k.h;
+        ss.cg0 = owner(k.Ws, U_, Ceff_);
+        ss.cg1 = k.w.ng > 0 ? owner(k.Ws + k.w.ng - 1, U_, Ceff_) : ss.cg0 - 1;
+        ss.cr0 = owner(k.Ws + k.w.ng, U_, Ceff_);
+        ss.cr1 = k.w.rt > 0 ? owner(k.Ps + k.w.u - 1, U_, Ceff_) : ss.cr0 - 1;
+        ss.nseg = static_cast<int>((ss.cg1 - ss.cg0 + 1) + (ss.cr1 - ss.cr0 + 1));
+        float* out_s = a.out + (static_cast<int64_t>(k.b) * a.Hq + static_cast<int64_t>(k.h) * GQ) * kD;
+        finish_segment<GQ>(a, ss, 2 * ss.s + part + c, out_s, sm.red_m, sm.red_l, sm.red_acc, &sm.s_misc[0],
+                           reinterpret_cast<float*>(smem) + GQ * (kWarps + 1) * kD + GQ);
+    };
+
+    while (true) {
+        {
+            const int b = static_cast<int>(vw[5]);
+            if (b >= a.nseq || vw[4] >= vw[1]) break;
+        }
+        Cur k = current();
+        if (k.Ps >= vw[1]) break;
+        if (k.w.u != 0 && k.x1 > k.x0) {
+            if (k.x0 < k.w.ng) {
+                __syncthreads();   // the previous segment is done with qs and the shared arrays
+                load_q<DT, GQ>(a, sm.qs, k.b, k.h);
+                __syncthreads();
+                group_segment<BITS, DT, GQ>(a, sm, k.b, k.h, k.x0, k.x1 < k.w.ng ? k.x1 : k.w.ng);
+                finish(0);
+                k = current();
+            }
+            if (k.x1 > k.w.ng) {
+                const int64_t u0 = (k.x0 > k.w.ng ? k.x0 : k.w.ng) - k.w.ng, u1 = k.x1 - k.w.ng;
+                __syncthreads();
+                load_q<DT, GQ>(a, sm.qs, k.b, k.h);
+                __syncthreads();
+                residual_segment<DT, GQ>(a, sm, k.b, k.h, k.w, (u0 + kResidualWeight - 1) / kResidualWeight,
+                                         (u1 + kResidualWeight - 1) / kResidualWeight);
+                finish(1);
+            }
+        }
+        __syncthreads();   // every thread has read the walk state of this stream
+        if (tid == 0) {
+            const int b = static_cast<int>(vw[5]), h = static_cast<int>(vw[6]);
+            if (h + 1 < H) {
+                vw[6] = h + 1;
+            } else {
+                vw[4] = vw[4] + static_cast<int64_t>(H) * seq_work(a, b).u;
+                vw[5] = b + 1;
+                vw[6] = 0;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// Resident CTAs of a kernel on the current device (SM count x blocks per SM), cached per
+// device; at most kMaxCtas.
+template <typename K>
+int resident_ctas(K kernel, int smem, int* cache) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev] > 0) return cache[dev];
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem) != cudaSuccess) return 0;
+    int n = sms * (per_sm > 0 ? per_sm : 1);
+    n = n > kMaxCtas ? kMaxCtas : n;
+    cache[dev] = n;
+    return n;
+}
+
+template <int BITS, int DT, int GQ>
+cudaError_t launch_mma(const DecodeArgs& a, cudaStream_t stream) {
     constexpr int smem = MmaLayout<BITS>::kSmemBytes(GQ);
+    static int ctas[64] = {};
     const cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<BITS, DT, GQ>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    decode_mma_kernel<BITS, DT, GQ><<<grid, kThreads, smem, stream>>>(a);
+    const int n = resident_ctas(decode_mma_kernel<BITS, DT, GQ>, smem, ctas);
+    if (n <= 0) return cudaErrorInvalidValue;
+    decode_mma_kernel<BITS, DT, GQ><<<n, kThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
 template <int BITS, int DT>
-cudaError_t launch_gq(const DecodeArgs& a, dim3 grid, cudaStream_t stream) {
+cudaError_t launch_gq(const DecodeArgs& a, cudaStream_t stream) {
     switch (a.Hq / a.H) {
-        case 1: return launch_mma<BITS, DT, 1>(a, grid, stream);
-        case 2: return launch_mma<BITS, DT, 2>(a, grid, stream);
-        case 4: return launch_mma<BITS, DT, 4>(a, grid, stream);
-        case 8: decode_split_kernel<BITS, DT, 8><<<grid, kThreads, 0, stream>>>(a); break;
+        case 1: return launch_mma<BITS, DT, 1>(a, stream);
+        case 2: return launch_mma<BITS, DT, 2>(a, stream);
+        case 4: return launch_mma<BITS, DT, 4>(a, stream);
+        case 8: decode_split_kernel<BITS, DT, 8><<<dim3(a.max_splits, a.H, a.nseq), kThreads, 0, stream>>>(a); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -826,27 +1126,33 @@ cudaError_t launch_gq(const DecodeArgs& a, dim3 grid, cudaStream_t stream) {
 
 void decode_plan(int nseq, int H, int Hq, int D, int max_kv_len, int* chunk, int* max_splits,
                  size_t* counter_bytes, size_t* partial_bytes) {
-    // Split size: about an eighth of the longest sequence, in whole 256-token
-    // steps, between 2048 and 4096 tokens; one more split for the residual tokens.
-    // Below 2048 tokens (16 groups per warp) the per-CTA setup and merge dominate;
-    // measured on the workloads, 2048..4096 is within 1 % of the best fixed size.
+    *counter_bytes = ((static_cast<size_t>(nseq) * H * sizeof(int32_t) + 255) / 256) * 256;
+    const int gq = H > 0 ? Hq / H : 0;
+    if (gq == 1 || gq == 2 || gq == 4) {
+        // decode_mma_kernel: one record per segment, fewer than 2 S + kMaxCtas of them
+        *chunk = 0;
+        *max_splits = 0;
+        *partial_bytes = (2 * static_cast<size_t>(nseq) * H + kMaxCtas) * gq * (D + 4) * sizeof(float);
+        return;
+    }
+    // decode_split_kernel: splits of about an eighth of the longest sequence, in whole
+    // 256-token steps between 2048 and 4096 tokens (below that the per-CTA setup and merge
+    // dominate); the residual tokens are read inside the splits.
     const int64_t eighth = (static_cast<int64_t>(max_kv_len) + 7) / 8;
     int64_t c = ((eighth + 255) / 256) * 256;
     c = c < 2048 ? 2048 : (c > 4096 ? 4096 : c);
-    const int64_t ms = (max_kv_len <= 0 ? 1 : (max_kv_len + c - 1) / c) + 1;
+    const int64_t ms = max_kv_len <= 0 ? 1 : (max_kv_len + c - 1) / c;
     *chunk = static_cast<int>(c);
     *max_splits = static_cast<int>(ms);
-    *counter_bytes = ((static_cast<size_t>(nseq) * H * sizeof(int32_t) + 255) / 256) * 256;
     *partial_bytes = static_cast<size_t>(nseq) * Hq * ms * (D + 4) * sizeof(float);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     if (a.nseq == 0) return cudaSuccess;
-    const dim3 grid(a.max_splits, a.H, a.nseq);
-    if (a.bits == 2 && a.dtype == KIVI_F16) return launch_gq<2, KIVI_F16>(a, grid, stream);
-    if (a.bits == 2) return launch_gq<2, KIVI_BF16>(a, grid, stream);
-    if (a.dtype == KIVI_F16) return launch_gq<4, KIVI_F16>(a, grid, stream);
-    return launch_gq<4, KIVI_BF16>(a, grid, stream);
+    if (a.bits == 2 && a.dtype == KIVI_F16) return launch_gq<2, KIVI_F16>(a, stream);
+    if (a.bits == 2) return launch_gq<2, KIVI_BF16>(a, stream);
+    if (a.dtype == KIVI_F16) return launch_gq<4, KIVI_F16>(a, stream);
+    return launch_gq<4, KIVI_BF16>(a, stream);
 }
 
 }  // namespace kivi
