@@ -75,15 +75,42 @@ def test_decode_empty_sequence_gives_zeros():
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_split_count_invariance(dtype):
-    """The split size follows max_kv_len; different split counts agree to 1e-4. (The
-    tensor-core path carries ~22 bits on normal f16 hi+lo operands with an absolute
-    floor of 2^-25 on subnormal low parts; each split's running max changes which
-    terms sit at that floor.)"""
-    wl = synth.Workload("splits", 2, 8, 2, 128, (9000, 5000), dtype, seed=8)
+    """The same sequences give the same attention however the work is cut: alone, next
+    to each other, or behind other sequences that move the CTA boundaries (query group
+    4, persistent schedule); and with different split sizes (query group 8, split size
+    from max_kv_len). Agreement to 1e-4: the f16 hi+lo operands carry ~22 bits with an
+    absolute floor of 2^-25 on subnormal low parts, and each part's running max changes
+    which terms sit at that floor."""
+    lens = (9000, 5000)
+    base = synth.Workload("splits", 2, 8, 2, 128, lens, dtype, seed=8)
+    kcfg, ocfg = configs(2, dtype, 8, 2)
+    kv = [base.kv_seq(i, 0, lens[i]) for i in range(2)]
+    refs = []
+    for K, V in kv:
+        r = oracle.SeqCache(ocfg, 20000)
+        assert r.append(K, V) == oracle.OK
+        refs.append(r)
+    q0 = base.query(0)
+    outs = []
+    for pad in ((), (3000,), (700, 20000, 64)):
+        padw = synth.Workload("pad", max(len(pad), 1), 8, 2, 128, pad or (1,), dtype, seed=9)
+        kvp = [padw.kv_seq(i, 0, pad[i]) for i in range(len(pad))] + kv
+        cache = kivi.KVCache(kcfg, len(kvp), 20000)
+        cache.append([dev_tensor(K, dtype) for K, _ in kvp], [dev_tensor(V, dtype) for _, V in kvp])
+        q = np.concatenate([padw.query(0)[:len(pad)], q0]) if pad else q0
+        out = cache.decode(dev_tensor(q, dtype), softmax_scale=base.softmax_scale).cpu().numpy()[len(pad):]
+        assert int(cache.status.item()) == 0
+        for i, r in enumerate(refs):
+            err = float(np.max(np.abs(out[i] - r.decode(q0[i], base.softmax_scale))))
+            record_error(err)
+            assert err <= ATTN_TOL, err
+        outs.append(out)
+    assert np.max(np.abs(outs[0] - outs[1])) <= 1e-4 and np.max(np.abs(outs[0] - outs[2])) <= 1e-4
+    wl = synth.Workload("splits8", 2, 16, 2, 128, lens, dtype, seed=8)
     cache, refs = build(wl, 2, 9024)
-    a, _ = check_decode(wl, cache, refs, max_kv_len=9000)          # 2048-token splits (5 packed)
-    b, _ = check_decode(wl, cache, refs, max_kv_len=400000)        # 4096-token splits (3 packed)
-    c, _ = check_decode(wl, cache, refs, max_kv_len=24000)         # 3072-token splits (3 packed)
+    a, _ = check_decode(wl, cache, refs, max_kv_len=9000)          # 2048-token splits
+    b, _ = check_decode(wl, cache, refs, max_kv_len=400000)        # 4096-token splits
+    c, _ = check_decode(wl, cache, refs, max_kv_len=24000)         # 3072-token splits
     assert np.max(np.abs(a - b)) <= 1e-4 and np.max(np.abs(a - c)) <= 1e-4
 
 
@@ -133,3 +160,26 @@ def test_workload_llama2_7b_mha():
     for b in (0, 7):
         assert_state_equal(cache, b, refs[b])
     check_decode(wl, cache, refs)
+
+
+@pytest.mark.parametrize("g", [1, 4])
+@pytest.mark.parametrize("shape", ["short", "one_long"])
+def test_many_streams_persistent_schedule(g, shape):
+    """Hundreds of sequences (more than one per scan thread) of mixed lengths: empty ones,
+    residual-only ones, a few groups; in "one_long" also one 20000-token sequence, so
+    that one stream spans many CTAs while single CTAs hold many short streams."""
+    rng = np.random.default_rng(900 + g)
+    n = 300
+    lengths = rng.integers(0, 700, size=n)
+    lengths[rng.random(n) < 0.1] = 0
+    short = rng.random(n) < 0.2
+    lengths[short] = rng.integers(1, 160, size=int(short.sum()))          # residual-only
+    lengths[:6] = (0, 1, 159, 160, 161, 192)
+    if shape == "one_long":
+        lengths[137] = 20000
+    H = 2
+    wl = synth.Workload("streams", n, g * H, H, 128, tuple(int(x) for x in lengths), "f16", seed=31 + g)
+    cap = ((int(lengths.max()) + 31) // 32) * 32
+    cache, refs = build(wl, 2, cap)
+    out, _ = check_decode(wl, cache, refs)
+    assert np.all(out[lengths == 0] == 0)
