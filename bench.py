@@ -308,7 +308,7 @@ def run_gpu(args, rank, world, local_rank):
     res = {
         "total_ms": total_ms, "attn_ms": attn_ms, "kv_tokens": kv_tokens, "attn_bytes": bytes_per_step,
         "attn_units": units_per_step,
-        "clocks": clk.summary(), "e2e": e2e, "launches_per_step": 3, "cap": cap, "flush": flush,
+        "clocks": clk.summary(), "e2e": e2e, "launches_per_step": 4, "cap": cap, "flush": flush,
         "prefill": {"ms": prefill_ms, "algorithmic_bytes": prefill_bytes,
                     "GBps": prefill_bytes / (prefill_ms / 1e3) / 1e9 if prefill_ms > 0 else None},
     }
