@@ -149,16 +149,6 @@ __device__ __noinline__ uint32_t keys_exact4(const uint16_t* p, float z0, float 
            encode(half_at<DT>(v.y, 0), z2, s2, qmax) << (2 * BITS) | encode(half_at<DT>(v.y, 1), z3, s3, qmax) << (3 * BITS);
 }
 
-// Code words of one 32-channel value group at p with the IEEE division.
-template <int BITS, int DT>
-__device__ __noinline__ uint4 values_exact(const uint16_t* p, float z, float s) {
-    constexpr int qmax = (1 << BITS) - 1, CPW = 32 / BITS;
-    uint32_t out[4] = {0, 0, 0, 0};
-#pragma unroll 1
-    for (int c = 0; c < kGroup; ++c) out[c / CPW] |= encode(widen<DT>(p[c]), z, s, qmax) << ((c % CPW) * BITS);
-    return make_uint4(out[0], out[1], out[2], out[3]);
-}
-
 // One lane's share of a 32-row x DS-channel tile of 16-bit elements, in registers.
 // Keys: lane l owns channels 4 (l mod DS/4) .. +3 of the slice and the tokens j,
 // j + TS, ... (j = l / (DS/4), TS = 128 / DS): w[2 i], w[2 i + 1] hold token i TS + j.
@@ -303,84 +293,110 @@ __device__ __forceinline__ void values_load(const uint16_t* src, Tile<DS>& x) {
 }
 
 // Values of one token over one DS-channel slice (DS / 32 channel groups), by one lane,
-// from the row values_load() read from src; codes, scale and zero point at the slice's
-// first code byte and first group of the token's rows. Packed min/max over channel
-// pairs, then the pair's two halves; a zero minimum or maximum takes the sign of the
-// first zero in channel order.
+// from the row values_load() read from src (null: no token for this lane); codes, scale
+// and zero point at the slice's first code byte and first group of the token's rows.
+// Packed min/max over channel pairs, then the pair's two halves; a zero minimum or
+// maximum takes the sign of the first zero in channel order. Every lane of the warp
+// calls it: the exact redo at the end is done by the warp together.
 template <int BITS, int DT, int DS>
 __device__ __forceinline__ void values_compute(const Tile<DS>& x, const uint16_t* src, uint8_t* codes, uint16_t* scale,
                                                uint16_t* zero) {
-    if (src == nullptr) return;
     constexpr int NKG = DS / kGroup, qmax = (1 << BITS) - 1;
     constexpr int WPG = kGroup * BITS / 32;   // code words per channel group
-    uint32_t code_w[NKG][WPG];
-    uint32_t s16[NKG], z16[NKG];
+    constexpr int CPW = 32 / BITS;            // codes per word
     float zq[NKG], sq[NKG];   // fp32 zero and scale per group, for the exact redo
     uint32_t tie_groups = 0;  // groups to redo with the exact division
+    if (src != nullptr) {
+        uint32_t code_w[NKG][WPG];
+        uint32_t s16[NKG], z16[NKG];
 #pragma unroll
-    for (int k = 0; k < NKG; ++k) {
-        const uint32_t* w = x.w + 16 * k;
-        uint32_t mn2 = w[0], mx2 = w[0];
+        for (int k = 0; k < NKG; ++k) {
+            const uint32_t* w = x.w + 16 * k;
+            uint32_t mn2 = w[0], mx2 = w[0];
 #pragma unroll
-        for (int c = 1; c < 16; ++c) {
-            mn2 = hmin2<DT>(mn2, w[c]);
-            mx2 = hmax2<DT>(mx2, w[c]);
-        }
-        uint32_t mn = pick_min<DT>(lo16(mn2), hi16(mn2));
-        uint32_t mx = pick_max<DT>(lo16(mx2), hi16(mx2));
-        if (is_zero16(mn) || is_zero16(mx)) {   // sign of the first zero in channel order
-            uint32_t zs = 0;
-#pragma unroll 1
-            for (int c = kGroup - 1; c >= 0; --c) {
-                const uint32_t hv = src[k * kGroup + c];
-                zs = is_zero16(hv) ? hv & 0x8000u : zs;
+            for (int c = 1; c < 16; ++c) {
+                mn2 = hmin2<DT>(mn2, w[c]);
+                mx2 = hmax2<DT>(mx2, w[c]);
             }
-            if (is_zero16(mn)) mn = zs;
-            if (is_zero16(mx)) mx = zs;
+            uint32_t mn = pick_min<DT>(lo16(mn2), hi16(mn2));
+            uint32_t mx = pick_max<DT>(lo16(mx2), hi16(mx2));
+            if (is_zero16(mn) || is_zero16(mx)) {   // sign of the first zero in channel order
+                uint32_t zs = 0;
+#pragma unroll 1
+                for (int c = kGroup - 1; c >= 0; --c) {
+                    const uint32_t hv = src[k * kGroup + c];
+                    zs = is_zero16(hv) ? hv & 0x8000u : zs;
+                }
+                if (is_zero16(mn)) mn = zs;
+                if (is_zero16(mx)) mx = zs;
+            }
+            const float fmn = widen<DT>(static_cast<uint16_t>(mn)), fmx = widen<DT>(static_cast<uint16_t>(mx));
+            const GroupParams gp = group_params(fmn, fmx, qmax);
+            s16[k] = gp.s16;
+            z16[k] = gp.z16;
+            const Quantizer q = make_quantizer(gp);
+            zq[k] = q.z;
+            sq[k] = q.s;
+            bool tie = !codes_in_range<BITS>(fmn, fmx, q);
+#pragma unroll
+            for (int ww = 0; ww < WPG; ++ww) {
+                uint32_t acc = magic_offset(CPW, BITS);
+#pragma unroll
+                for (int e = 0; e < CPW; ++e) {
+                    const int c = ww * CPW + e;
+                    acc += code_bits<BITS>(half_at<DT>(w[c >> 1], c & 1), q, tie) << (e * BITS);
+                }
+                code_w[k][ww] = acc;
+            }
+            tie_groups |= static_cast<uint32_t>(tie) << k;
         }
-        const float fmn = widen<DT>(static_cast<uint16_t>(mn)), fmx = widen<DT>(static_cast<uint16_t>(mx));
-        const GroupParams gp = group_params(fmn, fmx, qmax);
-        s16[k] = gp.s16;
-        z16[k] = gp.z16;
-        const Quantizer q = make_quantizer(gp);
-        zq[k] = q.z;
-        sq[k] = q.s;
-        bool tie = !codes_in_range<BITS>(fmn, fmx, q);
+        // code row: NKG * WPG words (8 bytes per 32 channels at 2 bits, 16 at 4 bits)
+        uint32_t* cw = reinterpret_cast<uint32_t*>(codes);
+        if constexpr (NKG * WPG % 4 == 0) {
+#pragma unroll
+            for (int i = 0; i < NKG * WPG / 4; ++i)
+                reinterpret_cast<uint4*>(cw)[i] = make_uint4(code_w[(4 * i) / WPG][(4 * i) % WPG], code_w[(4 * i + 1) / WPG][(4 * i + 1) % WPG],
+                                                             code_w[(4 * i + 2) / WPG][(4 * i + 2) % WPG], code_w[(4 * i + 3) / WPG][(4 * i + 3) % WPG]);
+        } else {
+            reinterpret_cast<uint2*>(cw)[0] = make_uint2(code_w[0][0], code_w[0][1]);   // NKG * WPG == 2
+        }
+#pragma unroll
+        for (int k = 0; k < NKG; ++k) {
+            scale[k] = static_cast<uint16_t>(s16[k]);
+            zero[k] = static_cast<uint16_t>(z16[k]);
+        }
+    }
+    // Exact redo, by the whole warp: one flagged (token, group) at a time, each lane
+    // encoding one of its 32 elements with the IEEE division, the words packed by an OR
+    // reduction. (A lane redoing its own group alone would run 32 divisions while the
+    // others wait.) Every lane of the warp runs this loop.
+    const int lane = threadIdx.x & 31;
+    uint32_t pending = tie_groups;
+    while (true) {
+        const uint32_t ball = __ballot_sync(0xffffffffu, pending != 0);
+        if (ball == 0) break;
+        const int leader = __ffs(ball) - 1;
+        const int k = __ffs(__shfl_sync(0xffffffffu, pending, leader)) - 1;
+        float zk = zq[0], sk = sq[0];
+#pragma unroll
+        for (int i = 1; i < NKG; ++i) {
+            zk = k == i ? zq[i] : zk;
+            sk = k == i ? sq[i] : sk;
+        }
+        zk = __shfl_sync(0xffffffffu, zk, leader);
+        sk = __shfl_sync(0xffffffffu, sk, leader);
+        const uint16_t* gsrc = reinterpret_cast<const uint16_t*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src), leader)) + k * kGroup;
+        uint32_t* gdst = reinterpret_cast<uint32_t*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(codes), leader)) + k * WPG;
+        const uint32_t code = encode(widen<DT>(gsrc[lane]), zk, sk, qmax);
 #pragma unroll
         for (int ww = 0; ww < WPG; ++ww) {
-            constexpr int CPW = 32 / BITS;   // codes per word
-            uint32_t acc = magic_offset(CPW, BITS);
-#pragma unroll
-            for (int e = 0; e < CPW; ++e) {
-                const int c = ww * CPW + e;
-                acc += code_bits<BITS>(half_at<DT>(w[c >> 1], c & 1), q, tie) << (e * BITS);
-            }
-            code_w[k][ww] = acc;
+            const uint32_t part = lane / CPW == ww ? code << ((lane % CPW) * BITS) : 0u;
+            const uint32_t word = __reduce_or_sync(0xffffffffu, part);
+            if (lane == ww) gdst[ww] = word;
         }
-        tie_groups |= static_cast<uint32_t>(tie) << k;
-    }
-    // code row: NKG * WPG words (8 bytes per 32 channels at 2 bits, 16 at 4 bits)
-    uint32_t* cw = reinterpret_cast<uint32_t*>(codes);
-    if constexpr (NKG * WPG % 4 == 0) {
-#pragma unroll
-        for (int i = 0; i < NKG * WPG / 4; ++i)
-            reinterpret_cast<uint4*>(cw)[i] = make_uint4(code_w[(4 * i) / WPG][(4 * i) % WPG], code_w[(4 * i + 1) / WPG][(4 * i + 1) % WPG],
-                                                         code_w[(4 * i + 2) / WPG][(4 * i + 2) % WPG], code_w[(4 * i + 3) / WPG][(4 * i + 3) % WPG]);
-    } else {
-        reinterpret_cast<uint2*>(cw)[0] = make_uint2(code_w[0][0], code_w[0][1]);   // NKG * WPG == 2
-    }
-#pragma unroll
-    for (int k = 0; k < NKG; ++k) {
-        scale[k] = static_cast<uint16_t>(s16[k]);
-        zero[k] = static_cast<uint16_t>(z16[k]);
-    }
-#pragma unroll
-    for (int k = 0; k < NKG; ++k) {
-        if (tie_groups & (1u << k)) {
-            const uint4 ex = values_exact<BITS, DT>(src + k * kGroup, zq[k], sq[k]);
-            if constexpr (WPG == 4) reinterpret_cast<uint4*>(cw)[k] = ex;
-            else reinterpret_cast<uint2*>(cw)[k] = make_uint2(ex.x, ex.y);
-        }
+        if (lane == leader) pending &= pending - 1;
     }
 }
 
