@@ -216,7 +216,7 @@ def run_gpu(args, rank, world, local_rank):
     cap = ((L0 + n_steps + args.steps + 31) // 32) * 32   # decode steps of both timed legs
     cfg = kivi.Config(bits=bits, head_dim=D, num_q_heads=Hq, num_kv_heads=H,
                       dtype=kivi.BF16 if wl.dtype == "bf16" else kivi.F16)
-    cache = kivi.KVCache(cfg, B, cap, device)
+    cache = kivi.KVCache(cfg, B, cap, device, paged=args.paged, page_seed=1)
 
     # prefill (outside the timed steps): every sequence's K and V drawn on the GPU, then one
     # append call for the whole batch, timed on its own for the prefill line of the report.
@@ -398,6 +398,8 @@ def main():
     ap.add_argument("--workload", type=int, default=2, choices=[0, 1, 2, 3, 4],
                     help="0 tiny, 1 Llama-2-7B MHA, 2 Llama-3-8B GQA (default), 3 streaming, 4 long varlen")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--paged", action="store_true",
+                    help="packed cache in shared 32-token pages behind block tables (random page order)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", 0))
@@ -418,6 +420,7 @@ def main():
                if attn_bytes(wl, list(wl.lengths), wl.bits) < 256 << 20 else
                "no flush: the packed cache is larger than L2 (129 MB)"),
         "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        "layout": "paged: 32-token pages of one shared pool in random order" if args.paged else "contiguous",
     }
     if args.impl == "reference":
         if rank != 0:
@@ -454,7 +457,7 @@ def main():
     # the decode kernel the library picks: tensor-core path for query groups of 1, 2 or 4
     group = config["q_heads"] // config["kv_heads"]
     kernel = "decode_mma_kernel" if group in (1, 2, 4) else "decode_split_kernel"
-    per_unit = NCU_TRAFFIC_BYTES_PER_UNIT.get((kernel, config["bits"], group, config["input_dtype"]))
+    per_unit = None if args.paged else NCU_TRAFFIC_BYTES_PER_UNIT.get((kernel, config["bits"], group, config["input_dtype"]))
     traffic = per_unit * sum(res["attn_units"]) / len(res["attn_units"]) if per_unit else None
     line = {
         "metric": METRIC, "value": value, "unit": "KV-tokens/s", "n_gpus": world, "steps": args.steps,

@@ -44,7 +44,8 @@ class _Cfg(ctypes.Structure):
 
 
 SEQ_FIELDS = ("k_codes", "k_scale", "k_zero", "v_codes", "v_scale", "v_zero", "k_res", "v_res")
-SEQ_STRUCT_BYTES = 8 * 8 + 2 * 4   # eight pointers, cap_tokens, reserved
+SEQ_STRUCT_BYTES = 8 * 8 + 2 * 4 + 8   # eight pointers, cap_tokens, flags, block_table
+SEQ_PAGED = 1
 
 _lock = threading.Lock()
 _lib = None
@@ -184,20 +185,33 @@ class KVCache:
     sequences live in one allocation per kind; the device array of kivi_seq
     records points into them."""
 
-    def __init__(self, cfg: Config, nseq: int, cap_tokens: int, device="cuda"):
+    def __init__(self, cfg: Config, nseq: int, cap_tokens: int, device="cuda", paged: bool = False,
+                 page_seed: int = 0, spare_pages: int = 0):
+        """paged: the packed buffers are one pool of 32-token pages shared by all sequences,
+        each sequence's groups mapped through a block table (kivi.h, paged layout); the pool
+        has nseq * cap_tokens / 32 + spare_pages pages, handed out in a seeded random order."""
         if cap_tokens % GROUP:
             raise ValueError("cap_tokens must be a multiple of 32")
         if not torch.cuda.is_available():
             raise RuntimeError("KIVI kernels need a CUDA device; there is no CPU path")
-        self.cfg, self.nseq, self.cap = cfg, nseq, cap_tokens
+        self.cfg, self.nseq, self.cap, self.paged = cfg, nseq, cap_tokens, paged
         self.device = torch.device(device)
         H, D, G = cfg.num_kv_heads, cfg.head_dim, GROUP
         dev = self.device
-        self.k_codes = torch.zeros((nseq, H, cap_tokens, cfg.row_bytes), dtype=torch.uint8, device=dev)
+        if paged:
+            npg = nseq * (cap_tokens // G) + spare_pages
+            self.k_codes = torch.zeros((npg, H, G, cfg.row_bytes), dtype=torch.uint8, device=dev)
+            self.k_scale = torch.zeros((npg, H, D), dtype=torch.int16, device=dev)
+            self.v_scale = torch.zeros((npg, H, G, D // G), dtype=torch.int16, device=dev)
+            perm = np.random.default_rng(page_seed).permutation(npg)[:nseq * (cap_tokens // G)]
+            self.block_tables = torch.from_numpy(perm.reshape(nseq, cap_tokens // G).astype(np.int32)).to(dev)
+        else:
+            self.k_codes = torch.zeros((nseq, H, cap_tokens, cfg.row_bytes), dtype=torch.uint8, device=dev)
+            self.k_scale = torch.zeros((nseq, H, cap_tokens // G, D), dtype=torch.int16, device=dev)
+            self.v_scale = torch.zeros((nseq, H, cap_tokens, D // G), dtype=torch.int16, device=dev)
+            self.block_tables = None
         self.v_codes = torch.zeros_like(self.k_codes)
-        self.k_scale = torch.zeros((nseq, H, cap_tokens // G, D), dtype=torch.int16, device=dev)
         self.k_zero = torch.zeros_like(self.k_scale)
-        self.v_scale = torch.zeros((nseq, H, cap_tokens, D // G), dtype=torch.int16, device=dev)
         self.v_zero = torch.zeros_like(self.v_scale)
         self.k_res = torch.zeros((nseq, H, cfg.ring, D), dtype=cfg.torch_dtype, device=dev)
         self.v_res = torch.zeros_like(self.k_res)
@@ -208,8 +222,11 @@ class KVCache:
         rec = np.zeros((nseq, SEQ_STRUCT_BYTES // 8), dtype=np.uint64)
         for b in range(nseq):
             for i, name in enumerate(SEQ_FIELDS):
-                rec[b, i] = getattr(self, name)[b].data_ptr()
-            rec[b, 8] = np.uint64(cap_tokens)   # cap_tokens (low half), reserved = 0 (high half)
+                t = getattr(self, name)
+                rec[b, i] = t.data_ptr() if (paged and name not in ("k_res", "v_res")) else t[b].data_ptr()
+            # cap_tokens (low half), flags (high half); then the block table pointer
+            rec[b, 8] = np.uint64(cap_tokens) | (np.uint64(SEQ_PAGED if paged else 0) << np.uint64(32))
+            rec[b, 9] = np.uint64(self.block_tables[b].data_ptr()) if paged else np.uint64(0)
         self.seqs = torch.from_numpy(rec.view(np.uint8).reshape(-1)).to(dev)
 
     @property
@@ -270,10 +287,19 @@ class KVCache:
 
     # -------------------------------------------------------------- inspection
     def seq_numpy(self, b: int) -> dict:
-        """Host copies of sequence b's buffers (uint8 / uint16 views), kv_len and status."""
+        """Host copies of sequence b's buffers in the contiguous layout (a paged sequence's
+        pages gathered through its block table; uint8 / uint16 views), and kv_len."""
         d = {}
         for name in SEQ_FIELDS:
-            t = getattr(self, name)[b].contiguous().cpu()
+            t = getattr(self, name)
+            if self.paged and name not in ("k_res", "v_res"):
+                t = t[self.block_tables[b].long()]          # [groups][H][...] in group order
+                t = t.transpose(0, 1)                         # [H][groups][...]
+                if name in ("k_codes", "v_codes", "v_scale", "v_zero"):
+                    t = t.reshape(t.shape[0], -1, t.shape[-1])   # [H][cap][...]
+            else:
+                t = t[b]
+            t = t.contiguous().cpu()
             if t.dtype in (torch.int16, torch.float16, torch.bfloat16):
                 d[name] = t.view(torch.int16).numpy().view(np.uint16)
             else:

@@ -511,19 +511,16 @@ __global__ void __launch_bounds__(kThreads, CtasPerSm<DS>::kValue) append_pack_k
     };
     auto compute = [&](int64_t unit, bool is_v, const Tile<DS>& tile) {
         const int sl = slice_of(unit);
-        const int64_t p0 = group_pos(unit);
-        const int64_t tok = static_cast<int64_t>(h) * cap + p0;
+        const int64_t p0 = group_pos(unit), j = p0 / kGroup;
+        const GroupAddr ga = group_addr(sq, a.H, h, j, group_page(sq, j), D, BITS);
         if (!is_v) {
-            const int64_t kg = static_cast<int64_t>(h) * (cap / kGroup) + p0 / kGroup;
             keys_compute<BITS, DT, DS>(tile, [&](int t) { return row_at(sq.k_res, a.k_new[b], p0, sl, t); },
-                                       sq.k_codes + tok * row_bytes + sl * (DS * BITS / 8), row_bytes,
-                                       sq.k_scale + kg * D + sl * DS, sq.k_zero + kg * D + sl * DS);
+                                       ga.kc + sl * (DS * BITS / 8), row_bytes, ga.ks + sl * DS, ga.kz + sl * DS);
         } else {
-            const int64_t tt = tok + lane;
             values_compute<BITS, DT, DS>(tile, row_at(sq.v_res, a.v_new[b], p0, sl, lane),
-                                         sq.v_codes + tt * row_bytes + sl * (DS * BITS / 8),
-                                         sq.v_scale + tt * (D / kGroup) + sl * (DS / kGroup),
-                                         sq.v_zero + tt * (D / kGroup) + sl * (DS / kGroup));
+                                         ga.vc + lane * row_bytes + sl * (DS * BITS / 8),
+                                         ga.vs + lane * (D / kGroup) + sl * (DS / kGroup),
+                                         ga.vz + lane * (D / kGroup) + sl * (DS / kGroup));
         }
     };
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarps;

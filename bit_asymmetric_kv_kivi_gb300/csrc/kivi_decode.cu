@@ -478,10 +478,10 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
             __syncwarp();
             continue;
         }
-        const int64_t p = ts + lane;   // packed tiles are always full
-        const int64_t j = ts / kGroup;
-        const uint16_t* ksc = sq.k_scale + (static_cast<int64_t>(h) * (cap / kGroup) + j) * kD;
-        const uint16_t* kzr = sq.k_zero + (static_cast<int64_t>(h) * (cap / kGroup) + j) * kD;
+        const int64_t j = ts / kGroup;   // packed tiles are whole groups
+        const GroupAddr ga = group_addr(sq, a.H, h, j, group_page(sq, j), kD, BITS);
+        const uint16_t* ksc = ga.ks;
+        const uint16_t* kzr = ga.kz;
         float sc[GQ], bias[GQ];
 #pragma unroll
         for (int hh = 0; hh < GQ; ++hh) bias[hh] = 0.0f;
@@ -497,18 +497,17 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
         }
 #pragma unroll
         for (int hh = 0; hh < GQ; ++hh) sc[hh] = warp_sum(bias[hh]);
-        const int64_t tok = static_cast<int64_t>(h) * cap + p;
-        const uint4* vrow = reinterpret_cast<const uint4*>(sq.v_codes + tok * (kD * BITS / 8));
+        const uint4* vrow = reinterpret_cast<const uint4*>(ga.vc + lane * (kD * BITS / 8));
 #pragma unroll
         for (int w = 0; w < kRowWords / 4; ++w)
             *reinterpret_cast<uint4*>(&vcode[warp][lane][4 * w]) = __ldg(vrow + w);
 #pragma unroll
         for (int k = 0; k < kNg; ++k) {
-            vsc[warp][lane][k] = f16_bits_to_float(sq.v_scale[tok * kNg + k]);
-            vzr[warp][lane][k] = f16_bits_to_float(sq.v_zero[tok * kNg + k]);
+            vsc[warp][lane][k] = f16_bits_to_float(ga.vs[lane * kNg + k]);
+            vzr[warp][lane][k] = f16_bits_to_float(ga.vz[lane * kNg + k]);
         }
         __syncwarp();
-        const uint4* krow = reinterpret_cast<const uint4*>(sq.k_codes + tok * (kD * BITS / 8));
+        const uint4* krow = reinterpret_cast<const uint4*>(ga.kc + lane * (kD * BITS / 8));
 #pragma unroll
         for (int w4 = 0; w4 < kRowWords / 4; ++w4) {
             const uint4 v4 = __ldg(krow + w4);
@@ -702,12 +701,17 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
     unsigned char* my_st = stages + warp * kStages * STAGE;
     float* pt = pt_all + warp * 4 * kPtLd;
 
-    const unsigned char* kc_base = sq.k_codes + static_cast<int64_t>(h) * cap * RB;
-    const unsigned char* vc_base = sq.v_codes + static_cast<int64_t>(h) * cap * RB;
-    const unsigned char* ks_base = reinterpret_cast<const unsigned char*>(sq.k_scale + static_cast<int64_t>(h) * (cap / kGroup) * kD);
-    const unsigned char* kz_base = reinterpret_cast<const unsigned char*>(sq.k_zero + static_cast<int64_t>(h) * (cap / kGroup) * kD);
-    const unsigned char* vs_base = reinterpret_cast<const unsigned char*>(sq.v_scale + static_cast<int64_t>(h) * cap * (kD / kGroup));
-    const unsigned char* vz_base = reinterpret_cast<const unsigned char*>(sq.v_zero + static_cast<int64_t>(h) * cap * (kD / kGroup));
+    // Group j's data sits at index idx of (G code rows, 256 bytes of each kind of
+    // metadata) from these bases: idx = j in a contiguous sequence (bases at head h), and
+    // idx = page * H + h in a paged one (bases at the pools; see group_addr).
+    const bool paged = seq_paged(sq);
+    const int64_t hc = paged ? 0 : static_cast<int64_t>(h) * cap;   // head offset in tokens
+    const unsigned char* kc_base = sq.k_codes + hc * RB;
+    const unsigned char* vc_base = sq.v_codes + hc * RB;
+    const unsigned char* ks_base = reinterpret_cast<const unsigned char*>(sq.k_scale + hc / kGroup * kD);
+    const unsigned char* kz_base = reinterpret_cast<const unsigned char*>(sq.k_zero + hc / kGroup * kD);
+    const unsigned char* vs_base = reinterpret_cast<const unsigned char*>(sq.v_scale + hc * (kD / kGroup));
+    const unsigned char* vz_base = reinterpret_cast<const unsigned char*>(sq.v_zero + hc * (kD / kGroup));
 
     // Per-lane cp.async plan of one group: code rows as 16-byte chunks (lane + 32k), then one
     // chunk of key scale / zero (lanes 0-15 / 16-31) and one of value scale / zero.
@@ -719,9 +723,10 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
     const unsigned char* vm_lane = (half ? vz_base : vs_base) + off16;
     const int km_dst = 2 * kGroup * RB + half * Lay::kMetaPad + (off16 >> 6) * 80 + (off16 & 63);
     const int vm_dst = 2 * kGroup * RB + 2 * Lay::kMetaPad + half * 256 + off16;
-    auto issue = [&](int slot, int64_t j) {
+    auto issue = [&](int slot, int64_t j, int32_t page) {
         unsigned char* dst = my_st + slot * STAGE;
-        const int64_t code_off = j * kGroup * RB, meta_off = j * 256;
+        const int64_t idx = paged ? static_cast<int64_t>(page) * a.H + h : j;
+        const int64_t code_off = idx * kGroup * RB, meta_off = idx * 256;
 #pragma unroll
         for (int k = 0; k < kCodeChunks; ++k) {
             cp_async16(dst + lane * 16 + 512 * k, kc_lane + code_off + 512 * k);
@@ -731,16 +736,23 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
         cp_async16(dst + vm_dst, vm_lane + meta_off);
     };
 
+    // page of this warp's i-th group (paged sequences); the in-loop issue uses an entry
+    // loaded one iteration earlier, so the table read stays off the critical path
+    auto page_of = [&](int i) -> int32_t { return paged ? sq.block_table[gfirst + static_cast<int64_t>(kWarps) * i] : 0; };
 #pragma unroll
     for (int i = 0; i < kStages - 1; ++i) {
-        if (i < n_my) issue(i, gfirst + static_cast<int64_t>(kWarps) * i);
+        if (i < n_my) issue(i, gfirst + static_cast<int64_t>(kWarps) * i, page_of(i));
         cp_async_commit();
     }
+    int32_t pg_ahead = kStages - 1 < n_my ? page_of(kStages - 1) : 0;
 
     for (int it = 0; it < n_my; ++it) {
         {
             const int nxt = it + kStages - 1;
-            if (nxt < n_my) issue(nxt % kStages, gfirst + static_cast<int64_t>(kWarps) * nxt);
+            if (nxt < n_my) {
+                issue(nxt % kStages, gfirst + static_cast<int64_t>(kWarps) * nxt, pg_ahead);
+                pg_ahead = nxt + 1 < n_my ? page_of(nxt + 1) : 0;
+            }
             cp_async_commit();
         }
         cp_async_wait<kStages - 1>();

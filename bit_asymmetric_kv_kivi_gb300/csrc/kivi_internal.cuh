@@ -68,6 +68,47 @@ __host__ __device__ __forceinline__ int64_t n_packed(int64_t L, int R) {
     return over <= 0 ? 0 : (over / kGroup) * kGroup;
 }
 
+// Addresses of packed group j of kv head h of a sequence, in either layout of kivi.h:
+// its G key code rows, D key scales and zeros, G value code rows and G x (D / G) value
+// scales and zeros. page is block_table[j] for a paged sequence (ignored otherwise).
+struct GroupAddr {
+    uint8_t* kc;
+    uint16_t* ks;
+    uint16_t* kz;
+    uint8_t* vc;
+    uint16_t* vs;
+    uint16_t* vz;
+};
+
+__device__ __forceinline__ bool seq_paged(const kivi_seq& sq) { return (sq.flags & KIVI_SEQ_PAGED) != 0; }
+
+__device__ __forceinline__ GroupAddr group_addr(const kivi_seq& sq, int H, int h, int64_t j, int32_t page, int D,
+                                                int bits) {
+    const int64_t rb = static_cast<int64_t>(D) * bits / 8, ng = D / kGroup;
+    int64_t row0, meta;   // first code row of the group, and its (head, group) metadata row
+    if (seq_paged(sq)) {
+        const int64_t pg = static_cast<int64_t>(page) * H + h;
+        row0 = pg * kGroup;
+        meta = pg;
+    } else {
+        const int64_t cap = sq.cap_tokens;
+        row0 = h * cap + j * kGroup;
+        meta = h * (cap / kGroup) + j;
+    }
+    GroupAddr a;
+    a.kc = sq.k_codes + row0 * rb;
+    a.ks = sq.k_scale + meta * D;
+    a.kz = sq.k_zero + meta * D;
+    a.vc = sq.v_codes + row0 * rb;
+    a.vs = sq.v_scale + row0 * ng;
+    a.vz = sq.v_zero + row0 * ng;
+    return a;
+}
+
+__device__ __forceinline__ int32_t group_page(const kivi_seq& sq, int64_t j) {
+    return seq_paged(sq) ? sq.block_table[j] : 0;
+}
+
 __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
     if (status != nullptr) atomicCAS(status, 0, code);
 }

@@ -65,7 +65,7 @@
 extern "C" {
 #endif
 
-#define KIVI_ABI_VERSION 1
+#define KIVI_ABI_VERSION 2
 
 typedef enum kivi_status {
     KIVI_OK = 0,
@@ -97,16 +97,35 @@ typedef struct kivi_cfg {
  * Buffers of one sequence (an array of these lives in device memory).
  * cap = cap_tokens, a multiple of G: packed capacity in tokens. A sequence
  * can hold up to cap + R + G - 1 tokens.
+ *
+ * Contiguous layout (flags = 0): the packed buffers belong to this sequence.
  *   k_codes [Hkv][cap][D*bits/8]  u8     packed key rows
  *   k_scale [Hkv][cap/G][D]       fp16   per (key group, channel)
  *   k_zero  [Hkv][cap/G][D]       fp16
  *   v_codes [Hkv][cap][D*bits/8]  u8     packed value rows
  *   v_scale [Hkv][cap][D/G]       fp16   per (token, channel group)
  *   v_zero  [Hkv][cap][D/G]       fp16
+ *
+ * Paged layout (flags = KIVI_SEQ_PAGED): the six packed buffers are pools of
+ * pages that any number of sequences may share. A page holds one packed group
+ * of G tokens for every kv head, laid out like a contiguous sequence with
+ * cap = G:
+ *   k_codes [pages][Hkv][G][D*bits/8], k_scale, k_zero [pages][Hkv][D],
+ *   v_codes [pages][Hkv][G][D*bits/8], v_scale, v_zero [pages][Hkv][G][D/G]
+ * block_table [cap/G] int32 (device memory) gives the page of each packed
+ * group of the sequence, in order; the caller keeps the pages of different
+ * sequences apart. Packed groups are written once (when they leave the
+ * residual window) and only read afterwards, so a table may be extended
+ * between calls.
+ *
+ * Both layouts:
  *   k_res   [Hkv][R+G][D]         dtype  residual ring (slot p mod (R+G))
  *   v_res   [Hkv][R+G][D]         dtype
  * Ring slots that hold no live residual position have unspecified contents.
+ * This paging is not on the pages that describe KIVI; it maps the packed cache
+ * onto the fixed-size blocks of a paged serving cache.
  */
+#define KIVI_SEQ_PAGED 1
 typedef struct kivi_seq {
     uint8_t* k_codes;
     uint16_t* k_scale;
@@ -117,7 +136,8 @@ typedef struct kivi_seq {
     void* k_res;
     void* v_res;
     int32_t cap_tokens;
-    int32_t reserved;      /* must be 0 */
+    int32_t flags;                 /* 0 or KIVI_SEQ_PAGED */
+    const int32_t* block_table;    /* KIVI_SEQ_PAGED only; else unused */
 } kivi_seq;
 
 /* ---------------------------------------------------------------- codec */

@@ -30,7 +30,7 @@ def test_exports_every_declared_symbol(lib):
     assert "kivi_decode_attn" in names and len(names) >= 10
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.kivi_abi_version() == 1
+    assert lib.kivi_abi_version() == 2
 
 
 def test_status_strings(lib):
@@ -95,3 +95,21 @@ def test_bad_arguments_rejected_before_launch(lib):
     assert lib.kivi_quant_keys(cfg, 0, 32, null, null, null, null, None) == kivi.OK
     assert lib.kivi_append_flush(cfg, 0, null, null, null, null, null, 0, null, None) == kivi.OK
     assert lib.kivi_decode_attn(cfg, 0, null, null, null, null, 0.1, 0, null, 0, null, None) == kivi.OK
+
+
+def test_seq_record_layout_matches_header(tmp_path):
+    """The binding writes kivi_seq records by hand; their size and field offsets must be
+    those of the C struct (compiled here from include/kivi.h)."""
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "kivi.h"\n'
+                   'int main(void) { printf("%zu %zu %zu %zu %d\\n", sizeof(kivi_seq), '
+                   'offsetof(kivi_seq, cap_tokens), offsetof(kivi_seq, flags), '
+                   'offsetof(kivi_seq, block_table), KIVI_SEQ_PAGED); return 0; }\n')
+    exe = tmp_path / "layout"
+    import subprocess
+    subprocess.run(["gcc", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
+    size, cap_off, flags_off, table_off, paged = map(int, subprocess.run([str(exe)], capture_output=True, text=True,
+                                                                         check=True).stdout.split())
+    assert size == kivi.SEQ_STRUCT_BYTES
+    assert cap_off == 8 * len(kivi.SEQ_FIELDS) and flags_off == cap_off + 4 and table_off == cap_off + 8
+    assert paged == kivi.SEQ_PAGED
