@@ -1,0 +1,21 @@
+"""The attention-error study run through the library's GPU codec equals the same study
+through the oracle's quantizers (the codes are bit-exact, so the dequantized caches are
+identical; only fp64 summation order differs)."""
+import pytest
+
+from bit_asymmetric_kv_kivi_gb300 import study
+from test_oracle_study import study as oracle_study
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("workload", [1, 2])
+def test_gpu_study_equals_oracle_study(workload):
+    res = study.run(workload=workload, seqs=1, tokens=512)
+    ref = oracle_study(workload, seqs=1, T=512)
+    assert res["tokens"] == 512
+    for r in res["rows"]:
+        want = ref[(r["scheme"], r["bits"])]
+        got = (r["score_rel_l2"], r["prob_tv"], r["out_rel_l2"])
+        for a, b in zip(got, want):
+            assert abs(a - b) <= 1e-9 + 1e-6 * abs(b), (r, want)
