@@ -58,7 +58,8 @@ def build(force: bool = False) -> str:
 
 
 class _Cfg(ctypes.Structure):
-    _fields_ = [("bits", ctypes.c_int32), ("group", ctypes.c_int32), ("residual", ctypes.c_int32),
+    _fields_ = [("k_bits", ctypes.c_int32), ("v_bits", ctypes.c_int32), ("group", ctypes.c_int32),
+                ("residual", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("dtype", ctypes.c_int32)]
 
@@ -105,7 +106,8 @@ def lib():
 
 @dataclass(frozen=True)
 class Cfg:
-    """KIVI configuration: bits, G, R, head_dim, query and kv heads, storage dtype."""
+    """KIVI configuration: code widths, G, R, head_dim, query and kv heads, storage dtype.
+    `bits` sets both code widths; k_bits / v_bits, when given, set one of them."""
     bits: int = 2
     group: int = 32
     residual: int = 128
@@ -113,14 +115,26 @@ class Cfg:
     num_q_heads: int = 1
     num_kv_heads: int = 1
     dtype: int = F16
+    k_bits: int | None = None
+    v_bits: int | None = None
+
+    def __post_init__(self):
+        if self.k_bits is None:
+            object.__setattr__(self, "k_bits", self.bits)
+        if self.v_bits is None:
+            object.__setattr__(self, "v_bits", self.bits)
 
     def c(self) -> _Cfg:
-        return _Cfg(self.bits, self.group, self.residual, self.head_dim, self.num_q_heads,
+        return _Cfg(self.k_bits, self.v_bits, self.group, self.residual, self.head_dim, self.num_q_heads,
                     self.num_kv_heads, self.dtype)
 
     @property
-    def row_bytes(self) -> int:
-        return self.head_dim * self.bits // 8
+    def k_row_bytes(self) -> int:
+        return self.head_dim * self.k_bits // 8
+
+    @property
+    def v_row_bytes(self) -> int:
+        return self.head_dim * self.v_bits // 8
 
     @property
     def ring(self) -> int:
@@ -160,7 +174,7 @@ def quant_keys(cfg: Cfg, x_bits: np.ndarray):
     x = _u16(x_bits)
     S, T, D = x.shape
     assert D == cfg.head_dim and T % cfg.group == 0
-    codes = np.zeros((S, T, cfg.row_bytes), np.uint8)
+    codes = np.zeros((S, T, cfg.k_row_bytes), np.uint8)
     scale = np.zeros((S, T // cfg.group, D), np.uint16)
     zero = np.zeros_like(scale)
     rc = lib().orc_quant_keys(cfg.c(), S, T, _p(x), _p(codes), _p(scale), _p(zero))
@@ -173,7 +187,7 @@ def quant_values(cfg: Cfg, x_bits: np.ndarray):
     x = _u16(x_bits)
     S, T, D = x.shape
     assert D == cfg.head_dim
-    codes = np.zeros((S, T, cfg.row_bytes), np.uint8)
+    codes = np.zeros((S, T, cfg.v_row_bytes), np.uint8)
     scale = np.zeros((S, T, D // cfg.group), np.uint16)
     zero = np.zeros_like(scale)
     rc = lib().orc_quant_values(cfg.c(), S, T, _p(x), _p(codes), _p(scale), _p(zero))
@@ -182,15 +196,18 @@ def quant_values(cfg: Cfg, x_bits: np.ndarray):
 
 
 def unpack_codes(cfg: Cfg, rows: np.ndarray) -> np.ndarray:
-    """[..., D*b/8] packed rows -> [..., D] integer codes, using the oracle's packing rule."""
+    """[..., D*b/8] packed rows -> [..., D] integer codes, using the oracle's packing rule
+    (b, 2 or 4, from the row length)."""
     rows = np.ascontiguousarray(rows, dtype=np.uint8)
-    flat = rows.reshape(-1, cfg.row_bytes)
+    bits = rows.shape[-1] * 8 // cfg.head_dim
+    assert bits in (2, 4) and rows.shape[-1] == cfg.head_dim * bits // 8
+    flat = rows.reshape(-1, rows.shape[-1])
     out = np.empty((flat.shape[0], cfg.head_dim), np.int32)
     L = lib()
     for i in range(flat.shape[0]):
         r = np.ascontiguousarray(flat[i])
         for d in range(cfg.head_dim):
-            out[i, d] = L.orc_get_code(_p(r), d, cfg.bits)
+            out[i, d] = L.orc_get_code(_p(r), d, bits)
     return out.reshape(*rows.shape[:-1], cfg.head_dim)
 
 
@@ -206,10 +223,10 @@ class SeqCache:
         assert cap % cfg.group == 0
         H, D, G = cfg.num_kv_heads, cfg.head_dim, cfg.group
         self.cfg, self.cap = cfg, cap
-        self.k_codes = np.zeros((H, cap, cfg.row_bytes), np.uint8)
+        self.k_codes = np.zeros((H, cap, cfg.k_row_bytes), np.uint8)
         self.k_scale = np.zeros((H, cap // G, D), np.uint16)
         self.k_zero = np.zeros((H, cap // G, D), np.uint16)
-        self.v_codes = np.zeros((H, cap, cfg.row_bytes), np.uint8)
+        self.v_codes = np.zeros((H, cap, cfg.v_row_bytes), np.uint8)
         self.v_scale = np.zeros((H, cap, D // G), np.uint16)
         self.v_zero = np.zeros((H, cap, D // G), np.uint16)
         self.k_res = np.zeros((H, cfg.ring, D), np.uint16)

@@ -35,8 +35,11 @@
  *    s == 0 gives all codes 0;
  *  - codes are packed along channels inside one token row, lowest bits first:
  *    channel d sits in byte d*bits/8 at bit (d mod (8/bits))*bits;
- *  - keys: one group per (32 consecutive tokens, channel), aligned to absolute
- *    position 0; values: one group per (token, 32 consecutive channels);
+ *  - keys: one group per (G consecutive tokens, channel), aligned to absolute
+ *    position 0; values: one group per (token, G consecutive channels);
+ *    G = 32 by default, 64 in the config example of "KV-Cache Quantization:
+ *    I Ran the Experiments So You Don't Have To" (which also sets R = 64 and
+ *    separate key and value widths, k_bits and v_bits);
  *  - the residual ring has R+G slots and position p lives in slot p mod (R+G);
  *    a group is flushed when the residual reaches R+G tokens;
  *  - query head hq reads kv head hq / (Hq/Hkv); no mask; the decode query
@@ -60,7 +63,8 @@
 #define ORC_ERR_CAPACITY 3
 
 typedef struct {
-    int32_t bits;        /* 2 or 4 */
+    int32_t k_bits;      /* key code width: 2 or 4 */
+    int32_t v_bits;      /* value code width: 2 or 4 */
     int32_t group;       /* G: tokens per key group, channels per value group */
     int32_t residual;    /* R: fp16 window length, a multiple of G */
     int32_t head_dim;    /* D: a multiple of G */
@@ -207,12 +211,12 @@ int orc_get_code(const uint8_t* row, int d, int bits) { return get_code(row, d, 
  * Keys, per channel: for every stream, every group of G consecutive tokens
  * and every channel d, one (s, z) pair and G codes.
  *   x      [n_streams][n_tokens][D]        dtype bit patterns
- *   codes  [n_streams][n_tokens][D*bits/8] packed rows
+ *   codes  [n_streams][n_tokens][D*k_bits/8] packed rows
  *   scale, zero [n_streams][n_tokens/G][D] fp16 bit patterns
  */
 int orc_quant_keys(const orc_cfg* cfg, int n_streams, int n_tokens, const uint16_t* x,
                    uint8_t* codes, uint16_t* scale, uint16_t* zero) {
-    const int D = cfg->head_dim, G = cfg->group, bits = cfg->bits;
+    const int D = cfg->head_dim, G = cfg->group, bits = cfg->k_bits;
     const int qmax = (1 << bits) - 1, row_bytes = D * bits / 8;
     if (n_tokens % G != 0) return ORC_ERR_ARG;
 #pragma omp parallel for schedule(static)
@@ -238,11 +242,12 @@ int orc_quant_keys(const orc_cfg* cfg, int n_streams, int n_tokens, const uint16
 /*
  * Values, per token: for every token and every group of G consecutive
  * channels, one (s, z) pair and G codes.
+ *   codes  [n_streams][n_tokens][D*v_bits/8]
  *   scale, zero [n_streams][n_tokens][D/G]
  */
 int orc_quant_values(const orc_cfg* cfg, int n_streams, int n_tokens, const uint16_t* x,
                      uint8_t* codes, uint16_t* scale, uint16_t* zero) {
-    const int D = cfg->head_dim, G = cfg->group, bits = cfg->bits;
+    const int D = cfg->head_dim, G = cfg->group, bits = cfg->v_bits;
     const int qmax = (1 << bits) - 1, row_bytes = D * bits / 8;
 #pragma omp parallel for schedule(static)
     for (int st = 0; st < n_streams; ++st) {
@@ -268,7 +273,7 @@ int orc_quant_values(const orc_cfg* cfg, int n_streams, int n_tokens, const uint
 /* ------------------------------------------------------------------ */
 
 /* Buffers of one sequence, laid out exactly as the library's:
- *   k_codes, v_codes  [Hkv][cap][D*bits/8]
+ *   k_codes [Hkv][cap][D*k_bits/8], v_codes [Hkv][cap][D*v_bits/8]
  *   k_scale, k_zero   [Hkv][cap/G][D]
  *   v_scale, v_zero   [Hkv][cap][D/G]
  *   k_res, v_res      [Hkv][R+G][D]  (dtype bit patterns)                */
@@ -290,8 +295,9 @@ int64_t orc_n_packed(const orc_cfg* cfg, int64_t L) {
 
 /* Pack group [n0, n0+G) of head h from the ring into the packed buffers. */
 static void flush_group(const orc_cfg* cfg, const orc_seq* s, int h, int64_t n0) {
-    const int D = cfg->head_dim, G = cfg->group, bits = cfg->bits, R = cfg->residual;
-    const int qmax = (1 << bits) - 1, row_bytes = D * bits / 8, ring = R + G;
+    const int D = cfg->head_dim, G = cfg->group, kb = cfg->k_bits, vb = cfg->v_bits, R = cfg->residual;
+    const int kq = (1 << kb) - 1, vq = (1 << vb) - 1, ring = R + G;
+    const int krow = D * kb / 8, vrow = D * vb / 8;
     const int64_t cap = s->cap;
     float* tile = (float*)malloc(sizeof(float) * G * D); /* [t][d] */
     float* kcol = (float*)malloc(sizeof(float) * G);
@@ -305,9 +311,9 @@ static void flush_group(const orc_cfg* cfg, const orc_seq* s, int h, int64_t n0)
     for (int d = 0; d < D; ++d) {
         for (int t = 0; t < G; ++t) kcol[t] = tile[t * D + d];
         int64_t m = ((int64_t)h * (cap / G) + n0 / G) * D + d;
-        quant_group(kcol, G, 1, qmax, &s->k_scale[m], &s->k_zero[m], c);
+        quant_group(kcol, G, 1, kq, &s->k_scale[m], &s->k_zero[m], c);
         for (int t = 0; t < G; ++t)
-            put_code(s->k_codes + ((int64_t)h * cap + n0 + t) * row_bytes, d, bits, c[t]);
+            put_code(s->k_codes + ((int64_t)h * cap + n0 + t) * krow, d, kb, c[t]);
     }
     /* values: per token over each group of G channels */
     for (int t = 0; t < G; ++t) {
@@ -316,9 +322,9 @@ static void flush_group(const orc_cfg* cfg, const orc_seq* s, int h, int64_t n0)
             tile[t * D + d] = widen(s->v_res[((int64_t)h * ring + slot) * D + d], cfg->dtype);
         for (int k = 0; k < D / G; ++k) {
             int64_t m = ((int64_t)h * cap + n0 + t) * (D / G) + k;
-            quant_group(tile + t * D + k * G, G, 1, qmax, &s->v_scale[m], &s->v_zero[m], c);
+            quant_group(tile + t * D + k * G, G, 1, vq, &s->v_scale[m], &s->v_zero[m], c);
             for (int i = 0; i < G; ++i)
-                put_code(s->v_codes + ((int64_t)h * cap + n0 + t) * row_bytes, k * G + i, bits, c[i]);
+                put_code(s->v_codes + ((int64_t)h * cap + n0 + t) * vrow, k * G + i, vb, c[i]);
         }
     }
     free(tile);
@@ -366,18 +372,18 @@ int orc_append(const orc_cfg* cfg, const orc_seq* s, int32_t* kv_len,
  * k = c * s + z (exact in fp64); residual tokens: the stored value. */
 static void token_kv(const orc_cfg* cfg, const orc_seq* s, int h, int64_t p, int64_t n_packed,
                      double* k, double* v) {
-    const int D = cfg->head_dim, G = cfg->group, bits = cfg->bits, R = cfg->residual;
-    const int row_bytes = D * bits / 8, ring = R + G;
+    const int D = cfg->head_dim, G = cfg->group, kb = cfg->k_bits, vb = cfg->v_bits, R = cfg->residual;
+    const int ring = R + G;
     const int64_t cap = s->cap;
     if (p < n_packed) {
-        const uint8_t* kr = s->k_codes + ((int64_t)h * cap + p) * row_bytes;
-        const uint8_t* vr = s->v_codes + ((int64_t)h * cap + p) * row_bytes;
+        const uint8_t* kr = s->k_codes + ((int64_t)h * cap + p) * (D * kb / 8);
+        const uint8_t* vr = s->v_codes + ((int64_t)h * cap + p) * (D * vb / 8);
         for (int d = 0; d < D; ++d) {
             int64_t mk = ((int64_t)h * (cap / G) + p / G) * D + d;
             int64_t mv = ((int64_t)h * cap + p) * (D / G) + d / G;
-            k[d] = (double)get_code(kr, d, bits) * (double)orc_f16_to_f32(s->k_scale[mk])
+            k[d] = (double)get_code(kr, d, kb) * (double)orc_f16_to_f32(s->k_scale[mk])
                  + (double)orc_f16_to_f32(s->k_zero[mk]);
-            v[d] = (double)get_code(vr, d, bits) * (double)orc_f16_to_f32(s->v_scale[mv])
+            v[d] = (double)get_code(vr, d, vb) * (double)orc_f16_to_f32(s->v_scale[mv])
                  + (double)orc_f16_to_f32(s->v_zero[mv]);
         }
     } else {
@@ -446,9 +452,9 @@ double orc_kv_bytes_plain(int layers, int kv_heads, int head_dim, double bits, d
  * and values (per token, per channel group), and the R+G-slot residual ring. */
 int64_t orc_seq_bytes(const orc_cfg* cfg, int64_t cap) {
     const int64_t D = cfg->head_dim, G = cfg->group, H = cfg->num_kv_heads;
-    const int64_t codes = cap * D * cfg->bits / 8;
+    const int64_t codes = cap * D * (cfg->k_bits + cfg->v_bits) / 8;
     const int64_t kmeta = 2 * (cap / G) * D * 2;
     const int64_t vmeta = 2 * cap * (D / G) * 2;
     const int64_t ring = (cfg->residual + G) * D * 2;
-    return H * (2 * codes + kmeta + vmeta + 2 * ring);
+    return H * (codes + kmeta + vmeta + 2 * ring);
 }

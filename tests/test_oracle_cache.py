@@ -29,15 +29,20 @@ def _rand_kv(rng, H, n, D, dtype="f16"):
     return to_dtype_bits(K, dtype), to_dtype_bits(V, dtype)
 
 
-def test_flush_schedule_closed_form(oracle_lib):
-    cfg = oracle.Cfg(num_kv_heads=1, head_dim=32)
-    G, R = cfg.group, cfg.residual
-    rng = np.random.default_rng(1)
+# (k_bits, v_bits, G, R): the default setting, the config example of "KV-Cache
+# Quantization: I Ran the Experiments So You Don't Have To" (G = R = 64), and mixed widths
+VARIANTS = [(2, 2, 32, 128), (4, 4, 32, 128), (2, 2, 64, 64), (4, 2, 32, 64), (2, 4, 64, 128)]
+
+
+@pytest.mark.parametrize("G,R", [(32, 128), (64, 64), (32, 64), (64, 128)])
+def test_flush_schedule_closed_form(oracle_lib, G, R):
+    cfg = oracle.Cfg(num_kv_heads=1, head_dim=64, group=G, residual=R)
+    rng = np.random.default_rng(1 + G + R)
     s = oracle.SeqCache(cfg, 1024)
     L = 0
     while L < 900:
         n = int(rng.integers(0, 70))
-        K, V = _rand_kv(rng, 1, n, 32)
+        K, V = _rand_kv(rng, 1, n, 64)
         assert s.append(K, V) == oracle.OK
         L += n
         assert s.L == L
@@ -47,13 +52,12 @@ def test_flush_schedule_closed_form(oracle_lib):
         assert (r == L) if L < R else (R <= r <= R + G - 1)
 
 
-@pytest.mark.parametrize("bits", [2, 4])
-def test_nothing_packed_beyond_n_packed(oracle_lib, bits):
+@pytest.mark.parametrize("kb,vb,G,R", VARIANTS)
+def test_nothing_packed_beyond_n_packed(oracle_lib, kb, vb, G, R):
     """Groups are packed exactly when the residual reaches R+G: after every append the
     packed buffers hold nothing past n_packed(L) (they keep a sentinel there)."""
-    cfg = oracle.Cfg(bits=bits, num_kv_heads=2, head_dim=64)
-    G = cfg.group
-    rng = np.random.default_rng(30 + bits)
+    cfg = oracle.Cfg(k_bits=kb, v_bits=vb, num_kv_heads=2, head_dim=64, group=G, residual=R)
+    rng = np.random.default_rng(30 + kb + 3 * vb + G + R)
     s = oracle.SeqCache(cfg, 512)
     for name in ("k_codes", "v_codes"):
         getattr(s, name)[...] = 0xAB
@@ -70,10 +74,10 @@ def test_nothing_packed_beyond_n_packed(oracle_lib, bits):
         assert not np.all(s.k_codes[:, :P] == 0xAB) or P == 0
 
 
-@pytest.mark.parametrize("bits", [2, 4])
-def test_streaming_equals_bulk(oracle_lib, bits):
-    cfg = oracle.Cfg(bits=bits, num_q_heads=4, num_kv_heads=2, head_dim=64)
-    rng = np.random.default_rng(2 + bits)
+@pytest.mark.parametrize("kb,vb,G,R", VARIANTS)
+def test_streaming_equals_bulk(oracle_lib, kb, vb, G, R):
+    cfg = oracle.Cfg(k_bits=kb, v_bits=vb, num_q_heads=4, num_kv_heads=2, head_dim=64, group=G, residual=R)
+    rng = np.random.default_rng(2 + kb + 3 * vb + G + R)
     n = 517
     K, V = _rand_kv(rng, 2, n, 64)
     bulk = oracle.SeqCache(cfg, 512)
@@ -93,20 +97,23 @@ def test_streaming_equals_bulk(oracle_lib, bits):
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_packed_history_matches_codec_and_ring_holds_inputs(oracle_lib, dtype):
+@pytest.mark.parametrize("kb,vb,G,R", [(2, 2, 32, 128), (2, 4, 64, 64), (4, 2, 64, 128)])
+def test_packed_history_matches_codec_and_ring_holds_inputs(oracle_lib, dtype, kb, vb, G, R):
     dt = oracle.BF16 if dtype == "bf16" else oracle.F16
-    cfg = oracle.Cfg(bits=2, num_q_heads=2, num_kv_heads=2, head_dim=64, dtype=dt)
-    rng = np.random.default_rng(5)
+    cfg = oracle.Cfg(k_bits=kb, v_bits=vb, num_q_heads=2, num_kv_heads=2, head_dim=64, dtype=dt, group=G,
+                     residual=R)
+    rng = np.random.default_rng(5 + G + R)
     n = 450
     K, V = _rand_kv(rng, 2, n, 64, dtype)
     s = oracle.SeqCache(cfg, 384)
     assert s.append(K, V) == oracle.OK
     P = oracle.n_packed(cfg, n)
-    assert P == 320
+    assert P == G * ((n - R) // G)
     kc, ks, kz = oracle.quant_keys(cfg, np.ascontiguousarray(K[:, :P]))
     vc, vs, vz = oracle.quant_values(cfg, np.ascontiguousarray(V[:, :P]))
+    assert kc.shape[-1] == 64 * kb // 8 and vc.shape[-1] == 64 * vb // 8
     assert np.array_equal(s.k_codes[:, :P], kc) and np.array_equal(s.v_codes[:, :P], vc)
-    assert np.array_equal(s.k_scale[:, :P // 32], ks) and np.array_equal(s.k_zero[:, :P // 32], kz)
+    assert np.array_equal(s.k_scale[:, :P // G], ks) and np.array_equal(s.k_zero[:, :P // G], kz)
     assert np.array_equal(s.v_scale[:, :P], vs) and np.array_equal(s.v_zero[:, :P], vz)
     for p in range(P, n):
         assert np.array_equal(s.k_res[:, p % cfg.ring], K[:, p])
@@ -154,26 +161,27 @@ def test_attention_unquantized_matches_sdpa(oracle_lib, L, dtype):
         assert np.array_equal(got, np.repeat(f(V)[:, 0], 4, axis=0))
 
 
-@pytest.mark.parametrize("bits", [2, 4])
-def test_attention_planted_cache_matches_sdpa(oracle_lib, bits):
+@pytest.mark.parametrize("kb,vb,G,R", VARIANTS)
+def test_attention_planted_cache_matches_sdpa(oracle_lib, kb, vb, G, R):
     """Packed tokens built on exact grids decode without error, so the oracle's
-    attention over packed + residual tokens must equal exact attention."""
-    D, H, g, G = 64, 2, 4, 32
-    cfg = oracle.Cfg(bits=bits, num_q_heads=H * g, num_kv_heads=H, head_dim=D)
-    qmax = (1 << bits) - 1
-    rng = np.random.default_rng(8 + bits)
-    L = 333                                  # 192 packed (6 groups) + 141 residual
+    attention over packed + residual tokens must equal exact attention. Keys and
+    values use their own code widths (codes 0 and qmax planted in every group)."""
+    D, H, g = 128, 2, 4
+    cfg = oracle.Cfg(k_bits=kb, v_bits=vb, num_q_heads=H * g, num_kv_heads=H, head_dim=D, group=G, residual=R)
+    kq, vq = (1 << kb) - 1, (1 << vb) - 1
+    rng = np.random.default_rng(8 + kb + 3 * vb + G + R)
+    L = 333                                  # e.g. 192 packed (6 groups of 32) + 141 residual
     P = oracle.n_packed(cfg, L)
-    assert P == 192
+    assert P == G * ((L - R) // G) and P > 0
     # keys: per (head, group, channel) a power-of-two scale and zero; codes use 0 and qmax
     sk = np.ldexp(1.0, rng.integers(-4, 0, size=(H, L // G + 1, D)))
     zk = rng.integers(-16, 16, size=sk.shape) * sk
-    ck = planted_codes(rng, (H, L // G + 1, G, D), qmax, axis=2).reshape(H, -1, D)[:, :L]
+    ck = planted_codes(rng, (H, L // G + 1, G, D), kq, axis=2).reshape(H, -1, D)[:, :L]
     K = np.repeat(zk, G, axis=1)[:, :L] + ck * np.repeat(sk, G, axis=1)[:, :L]
     # values: per (head, token, channel group)
     sv = np.ldexp(1.0, rng.integers(-4, 0, size=(H, L, D // G)))
     zv = rng.integers(-16, 16, size=sv.shape) * sv
-    cv = planted_codes(rng, (H, L, D // G, G), qmax, axis=3).reshape(H, L, D)
+    cv = planted_codes(rng, (H, L, D // G, G), vq, axis=3).reshape(H, L, D)
     V = np.repeat(zv, G, axis=2) + cv * np.repeat(sv, G, axis=2)
     Kb, Vb = to_dtype_bits(K, "f16"), to_dtype_bits(V, "f16")
     s = oracle.SeqCache(cfg, 256)

@@ -31,7 +31,7 @@ def f16(bits_u16):
 
 
 def planted_codes(rng, shape, qmax, axis):
-    """Random codes in [0, qmax] where every group along `axis` (length 32) holds a 0 and a qmax."""
+    """Random codes in [0, qmax] where every group along `axis` holds a 0 and a qmax."""
     c = rng.integers(0, qmax + 1, size=shape)
     c = np.moveaxis(c, axis, -1)
     flat = c.reshape(-1, c.shape[-1])
@@ -43,10 +43,11 @@ def planted_codes(rng, shape, qmax, axis):
 
 @pytest.mark.parametrize("bits", [2, 4])
 @pytest.mark.parametrize("dtype", [F16, BF16])
-def test_planted_grid_keys(oracle_lib, bits, dtype):
-    rng = np.random.default_rng(10 + bits + 7 * dtype)
-    S, T, D, G = 3, 96, 64, 32
-    cfg = oracle.Cfg(bits=bits, head_dim=D, dtype=dtype)
+@pytest.mark.parametrize("G", [32, 64])
+def test_planted_grid_keys(oracle_lib, bits, dtype, G):
+    rng = np.random.default_rng(10 + bits + 7 * dtype + G)
+    S, T, D = 3, 3 * G, 64
+    cfg = oracle.Cfg(bits=bits, head_dim=D, dtype=dtype, group=G)
     qmax = (1 << bits) - 1
     # one power-of-two scale and one zero (a multiple of the scale) per (stream, group, channel)
     k = rng.integers(-6, 3, size=(S, T // G, D))
@@ -64,10 +65,11 @@ def test_planted_grid_keys(oracle_lib, bits, dtype):
 
 @pytest.mark.parametrize("bits", [2, 4])
 @pytest.mark.parametrize("dtype", [F16, BF16])
-def test_planted_grid_values(oracle_lib, bits, dtype):
-    rng = np.random.default_rng(20 + bits + 7 * dtype)
-    S, T, D, G = 2, 40, 128, 32
-    cfg = oracle.Cfg(bits=bits, head_dim=D, dtype=dtype)
+@pytest.mark.parametrize("G", [32, 64])
+def test_planted_grid_values(oracle_lib, bits, dtype, G):
+    rng = np.random.default_rng(20 + bits + 7 * dtype + G)
+    S, T, D = 2, 40, 128
+    cfg = oracle.Cfg(bits=bits, head_dim=D, dtype=dtype, group=G)
     qmax = (1 << bits) - 1
     k = rng.integers(-6, 3, size=(S, T, D // G))
     s = np.ldexp(1.0, k)
@@ -108,7 +110,7 @@ def test_constant_group(oracle_lib):
 
 def _dequant_keys(cfg, codes, s, z):
     G = cfg.group
-    c = unpack(codes, cfg.bits, cfg.head_dim)
+    c = unpack(codes, cfg.k_bits, cfg.head_dim)
     return c * np.repeat(f16(s), G, axis=1) + np.repeat(f16(z), G, axis=1)
 
 
@@ -123,10 +125,11 @@ def _structured_inputs(rng, S, T, D, dtype):
 
 @pytest.mark.parametrize("bits", [2, 4])
 @pytest.mark.parametrize("dtype", [F16, BF16])
-def test_keys_brute_force_and_invariants(oracle_lib, bits, dtype):
-    rng = np.random.default_rng(30 + bits + dtype)
-    S, T, D, G = 2, 64, 64, 32
-    cfg = oracle.Cfg(bits=bits, head_dim=D, dtype=dtype)
+@pytest.mark.parametrize("G", [32, 64])
+def test_keys_brute_force_and_invariants(oracle_lib, bits, dtype, G):
+    rng = np.random.default_rng(30 + bits + dtype + G)
+    S, T, D = 2, 128, 64
+    cfg = oracle.Cfg(bits=bits, head_dim=D, dtype=dtype, group=G)
     qmax = (1 << bits) - 1
     xb, x = _structured_inputs(rng, S, T, D, dtype)
     codes, sb, zb = oracle.quant_keys(cfg, xb)
@@ -156,10 +159,11 @@ def test_keys_brute_force_and_invariants(oracle_lib, bits, dtype):
 
 @pytest.mark.parametrize("bits", [2, 4])
 @pytest.mark.parametrize("dtype", [F16, BF16])
-def test_values_brute_force_and_invariants(oracle_lib, bits, dtype):
-    rng = np.random.default_rng(40 + bits + dtype)
-    S, T, D, G = 2, 37, 128, 32
-    cfg = oracle.Cfg(bits=bits, head_dim=D, dtype=dtype)
+@pytest.mark.parametrize("G", [32, 64])
+def test_values_brute_force_and_invariants(oracle_lib, bits, dtype, G):
+    rng = np.random.default_rng(40 + bits + dtype + G)
+    S, T, D = 2, 37, 128
+    cfg = oracle.Cfg(bits=bits, head_dim=D, dtype=dtype, group=G)
     qmax = (1 << bits) - 1
     xb, x = _structured_inputs(rng, S, T, D, dtype)
     codes, sb, zb = oracle.quant_values(cfg, xb)

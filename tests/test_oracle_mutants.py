@@ -34,6 +34,14 @@ MUTANTS = {
     "flush_early": ("if (p + 1 - n_packed == R + G) {", "if (p + 1 - n_packed == R + G - 1) {"),
     # residual ring indexed modulo R instead of R + G
     "ring_modulus": ("const int ring = R + G;\n    int64_t L = *kv_len;", "const int ring = R;\n    int64_t L = *kv_len;"),
+    # flushed values coded at the key width
+    "value_width": ("const int kq = (1 << kb) - 1, vq = (1 << vb) - 1, ring = R + G;",
+                    "const int kq = (1 << kb) - 1, vq = (1 << kb) - 1, ring = R + G;"),
+    # dequantized keys read at the value width
+    "key_read_width": ("k[d] = (double)get_code(kr, d, kb)", "k[d] = (double)get_code(kr, d, vb)"),
+    # value metadata indexed with 32-channel groups whatever G is
+    "value_group_fixed": ("int64_t mv = ((int64_t)h * cap + p) * (D / G) + d / G;",
+                          "int64_t mv = ((int64_t)h * cap + p) * (D / G) + d / 32 % (D / G);"),
 }
 
 
