@@ -3,12 +3,13 @@
 
 One step = one decode step of the whole path for every sequence of the
 batch: kivi_append_flush appends one new K/V token per sequence (quantizing
-and packing a 32-token group whenever the residual window overflows), then
-kivi_decode_attn runs split-K decode attention over the packed 2-bit cache.
+and packing a G-token group whenever the residual window overflows), then
+kivi_decode_attn runs split-K decode attention over the packed cache.
 
 Default workload: Llama-3-8B GQA decode layer shape, 64 sequences, 32 query
 heads over 8 kv heads, head_dim 128, 32768 cached tokens per sequence, bf16
-inputs, 2-bit codes, G = 32, R = 128. Inputs are synthetic and seeded; the
+inputs, 2-bit codes, G = 32, R = 128 (--bits, --k-bits, --v-bits, --group and
+--residual select the other settings). Inputs are synthetic and seeded; the
 cache (about 1.64 GB) is larger than L2, so no flush is needed between steps.
 
 Prints one JSON line. value = KV tokens attended per second over the timed
@@ -63,15 +64,25 @@ def workload_spec(args):
         wl = wl.replace(lengths=(args.context,) * wl.batch)
     if args.bits:
         wl = wl.replace(bits=args.bits)
+    if args.group:
+        wl = wl.replace(group=args.group)
+    if args.residual:
+        wl = wl.replace(residual=args.residual)
     return wl
 
 
-def attn_bytes(wl, lengths, bits):
-    """Algorithmic bytes one decode launch must read: per (token, kv head) 96 B
-    (2-bit: 32 B key codes + 16 B key scale/zero share + 32 B value codes +
-    16 B value scale/zero) or 160 B (4-bit); 512 B per residual token (fp16/bf16 K and V)."""
+def kv_bits(args, wl):
+    """Key and value code widths: --k-bits / --v-bits where given, else the workload's."""
+    return (getattr(args, "k_bits", 0) or wl.bits), (getattr(args, "v_bits", 0) or wl.bits)
+
+
+def attn_bytes(wl, lengths, kb, vb):
+    """Algorithmic bytes one decode launch must read: per packed (token, kv head) the key
+    and value codes (D kb / 8 + D vb / 8 B) and the fp16 scale and zero shares of keys and
+    values (2 * 2 * 2 * D / G B): 96 B at 2 bits and G = 32 (32 + 16 + 32 + 16), 160 B at
+    4 bits; 512 B per residual token (fp16/bf16 K and V)."""
     R, G, D, H = wl.residual, wl.group, wl.head_dim, wl.num_kv_heads
-    per_packed = (2 * D * bits // 8) + 2 * 2 * 2 * D // G  # codes K+V, fp16 (s, z) K and V per element/G
+    per_packed = (D * kb // 8 + D * vb // 8) + 2 * 2 * 2 * D // G
     total = 0
     for L in lengths:
         npk = G * (max(L - R, 0) // G)
@@ -82,9 +93,10 @@ def attn_bytes(wl, lengths, bits):
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per (token, kv head) of one
 # decode launch, from an ncu capture of the kernel in its current version on the 8-sequence
 # case of the Llama-3-8B GQA workload (2-bit, bf16): 209.84 MB for 8 x 8 x 32772 units.
-# Keyed by (kernel, bits, query group, input dtype); a configuration without an entry
-# reports traffic as null. Profile summary: profiles/decode_kernels_llama3-8b-gqa_b8_ctx32768.md.
-NCU_TRAFFIC_BYTES_PER_UNIT = {("decode_mma_kernel", 2, 4, "bf16"): 209_839_872 / (8 * 8 * 32772)}
+# Keyed by (kernel, k_bits, v_bits, G, R, query group, input dtype); a configuration without
+# an entry reports traffic as null. Profile summary:
+# profiles/decode_kernels_llama3-8b-gqa_b8_ctx32768.md.
+NCU_TRAFFIC_BYTES_PER_UNIT = {("decode_mma_kernel", 2, 2, 32, 128, 4, "bf16"): 209_839_872 / (8 * 8 * 32772)}
 
 
 def reduce_max(x: float, device=None) -> float:
@@ -103,13 +115,13 @@ def job_throughput(units_per_rank: float, world: int, max_ms: float) -> float:
     return units_per_rank * world / (max_ms / 1e3)
 
 
-def prefill_io_bytes(wl, L):
+def prefill_io_bytes(wl, L, kb, vb):
     """Algorithmic bytes of appending L tokens to an empty sequence: the K and V inputs read,
     the packed codes and fp16 scale/zero written for n_packed(L) tokens, the ring rows written."""
     R, G, D, H = wl.residual, wl.group, wl.head_dim, wl.num_kv_heads
     npk = G * (max(L - R, 0) // G)
     read = 2 * L * D * 2
-    written = npk * (2 * D * wl.bits // 8 + 2 * 2 * 2 * D // G) + (L - npk) * 2 * D * 2
+    written = npk * (D * kb // 8 + D * vb // 8 + 2 * 2 * 2 * D // G) + (L - npk) * 2 * D * 2
     return H * (read + written)
 
 
@@ -209,13 +221,15 @@ def run_gpu(args, rank, world, local_rank):
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     wl = workload_spec(args)
-    B, Hq, H, D, bits = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.bits
+    B, Hq, H, D = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
+    kb, vb = kv_bits(args, wl)
     L0s = list(wl.lengths)
     L0 = max(L0s)
     n_steps = args.warmup + args.steps
-    cap = ((L0 + n_steps + args.steps + 31) // 32) * 32   # decode steps of both timed legs
-    cfg = kivi.Config(bits=bits, head_dim=D, num_q_heads=Hq, num_kv_heads=H,
-                      dtype=kivi.BF16 if wl.dtype == "bf16" else kivi.F16)
+    G = wl.group
+    cap = ((L0 + n_steps + args.steps + G - 1) // G) * G   # decode steps of both timed legs
+    cfg = kivi.Config(k_bits=kb, v_bits=vb, group=G, residual=wl.residual, head_dim=D, num_q_heads=Hq,
+                      num_kv_heads=H, dtype=kivi.BF16 if wl.dtype == "bf16" else kivi.F16)
     cache = kivi.KVCache(cfg, B, cap, device, paged=args.paged, page_seed=1)
 
     # prefill (outside the timed steps): every sequence's K and V drawn on the GPU, then one
@@ -239,7 +253,7 @@ def run_gpu(args, rank, world, local_rank):
     pe1.record()
     torch.cuda.synchronize()
     prefill_ms = pe0.elapsed_time(pe1)
-    prefill_bytes = sum(prefill_io_bytes(wl, L) for L in L0s)
+    prefill_bytes = sum(prefill_io_bytes(wl, L, kb, vb) for L in L0s)
     del ks, vs
     torch.cuda.synchronize()
     cache.max_len = L0
@@ -258,7 +272,7 @@ def run_gpu(args, rank, world, local_rank):
 
     # caches smaller than twice the 129 MB L2 are flushed (a 512 MB write) before every
     # step, outside the per-step timing
-    cache_bytes = attn_bytes(wl, L0s, bits)
+    cache_bytes = attn_bytes(wl, L0s, kb, vb)
     flush = cache_bytes < 256 << 20
     flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=device) if flush else None
     step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -299,7 +313,7 @@ def run_gpu(args, rank, world, local_rank):
 
     lens_per_step = [[L + args.warmup + i + 1 for L in L0s] for i in range(args.steps)]
     kv_tokens = sum(sum(ls) for ls in lens_per_step)
-    bytes_per_step = [attn_bytes(wl, ls, bits) for ls in lens_per_step]
+    bytes_per_step = [attn_bytes(wl, ls, kb, vb) for ls in lens_per_step]
     units_per_step = [wl.num_kv_heads * sum(ls) for ls in lens_per_step]
 
     # ------------------------------------------------------------ end to end through the public API
@@ -353,16 +367,16 @@ def run_e2e(args, cache, wl, device, L_start, max_len, out_dev):
 
 
 # ---------------------------------------------------------------- CPU oracle arm
-def oracle_sample(wl, n_steps, budget_s=20.0):
+def oracle_sample(wl, n_steps, kb, vb, budget_s=20.0):
     """The oracle on a bounded sample of the workload: one sequence (all kv and query
     heads) prefilled to the workload's context, then n_steps decode steps of
     append + attention. Returns (KV-tokens/s, threads, description)."""
     import oracle
     oracle.build()
     L0 = wl.lengths[0]
-    ocfg = oracle.Cfg(bits=wl.bits, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
-                      dtype=oracle.BF16 if wl.dtype == "bf16" else oracle.F16)
-    cap = ((L0 + n_steps + 31) // 32) * 32
+    ocfg = oracle.Cfg(k_bits=kb, v_bits=vb, group=wl.group, residual=wl.residual, num_q_heads=wl.num_q_heads,
+                      num_kv_heads=wl.num_kv_heads, dtype=oracle.BF16 if wl.dtype == "bf16" else oracle.F16)
+    cap = ((L0 + n_steps + wl.group - 1) // wl.group) * wl.group
     seq = oracle.SeqCache(ocfg, cap)
     K, V = wl.kv_seq(0, 0, L0)
     assert seq.append(K, V) == oracle.OK
@@ -394,38 +408,45 @@ def main():
     ap.add_argument("--impl", default="kivi", choices=["kivi", "reference"])
     ap.add_argument("--batch", type=int, default=0)
     ap.add_argument("--context", type=int, default=0)
-    ap.add_argument("--bits", type=int, default=0)
+    ap.add_argument("--bits", type=int, default=0, help="code width of keys and values (default: 2)")
+    ap.add_argument("--k-bits", type=int, default=0, help="key code width (overrides --bits)")
+    ap.add_argument("--v-bits", type=int, default=0, help="value code width (overrides --bits)")
+    ap.add_argument("--group", type=int, default=0, help="G: 32 (default) or 64")
+    ap.add_argument("--residual", type=int, default=0, help="R: a multiple of G (default 128)")
     ap.add_argument("--workload", type=int, default=2, choices=[0, 1, 2, 3, 4],
                     help="0 tiny, 1 Llama-2-7B MHA, 2 Llama-3-8B GQA (default), 3 streaming, 4 long varlen")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--paged", action="store_true",
-                    help="packed cache in shared 32-token pages behind block tables (random page order)")
+                    help="packed cache in shared G-token pages behind block tables (random page order)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
     wl = workload_spec(args)
+    kb, vb = kv_bits(args, wl)
+    widths = f"{kb}-bit" if kb == vb else f"{kb}-bit key / {vb}-bit value"
     ctx = (f"{wl.lengths[0]} cached tokens" if len(set(wl.lengths)) == 1 else
            f"{min(wl.lengths)}..{max(wl.lengths)} cached tokens (mean {sum(wl.lengths) / len(wl.lengths):.0f})")
     config = {
         "workload": (f"{WORKLOAD_NAMES[args.workload]}: {wl.batch} sequences x {ctx}, "
                      f"{wl.num_q_heads} query / {wl.num_kv_heads} kv heads, head_dim {wl.head_dim}, "
-                     f"{wl.bits}-bit KIVI (G=32, R=128), {wl.dtype} inputs"),
+                     f"{widths} KIVI (G={wl.group}, R={wl.residual}), {wl.dtype} inputs"),
         "batch": wl.batch, "context": wl.lengths[0] if len(set(wl.lengths)) == 1 else "varlen",
         "q_heads": wl.num_q_heads, "kv_heads": wl.num_kv_heads,
-        "head_dim": wl.head_dim, "bits": wl.bits, "group": wl.group, "residual": wl.residual,
-        "input_dtype": wl.dtype, "step": "append 1 token/sequence (+ group flush every 32 steps) + decode attention",
+        "head_dim": wl.head_dim, "bits": wl.bits if kb == vb else None, "k_bits": kb, "v_bits": vb,
+        "group": wl.group, "residual": wl.residual, "input_dtype": wl.dtype,
+        "step": f"append 1 token/sequence (+ group flush every {wl.group} steps) + decode attention",
         "l2": ("flushed before every step (512 MB write, outside the step timing): the cache is smaller than L2"
-               if attn_bytes(wl, list(wl.lengths), wl.bits) < 256 << 20 else
+               if attn_bytes(wl, list(wl.lengths), kb, vb) < 256 << 20 else
                "no flush: the packed cache is larger than L2 (129 MB)"),
         "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-        "layout": "paged: 32-token pages of one shared pool in random order" if args.paged else "contiguous",
+        "layout": f"paged: {wl.group}-token pages of one shared pool in random order" if args.paged else "contiguous",
     }
     if args.impl == "reference":
         if rank != 0:
             return
-        v, threads, desc, dt = oracle_sample(wl, args.warmup + args.steps, budget_s=60.0)
+        v, threads, desc, dt = oracle_sample(wl, args.warmup + args.steps, kb, vb, budget_s=60.0)
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "KV-tokens/s", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / (args.warmup + args.steps), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
@@ -457,7 +478,8 @@ def main():
     # the decode kernel the library picks: tensor-core path for query groups of 1, 2 or 4
     group = config["q_heads"] // config["kv_heads"]
     kernel = "decode_mma_kernel" if group in (1, 2, 4) else "decode_split_kernel"
-    per_unit = None if args.paged else NCU_TRAFFIC_BYTES_PER_UNIT.get((kernel, config["bits"], group, config["input_dtype"]))
+    per_unit = None if args.paged else NCU_TRAFFIC_BYTES_PER_UNIT.get(
+        (kernel, kb, vb, wl.group, wl.residual, group, config["input_dtype"]))
     traffic = per_unit * sum(res["attn_units"]) / len(res["attn_units"]) if per_unit else None
     line = {
         "metric": METRIC, "value": value, "unit": "KV-tokens/s", "n_gpus": world, "steps": args.steps,
@@ -476,7 +498,7 @@ def main():
         "clocks": res["clocks"],
     }
     if not args.no_cpu_baseline:
-        v, threads, desc, dt = oracle_sample(wl, 4, budget_s=20.0)
+        v, threads, desc, dt = oracle_sample(wl, 4, kb, vb, budget_s=20.0)
         line["cpu_baseline"] = {"value": v, "unit": "KV-tokens/s", "cores": threads, "kind": "oracle",
                                 "sample": desc}
     print(json.dumps(line))

@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libkivi.so")
 
 F16, BF16 = 0, 1
 OK, ERR_ARG, ERR_UNSUPPORTED, ERR_CAPACITY, ERR_WORKSPACE, ERR_CUDA, ERR_LENGTH = range(7)
-GROUP = 32
+GROUP = 32          # the default G
 
 _TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16}
 
@@ -38,8 +38,8 @@ class KiviError(RuntimeError):
 
 
 class _Cfg(ctypes.Structure):
-    _fields_ = [("bits", ctypes.c_int32), ("group", ctypes.c_int32), ("residual", ctypes.c_int32),
-                ("head_dim", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+    _fields_ = [("k_bits", ctypes.c_int32), ("v_bits", ctypes.c_int32), ("group", ctypes.c_int32),
+                ("residual", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("dtype", ctypes.c_int32)]
 
 
@@ -112,7 +112,8 @@ def _ptr(t: torch.Tensor | None) -> ctypes.c_void_p:
 
 @dataclass(frozen=True)
 class Config:
-    """A KIVI configuration (mirrors kivi_cfg)."""
+    """A KIVI configuration (mirrors kivi_cfg). `bits` sets both code widths; k_bits and
+    v_bits, when given, set the key and value widths apart."""
     bits: int = 2
     head_dim: int = 128
     num_q_heads: int = 1
@@ -120,9 +121,17 @@ class Config:
     dtype: int = F16
     residual: int = 128
     group: int = GROUP
+    k_bits: int | None = None
+    v_bits: int | None = None
+
+    def __post_init__(self):
+        if self.k_bits is None:
+            object.__setattr__(self, "k_bits", self.bits)
+        if self.v_bits is None:
+            object.__setattr__(self, "v_bits", self.bits)
 
     def c(self) -> _Cfg:
-        return _Cfg(self.bits, self.group, self.residual, self.head_dim, self.num_q_heads,
+        return _Cfg(self.k_bits, self.v_bits, self.group, self.residual, self.head_dim, self.num_q_heads,
                     self.num_kv_heads, self.dtype)
 
     @property
@@ -130,8 +139,12 @@ class Config:
         return _TORCH_DTYPE[self.dtype]
 
     @property
-    def row_bytes(self) -> int:
-        return self.head_dim * self.bits // 8
+    def k_row_bytes(self) -> int:
+        return self.head_dim * self.k_bits // 8
+
+    @property
+    def v_row_bytes(self) -> int:
+        return self.head_dim * self.v_bits // 8
 
     @property
     def ring(self) -> int:
@@ -154,12 +167,12 @@ class Config:
 
 # ---------------------------------------------------------------- codec
 def quant_keys(cfg: Config, x: torch.Tensor):
-    """Per-channel key quantization. x [S][T][D] (cfg dtype, T % 32 == 0) ->
-    codes [S][T][D*bits/8] u8, scale/zero [S][T/32][D] (fp16 bit patterns as int16)."""
+    """Per-channel key quantization. x [S][T][D] (cfg dtype, T % G == 0) ->
+    codes [S][T][D*k_bits/8] u8, scale/zero [S][T/G][D] (fp16 bit patterns as int16)."""
     _require_cuda(x, "x")
     S, T, D = x.shape
-    codes = torch.empty((S, T, cfg.row_bytes), dtype=torch.uint8, device=x.device)
-    scale = torch.empty((S, T // GROUP, D), dtype=torch.int16, device=x.device)
+    codes = torch.empty((S, T, cfg.k_row_bytes), dtype=torch.uint8, device=x.device)
+    scale = torch.empty((S, T // cfg.group, D), dtype=torch.int16, device=x.device)
     zero = torch.empty_like(scale)
     _check(lib().kivi_quant_keys(cfg.c(), S, T, _ptr(x), _ptr(codes), _ptr(scale), _ptr(zero),
                                  _stream(x.device)), "kivi_quant_keys")
@@ -167,11 +180,11 @@ def quant_keys(cfg: Config, x: torch.Tensor):
 
 
 def quant_values(cfg: Config, x: torch.Tensor):
-    """Per-token value quantization. x [S][T][D] -> codes [S][T][D*bits/8], scale/zero [S][T][D/32]."""
+    """Per-token value quantization. x [S][T][D] -> codes [S][T][D*v_bits/8], scale/zero [S][T][D/G]."""
     _require_cuda(x, "x")
     S, T, D = x.shape
-    codes = torch.empty((S, T, cfg.row_bytes), dtype=torch.uint8, device=x.device)
-    scale = torch.empty((S, T, D // GROUP), dtype=torch.int16, device=x.device)
+    codes = torch.empty((S, T, cfg.v_row_bytes), dtype=torch.uint8, device=x.device)
+    scale = torch.empty((S, T, D // cfg.group), dtype=torch.int16, device=x.device)
     zero = torch.empty_like(scale)
     _check(lib().kivi_quant_values(cfg.c(), S, T, _ptr(x), _ptr(codes), _ptr(scale), _ptr(zero),
                                    _stream(x.device)), "kivi_quant_values")
@@ -187,30 +200,31 @@ class KVCache:
 
     def __init__(self, cfg: Config, nseq: int, cap_tokens: int, device="cuda", paged: bool = False,
                  page_seed: int = 0, spare_pages: int = 0):
-        """paged: the packed buffers are one pool of 32-token pages shared by all sequences,
+        """paged: the packed buffers are one pool of G-token pages shared by all sequences,
         each sequence's groups mapped through a block table (kivi.h, paged layout); the pool
-        has nseq * cap_tokens / 32 + spare_pages pages, handed out in a seeded random order."""
-        if cap_tokens % GROUP:
-            raise ValueError("cap_tokens must be a multiple of 32")
+        has nseq * cap_tokens / G + spare_pages pages, handed out in a seeded random order."""
+        if cap_tokens % cfg.group:
+            raise ValueError("cap_tokens must be a multiple of G")
         if not torch.cuda.is_available():
             raise RuntimeError("KIVI kernels need a CUDA device; there is no CPU path")
         self.cfg, self.nseq, self.cap, self.paged = cfg, nseq, cap_tokens, paged
         self.device = torch.device(device)
-        H, D, G = cfg.num_kv_heads, cfg.head_dim, GROUP
+        H, D, G = cfg.num_kv_heads, cfg.head_dim, cfg.group
         dev = self.device
         if paged:
             npg = nseq * (cap_tokens // G) + spare_pages
-            self.k_codes = torch.zeros((npg, H, G, cfg.row_bytes), dtype=torch.uint8, device=dev)
+            self.k_codes = torch.zeros((npg, H, G, cfg.k_row_bytes), dtype=torch.uint8, device=dev)
+            self.v_codes = torch.zeros((npg, H, G, cfg.v_row_bytes), dtype=torch.uint8, device=dev)
             self.k_scale = torch.zeros((npg, H, D), dtype=torch.int16, device=dev)
             self.v_scale = torch.zeros((npg, H, G, D // G), dtype=torch.int16, device=dev)
             perm = np.random.default_rng(page_seed).permutation(npg)[:nseq * (cap_tokens // G)]
             self.block_tables = torch.from_numpy(perm.reshape(nseq, cap_tokens // G).astype(np.int32)).to(dev)
         else:
-            self.k_codes = torch.zeros((nseq, H, cap_tokens, cfg.row_bytes), dtype=torch.uint8, device=dev)
+            self.k_codes = torch.zeros((nseq, H, cap_tokens, cfg.k_row_bytes), dtype=torch.uint8, device=dev)
+            self.v_codes = torch.zeros((nseq, H, cap_tokens, cfg.v_row_bytes), dtype=torch.uint8, device=dev)
             self.k_scale = torch.zeros((nseq, H, cap_tokens // G, D), dtype=torch.int16, device=dev)
             self.v_scale = torch.zeros((nseq, H, cap_tokens, D // G), dtype=torch.int16, device=dev)
             self.block_tables = None
-        self.v_codes = torch.zeros_like(self.k_codes)
         self.k_zero = torch.zeros_like(self.k_scale)
         self.v_zero = torch.zeros_like(self.v_scale)
         self.k_res = torch.zeros((nseq, H, cfg.ring, D), dtype=cfg.torch_dtype, device=dev)

@@ -9,14 +9,13 @@
 
 namespace {
 
-using kivi::kGroup;
-
 bool cfg_ok(const kivi_cfg* c) {
     if (c == nullptr) return false;
-    if (c->bits != 2 && c->bits != 4) return false;
-    if (c->group != kGroup) return false;
-    if (c->residual <= 0 || c->residual % kGroup != 0) return false;
-    if (c->head_dim <= 0 || c->head_dim % 32 != 0 || c->head_dim > kivi::kMaxHeadDim) return false;
+    if (c->k_bits != 2 && c->k_bits != 4) return false;
+    if (c->v_bits != 2 && c->v_bits != 4) return false;
+    if (c->group != 32 && c->group != 64) return false;
+    if (c->residual <= 0 || c->residual % c->group != 0) return false;
+    if (c->head_dim <= 0 || c->head_dim % c->group != 0 || c->head_dim > kivi::kMaxHeadDim) return false;
     if (c->num_kv_heads <= 0 || c->num_kv_heads > 65535) return false;
     if (c->num_q_heads <= 0 || c->num_q_heads % c->num_kv_heads != 0) return false;
     if (c->dtype != KIVI_F16 && c->dtype != KIVI_BF16) return false;
@@ -25,14 +24,15 @@ bool cfg_ok(const kivi_cfg* c) {
 
 kivi_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KIVI_OK : KIVI_ERR_CUDA; }
 
-kivi_status codec_common(const kivi_cfg* cfg, int32_t n_streams, int32_t n_tokens, const void* x,
+kivi_status codec_common(const kivi_cfg* cfg, int bits, int32_t n_streams, int32_t n_tokens, const void* x,
                          uint8_t* codes, uint16_t* scale, uint16_t* zero, kivi::CodecArgs* a) {
     if (!cfg_ok(cfg)) return KIVI_ERR_ARG;
     if (n_streams < 0 || n_tokens < 0 || n_streams > 65535) return KIVI_ERR_ARG;
     if (n_streams > 0 && n_tokens > 0 &&
         (x == nullptr || codes == nullptr || scale == nullptr || zero == nullptr))
         return KIVI_ERR_ARG;
-    a->bits = cfg->bits;
+    a->bits = bits;
+    a->G = cfg->group;
     a->D = cfg->head_dim;
     a->dtype = cfg->dtype;
     a->n_streams = n_streams;
@@ -51,16 +51,18 @@ extern "C" {
 kivi_status kivi_quant_keys(const kivi_cfg* cfg, int32_t n_streams, int32_t n_tokens, const void* x_dev,
                             uint8_t* codes_dev, uint16_t* scale_dev, uint16_t* zero_dev, void* stream) {
     kivi::CodecArgs a;
-    const kivi_status st = codec_common(cfg, n_streams, n_tokens, x_dev, codes_dev, scale_dev, zero_dev, &a);
+    const kivi_status st = codec_common(cfg, cfg ? cfg->k_bits : 0, n_streams, n_tokens, x_dev, codes_dev, scale_dev,
+                                        zero_dev, &a);
     if (st != KIVI_OK) return st;
-    if (n_tokens % kGroup != 0) return KIVI_ERR_ARG;
+    if (n_tokens % cfg->group != 0) return KIVI_ERR_ARG;
     return from_cuda(kivi::launch_quant_keys(a, static_cast<cudaStream_t>(stream)));
 }
 
 kivi_status kivi_quant_values(const kivi_cfg* cfg, int32_t n_streams, int32_t n_tokens, const void* x_dev,
                               uint8_t* codes_dev, uint16_t* scale_dev, uint16_t* zero_dev, void* stream) {
     kivi::CodecArgs a;
-    const kivi_status st = codec_common(cfg, n_streams, n_tokens, x_dev, codes_dev, scale_dev, zero_dev, &a);
+    const kivi_status st = codec_common(cfg, cfg ? cfg->v_bits : 0, n_streams, n_tokens, x_dev, codes_dev, scale_dev,
+                                        zero_dev, &a);
     if (st != KIVI_OK) return st;
     return from_cuda(kivi::launch_quant_values(a, static_cast<cudaStream_t>(stream)));
 }
@@ -75,7 +77,9 @@ kivi_status kivi_append_flush(const kivi_cfg* cfg, int32_t nseq, const kivi_seq*
         n_new_dev == nullptr || status_dev == nullptr)
         return KIVI_ERR_ARG;
     kivi::AppendArgs a;
-    a.bits = cfg->bits;
+    a.kb = cfg->k_bits;
+    a.vb = cfg->v_bits;
+    a.G = cfg->group;
     a.D = cfg->head_dim;
     a.R = cfg->residual;
     a.H = cfg->num_kv_heads;
@@ -116,7 +120,9 @@ kivi_status kivi_decode_attn(const kivi_cfg* cfg, int32_t nseq, const kivi_seq* 
     kivi::decode_plan(nseq, cfg->num_kv_heads, cfg->num_q_heads, cfg->head_dim, max_kv_len, &a.chunk,
                       &a.max_splits, &cb, &pb);
     if (workspace_dev == nullptr || workspace_bytes < cb + pb) return KIVI_ERR_WORKSPACE;
-    a.bits = cfg->bits;
+    a.kb = cfg->k_bits;
+    a.vb = cfg->v_bits;
+    a.G = cfg->group;
     a.D = cfg->head_dim;
     a.R = cfg->residual;
     a.Hq = cfg->num_q_heads;
@@ -136,14 +142,14 @@ kivi_status kivi_decode_attn(const kivi_cfg* cfg, int32_t nseq, const kivi_seq* 
 }
 
 kivi_status kivi_seq_buffer_bytes(const kivi_cfg* cfg, int32_t cap_tokens, size_t bytes_out[8]) {
-    if (!cfg_ok(cfg) || cap_tokens < 0 || cap_tokens % kGroup != 0 || bytes_out == nullptr) return KIVI_ERR_ARG;
-    const size_t H = cfg->num_kv_heads, D = cfg->head_dim, cap = cap_tokens;
+    if (!cfg_ok(cfg) || cap_tokens < 0 || cap_tokens % cfg->group != 0 || bytes_out == nullptr) return KIVI_ERR_ARG;
+    const size_t H = cfg->num_kv_heads, D = cfg->head_dim, cap = cap_tokens, G = cfg->group;
     const size_t esz = 2;  // fp16 and bf16
-    const size_t codes = H * cap * D * cfg->bits / 8;
-    const size_t kmeta = H * (cap / kGroup) * D * 2;
-    const size_t vmeta = H * cap * (D / kGroup) * 2;
-    const size_t ring = H * (cfg->residual + kGroup) * D * esz;
-    const size_t sizes[8] = {codes, kmeta, kmeta, codes, vmeta, vmeta, ring, ring};
+    const size_t kcodes = H * cap * D * cfg->k_bits / 8, vcodes = H * cap * D * cfg->v_bits / 8;
+    const size_t kmeta = H * (cap / G) * D * 2;
+    const size_t vmeta = H * cap * (D / G) * 2;
+    const size_t ring = H * (cfg->residual + G) * D * esz;
+    const size_t sizes[8] = {kcodes, kmeta, kmeta, vcodes, vmeta, vmeta, ring, ring};
     memcpy(bytes_out, sizes, sizeof(sizes));
     return KIVI_OK;
 }
@@ -158,7 +164,7 @@ int64_t kivi_seq_bytes(const kivi_cfg* cfg, int32_t cap_tokens) {
 
 int64_t kivi_n_packed(const kivi_cfg* cfg, int64_t kv_len) {
     if (!cfg_ok(cfg) || kv_len < 0) return -1;
-    return kivi::n_packed(kv_len, cfg->residual);
+    return kivi::n_packed(kv_len, cfg->residual, cfg->group);
 }
 
 const char* kivi_status_string(int32_t status) {

@@ -9,9 +9,9 @@
 // group and window sizes from "KV cache quantization with KIVI INT2 setup
 // guide 2026" (G = 32, R = 128).
 //
-// Design. One warp quantizes one 32-token group tile (or, for values, up to
+// Design. One warp quantizes one G-token group tile (or, for values, up to
 // 32 tokens) over a slice of up to 128 channels, entirely in registers: no
-// shared memory and no block barriers. For keys a lane owns four channels and
+// shared memory and no block barriers. G is 32 or 64 (a template parameter). For keys a lane owns four channels and
 // loads them from every token row (each load instruction reads whole rows,
 // coalesced); for values a lane owns one token row. Minimum and maximum run on
 // packed pairs (min/max.f16x2 or .bf16x2); the codes come from one fused
@@ -29,14 +29,19 @@ constexpr int kWarps = kThreads / 32;
 
 // Channels one warp covers of a D-channel tile. Values: 64 where that divides D, else 32
 // (a 64-channel slice holds 32 registers of elements per lane, so that three CTAs of
-// eight warps fit on an SM). Keys: 128 where that divides D (then a lane owns four
-// channels over all 32 tokens and no lane repeats another's per-channel scale and zero;
-// two CTAs per SM; measured 6 % faster on the flush), else as values.
+// eight warps fit on an SM; D is a multiple of G, so G = 64 always gets 64). Keys, G =
+// 32: 128 where that divides D (then a lane owns four channels over all 32 tokens and no
+// lane repeats another's per-channel scale and zero; two CTAs per SM; measured 6 % faster
+// on the flush), else as values; G = 64: 64 (four channels of 32 of the 64 tokens per
+// lane, the same 64 registers).
 __host__ __device__ constexpr int slice_width(int D) { return D % 64 == 0 ? 64 : 32; }
-__host__ __device__ constexpr int key_slice_width(int D) { return D % 128 == 0 ? 128 : slice_width(D); }
-template <int DS>
+__host__ __device__ constexpr int key_slice_width(int D, int G) {
+    return G == 64 ? 64 : (D % 128 == 0 ? 128 : slice_width(D));
+}
+// Registers of elements per lane: DS * TOK / 64 for a DS-channel, TOK-token tile.
+template <int DS, int TOK>
 struct CtasPerSm {
-    static constexpr int kValue = DS == 128 ? 2 : 3;
+    static constexpr int kValue = DS * TOK / 64 >= 64 ? 2 : 3;
 };
 
 template <int DT>
@@ -156,20 +161,20 @@ __device__ __noinline__ uint32_t keys_exact4(const uint16_t* p, float z0, float 
            encode(half_at<DT>(v.y, 0), z2, s2, qmax) << (2 * BITS) | encode(half_at<DT>(v.y, 1), z3, s3, qmax) << (3 * BITS);
 }
 
-// One lane's share of a 32-row x DS-channel tile of 16-bit elements, in registers.
-// Keys: lane l owns channels 4 (l mod DS/4) .. +3 of the slice and the tokens j,
-// j + TS, ... (j = l / (DS/4), TS = 128 / DS): w[2 i], w[2 i + 1] hold token i TS + j.
-// Values: lane l owns token l, w[c] holding channels 2 c and 2 c + 1 of the slice.
-template <int DS>
+// One lane's share of a TOK-row x DS-channel tile of 16-bit elements, in registers.
+// Keys (TOK = G): lane l owns channels 4 (l mod DS/4) .. +3 of the slice and the tokens
+// j, j + TS, ... (j = l / (DS/4), TS = 128 / DS): w[2 i], w[2 i + 1] hold token i TS + j.
+// Values (TOK = 32): lane l owns token l, w[c] holding channels 2 c and 2 c + 1.
+template <int DS, int TOK>
 struct Tile {
-    uint32_t w[DS / 2];
+    uint32_t w[DS * TOK / 64];
 };
 
 // Loads a key tile. row(t) is token t's row at the slice's first channel; where
 // `contiguous` is set (the same on every lane) the rows are known to be row(0) + t * D.
-template <int DS, typename RowFn>
-__device__ __forceinline__ void keys_load(RowFn row, bool contiguous, int D, Tile<DS>& x) {
-    constexpr int LPR = DS / 4, TS = 32 / LPR, NT = 32 / TS;
+template <int DS, int G, typename RowFn>
+__device__ __forceinline__ void keys_load(RowFn row, bool contiguous, int D, Tile<DS, G>& x) {
+    constexpr int LPR = DS / 4, TS = 32 / LPR, NT = G / TS;
     const int lane = threadIdx.x & 31, cq = lane % LPR, j = lane / LPR;
     if (contiguous) {
         const uint16_t* p = row(j) + 4 * cq;
@@ -190,16 +195,17 @@ __device__ __forceinline__ void keys_load(RowFn row, bool contiguous, int D, Til
     }
 }
 
-// Keys of one 32-token group over one DS-channel slice, by one warp, from a tile that
+// Keys of one G-token group over one DS-channel slice, by one warp, from a tile that
 // keys_load() filled; row() as there (used again only on the rare exact paths). codes,
 // scale and zero point at the slice's first channel of token 0's code row and of the
 // group's scale and zero rows. The minimum and maximum come from packed min/max over
 // token pairs and a shuffle across token subsets; where one is a zero, the rule "the
 // first value seen wins" is applied by finding the sign of the first zero in token order.
-template <int BITS, int DT, int DS, typename RowFn>
-__device__ __forceinline__ void keys_compute(const Tile<DS>& x, RowFn row, uint8_t* codes, int code_ld, uint16_t* scale,
-                                             uint16_t* zero) {
-    constexpr int LPR = DS / 4, TS = 32 / LPR, NT = 32 / TS;
+template <int BITS, int DT, int DS, int G, typename RowFn>
+__device__ __forceinline__ void keys_compute(const Tile<DS, G>& x, RowFn row, uint8_t* codes, int code_ld,
+                                             uint16_t* scale, uint16_t* zero) {
+    constexpr int LPR = DS / 4, TS = 32 / LPR, NT = G / TS;
+    static_assert(NT <= 32, "rows to redo are kept in one 32-bit mask");
     const int lane = threadIdx.x & 31, cq = lane % LPR, j = lane / LPR;
     uint32_t mn0 = x.w[0], mx0 = x.w[0], mn1 = x.w[1], mx1 = x.w[1];
 #pragma unroll
@@ -287,7 +293,7 @@ __device__ __forceinline__ void keys_compute(const Tile<DS>& x, RowFn row, uint8
 // Loads one lane's value row: src is the token's row at the slice's first channel
 // (null: this lane has no token).
 template <int DS>
-__device__ __forceinline__ void values_load(const uint16_t* src, Tile<DS>& x) {
+__device__ __forceinline__ void values_load(const uint16_t* src, Tile<DS, 32>& x) {
     if (src == nullptr) return;
 #pragma unroll
     for (int c = 0; c < DS / 8; ++c) {
@@ -299,17 +305,18 @@ __device__ __forceinline__ void values_load(const uint16_t* src, Tile<DS>& x) {
     }
 }
 
-// Values of one token over one DS-channel slice (DS / 32 channel groups), by one lane,
+// Values of one token over one DS-channel slice (DS / G channel groups), by one lane,
 // from the row values_load() read from src (null: no token for this lane); codes, scale
 // and zero point at the slice's first code byte and first group of the token's rows.
 // Packed min/max over channel pairs, then the pair's two halves; a zero minimum or
 // maximum takes the sign of the first zero in channel order. Every lane of the warp
 // calls it: the exact redo at the end is done by the warp together.
-template <int BITS, int DT, int DS>
-__device__ __forceinline__ void values_compute(const Tile<DS>& x, const uint16_t* src, uint8_t* codes, uint16_t* scale,
-                                               uint16_t* zero) {
-    constexpr int NKG = DS / kGroup, qmax = (1 << BITS) - 1;
-    constexpr int WPG = kGroup * BITS / 32;   // code words per channel group
+template <int BITS, int DT, int DS, int G>
+__device__ __forceinline__ void values_compute(const Tile<DS, 32>& x, const uint16_t* src, uint8_t* codes,
+                                               uint16_t* scale, uint16_t* zero) {
+    static_assert(DS % G == 0, "a slice holds whole channel groups");
+    constexpr int NKG = DS / G, qmax = (1 << BITS) - 1;
+    constexpr int WPG = G * BITS / 32;        // code words per channel group
     constexpr int CPW = 32 / BITS;            // codes per word
     float zq[NKG], sq[NKG];   // fp32 zero and scale per group, for the exact redo
     uint32_t tie_groups = 0;  // groups to redo with the exact division
@@ -318,10 +325,10 @@ __device__ __forceinline__ void values_compute(const Tile<DS>& x, const uint16_t
         uint32_t s16[NKG], z16[NKG];
 #pragma unroll
         for (int k = 0; k < NKG; ++k) {
-            const uint32_t* w = x.w + 16 * k;
+            const uint32_t* w = x.w + (G / 2) * k;
             uint32_t mn2 = w[0], mx2 = w[0];
 #pragma unroll
-            for (int c = 1; c < 16; ++c) {
+            for (int c = 1; c < G / 2; ++c) {
                 mn2 = hmin2<DT>(mn2, w[c]);
                 mx2 = hmax2<DT>(mx2, w[c]);
             }
@@ -330,8 +337,8 @@ __device__ __forceinline__ void values_compute(const Tile<DS>& x, const uint16_t
             if (is_zero16(mn) || is_zero16(mx)) {   // sign of the first zero in channel order
                 uint32_t zs = 0;
 #pragma unroll 1
-                for (int c = kGroup - 1; c >= 0; --c) {
-                    const uint32_t hv = src[k * kGroup + c];
+                for (int c = G - 1; c >= 0; --c) {
+                    const uint32_t hv = src[k * G + c];
                     zs = is_zero16(hv) ? hv & 0x8000u : zs;
                 }
                 if (is_zero16(mn)) mn = zs;
@@ -374,8 +381,8 @@ __device__ __forceinline__ void values_compute(const Tile<DS>& x, const uint16_t
         }
     }
     // Exact redo, by the whole warp: one flagged (token, group) at a time, each lane
-    // encoding one of its 32 elements with the IEEE division, the words packed by an OR
-    // reduction. (A lane redoing its own group alone would run 32 divisions while the
+    // encoding G / 32 of its elements with the IEEE division, the words packed by an OR
+    // reduction. (A lane redoing its own group alone would run G divisions while the
     // others wait.) Every lane of the warp runs this loop.
     const int lane = threadIdx.x & 31;
     uint32_t pending = tie_groups;
@@ -393,13 +400,20 @@ __device__ __forceinline__ void values_compute(const Tile<DS>& x, const uint16_t
         zk = __shfl_sync(0xffffffffu, zk, leader);
         sk = __shfl_sync(0xffffffffu, sk, leader);
         const uint16_t* gsrc = reinterpret_cast<const uint16_t*>(
-            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src), leader)) + k * kGroup;
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src), leader)) + k * G;
         uint32_t* gdst = reinterpret_cast<uint32_t*>(
             __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(codes), leader)) + k * WPG;
-        const uint32_t code = encode(widen<DT>(gsrc[lane]), zk, sk, qmax);
+        uint32_t code[G / 32];
+#pragma unroll
+        for (int e = 0; e < G / 32; ++e) code[e] = encode(widen<DT>(gsrc[32 * e + lane]), zk, sk, qmax);
 #pragma unroll
         for (int ww = 0; ww < WPG; ++ww) {
-            const uint32_t part = lane / CPW == ww ? code << ((lane % CPW) * BITS) : 0u;
+            uint32_t part = 0u;
+#pragma unroll
+            for (int e = 0; e < G / 32; ++e) {
+                const int c = 32 * e + lane;
+                part |= c / CPW == ww ? code[e] << ((c % CPW) * BITS) : 0u;
+            }
             const uint32_t word = __reduce_or_sync(0xffffffffu, part);
             if (lane == ww) gdst[ww] = word;
         }
@@ -409,40 +423,40 @@ __device__ __forceinline__ void values_compute(const Tile<DS>& x, const uint16_t
 
 // ---------------------------------------------------------------- standalone codec
 
-// One warp per (stream, 32-token group, channel slice).
-template <int BITS, int DT, int DS>
-__global__ void __launch_bounds__(kThreads, CtasPerSm<DS>::kValue) quant_keys_kernel(CodecArgs a) {
-    const int D = a.D, nsl = D / DS, groups = a.n_tokens / kGroup;
+// One warp per (stream, G-token group, channel slice).
+template <int BITS, int DT, int DS, int G>
+__global__ void __launch_bounds__(kThreads, CtasPerSm<DS, G>::kValue) quant_keys_kernel(CodecArgs a) {
+    const int D = a.D, nsl = D / DS, groups = a.n_tokens / G;
     const int64_t unit = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
     if (unit >= static_cast<int64_t>(a.n_streams) * groups * nsl) return;
     const int sl = static_cast<int>(unit % nsl);
     const int64_t g = unit / nsl;   // stream * groups + group
-    const int64_t tok0 = g * kGroup;
+    const int64_t tok0 = g * G;
     const uint16_t* x = static_cast<const uint16_t*>(a.x) + tok0 * D + sl * DS;
     const int row_bytes = D * BITS / 8;
     auto row = [&](int t) { return x + static_cast<int64_t>(t) * D; };
-    Tile<DS> tile;
-    keys_load<DS>(row, true, D, tile);
-    keys_compute<BITS, DT, DS>(tile, row, a.codes + tok0 * row_bytes + sl * (DS * BITS / 8), row_bytes,
+    Tile<DS, G> tile;
+    keys_load<DS, G>(row, true, D, tile);
+    keys_compute<BITS, DT, DS, G>(tile, row, a.codes + tok0 * row_bytes + sl * (DS * BITS / 8), row_bytes,
                                a.scale + g * D + sl * DS, a.zero + g * D + sl * DS);
 }
 
 // One warp per (stream, run of 32 tokens, channel slice); lane t takes token t.
-template <int BITS, int DT, int DS>
-__global__ void __launch_bounds__(kThreads, CtasPerSm<DS>::kValue) quant_values_kernel(CodecArgs a) {
-    const int D = a.D, nsl = D / DS, runs = (a.n_tokens + kGroup - 1) / kGroup;
+template <int BITS, int DT, int DS, int G>
+__global__ void __launch_bounds__(kThreads, CtasPerSm<DS, 32>::kValue) quant_values_kernel(CodecArgs a) {
+    const int D = a.D, nsl = D / DS, runs = (a.n_tokens + kTile - 1) / kTile;
     const int64_t unit = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
     if (unit >= static_cast<int64_t>(a.n_streams) * runs * nsl) return;
     const int sl = static_cast<int>(unit % nsl);
     const int64_t sr = unit / nsl;
     const int st = static_cast<int>(sr / runs);
-    const int t = static_cast<int>(sr % runs) * kGroup + (threadIdx.x & 31);
+    const int t = static_cast<int>(sr % runs) * kTile + (threadIdx.x & 31);
     const int64_t tok = static_cast<int64_t>(st) * a.n_tokens + t;
     const uint16_t* src = t < a.n_tokens ? static_cast<const uint16_t*>(a.x) + tok * D + sl * DS : nullptr;
-    Tile<DS> tile;
+    Tile<DS, 32> tile;
     values_load<DS>(src, tile);
-    values_compute<BITS, DT, DS>(tile, src, a.codes + tok * (D * BITS / 8) + sl * (DS * BITS / 8),
-                                 a.scale + tok * (D / kGroup) + sl * (DS / kGroup), a.zero + tok * (D / kGroup) + sl * (DS / kGroup));
+    values_compute<BITS, DT, DS, G>(tile, src, a.codes + tok * (D * BITS / 8) + sl * (DS * BITS / 8),
+                                    a.scale + tok * (D / G) + sl * (DS / G), a.zero + tok * (D / G) + sl * (DS / G));
 }
 
 // ---------------------------------------------------------------- append + flush
@@ -458,22 +472,24 @@ __device__ __forceinline__ SeqState seq_state(const AppendArgs& a, int b, int ca
     s.L = a.kv_len[b];
     const int64_t n = a.n_new[b];
     s.L1 = s.L + n;
-    s.np0 = n_packed(s.L, a.R);
-    s.np1 = n_packed(s.L1, a.R);
+    s.np0 = n_packed(s.L, a.R, a.G);
+    s.np1 = n_packed(s.L1, a.R, a.G);
     s.ok = s.L >= 0 && n >= 0 && n <= a.max_new && s.np1 <= cap;
     return s;
 }
 
-// Work units of append_pack_kernel: (group that this append makes leave the residual
-// window, channel slice) of keys (SIDE 0) or values (SIDE 1), one launch per side, so
-// that each launch keeps one code path in the instruction cache (measured: 29 % faster
-// than one launch doing both); grid (warp runs, kv head, sequence), each warp taking
-// every (gridDim.x * kWarps)-th unit of its (head, sequence). Tokens older than kv_len
-// come from the ring, newer ones straight from the caller's buffers.
+// Work units of append_pack_kernel: keys (SIDE 0) take (group that this append makes
+// leave the residual window, channel slice), values (SIDE 1) take (32-token run of those
+// groups, channel slice), one lane per token. One launch per side, so that each launch
+// keeps one code path in the instruction cache (measured: 29 % faster than one launch
+// doing both); grid (warp runs, kv head, sequence), each warp taking every
+// (gridDim.x * kWarps)-th unit of its (head, sequence). Tokens older than kv_len come
+// from the ring, newer ones straight from the caller's buffers.
 constexpr int kUnitsPerWarp = 32;
 
-template <int BITS, int DT, int DS, int SIDE>
-__global__ void __launch_bounds__(kThreads, CtasPerSm<DS>::kValue) append_pack_kernel(AppendArgs a) {
+template <int BITS, int DT, int DS, int G, int SIDE>
+__global__ void __launch_bounds__(kThreads, CtasPerSm<DS, SIDE == 0 ? G : 32>::kValue) append_pack_kernel(AppendArgs a) {
+    constexpr int TOK = SIDE == 0 ? G : kTile;   // tokens of one unit
     const int h = blockIdx.y, b = blockIdx.z, D = a.D, nsl = D / DS;
     const kivi_seq& sq = a.seqs[b];
     const int cap = sq.cap_tokens;
@@ -485,14 +501,14 @@ __global__ void __launch_bounds__(kThreads, CtasPerSm<DS>::kValue) append_pack_k
         }
         return;
     }
-    const int64_t n_units = (st.np1 - st.np0) / kGroup * nsl;   // (group, slice) of this side
-    const int ring = a.R + kGroup;
+    const int64_t n_units = (st.np1 - st.np0) / TOK * nsl;   // (group or run, slice) of this side
+    const int ring = a.R + G;
     const int64_t n = st.L1 - st.L;
     const int row_bytes = D * BITS / 8;
     const int lane = threadIdx.x & 31;
-    // unit -> (group, slice)
+    // unit -> (first token, slice)
     auto slice_of = [&](int64_t unit) { return static_cast<int>(unit % nsl); };
-    auto group_pos = [&](int64_t unit) { return st.np0 + (unit / nsl) * kGroup; };
+    auto unit_pos = [&](int64_t unit) { return st.np0 + (unit / nsl) * TOK; };
     // row of position p0 + t at the slice's first channel
     auto row_at = [&](const void* res, const void* nw, int64_t p0, int sl, int t) -> const uint16_t* {
         const int64_t p = p0 + t;
@@ -503,33 +519,27 @@ __global__ void __launch_bounds__(kThreads, CtasPerSm<DS>::kValue) append_pack_k
         }
         return static_cast<const uint16_t*>(nw) + (static_cast<int64_t>(h) * n + (p - st.L)) * D + sl * DS;
     };
-    auto load = [&](int64_t unit, bool is_v, Tile<DS>& tile) {
-        const int sl = slice_of(unit);
-        const int64_t p0 = group_pos(unit);
-        if (is_v) values_load<DS>(row_at(sq.v_res, a.v_new[b], p0, sl, lane), tile);
-        else keys_load<DS>([&](int t) { return row_at(sq.k_res, a.k_new[b], p0, sl, t); }, p0 >= st.L, D, tile);
-    };
-    auto compute = [&](int64_t unit, bool is_v, const Tile<DS>& tile) {
-        const int sl = slice_of(unit);
-        const int64_t p0 = group_pos(unit), j = p0 / kGroup;
-        const GroupAddr ga = group_addr(sq, a.H, h, j, group_page(sq, j), D, BITS);
-        if (!is_v) {
-            keys_compute<BITS, DT, DS>(tile, [&](int t) { return row_at(sq.k_res, a.k_new[b], p0, sl, t); },
-                                       ga.kc + sl * (DS * BITS / 8), row_bytes, ga.ks + sl * DS, ga.kz + sl * DS);
-        } else {
-            values_compute<BITS, DT, DS>(tile, row_at(sq.v_res, a.v_new[b], p0, sl, lane),
-                                         ga.vc + lane * row_bytes + sl * (DS * BITS / 8),
-                                         ga.vs + lane * (D / kGroup) + sl * (DS / kGroup),
-                                         ga.vz + lane * (D / kGroup) + sl * (DS / kGroup));
-        }
-    };
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarps;
     int64_t unit = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
     if (unit >= n_units) return;
     for (; unit < n_units; unit += stride) {
-        Tile<DS> cur;
-        load(unit, SIDE != 0, cur);
-        compute(unit, SIDE != 0, cur);
+        const int sl = slice_of(unit);
+        const int64_t p0 = unit_pos(unit), j = p0 / G;
+        Tile<DS, TOK> tile;
+        if constexpr (SIDE == 0) {
+            auto row = [&](int t) { return row_at(sq.k_res, a.k_new[b], p0, sl, t); };
+            keys_load<DS, G>(row, p0 >= st.L, D, tile);
+            const GroupAddr ga = group_addr(sq, a.H, h, j, group_page(sq, j), D, BITS, BITS, G);
+            keys_compute<BITS, DT, DS, G>(tile, row, ga.kc + sl * (DS * BITS / 8), row_bytes, ga.ks + sl * DS,
+                                          ga.kz + sl * DS);
+        } else {
+            const int r = static_cast<int>(p0 - j * G) + lane;   // row within the group
+            const uint16_t* src = row_at(sq.v_res, a.v_new[b], p0, sl, lane);
+            values_load<DS>(src, tile);
+            const GroupAddr ga = group_addr(sq, a.H, h, j, group_page(sq, j), D, BITS, BITS, G);
+            values_compute<BITS, DT, DS, G>(tile, src, ga.vc + r * row_bytes + sl * (DS * BITS / 8),
+                                            ga.vs + r * (D / G) + sl * (DS / G), ga.vz + r * (D / G) + sl * (DS / G));
+        }
     }
 }
 
@@ -542,7 +552,7 @@ __global__ void __launch_bounds__(256) append_ring_kernel(AppendArgs a) {
     const kivi_seq& sq = a.seqs[b];
     const SeqState st = seq_state(a, b, sq.cap_tokens);
     if (!st.ok) return;
-    const int ring = a.R + kGroup;
+    const int ring = a.R + a.G;
     const int64_t n = st.L1 - st.L;
     const int64_t first = st.L > st.np1 ? st.L : st.np1;  // first position that stays in the ring
     const int64_t count = st.L1 - first;
@@ -568,19 +578,30 @@ __global__ void __launch_bounds__(256) append_ring_kernel(AppendArgs a) {
     if (threadIdx.x == 0) a.kv_len[b] = static_cast<int32_t>(st.L1);
 }
 
-// Calls f.template operator()<BITS, DT, DS>() for the runtime bit width, input type and
-// slice width ds (32, 64 or 128).
+// Calls f.template operator()<BITS, DT, DS, G>() for the runtime bit width, input type,
+// slice width ds (32, 64 or 128) and group size g (32 or 64).
 template <typename F>
-cudaError_t dispatch(int bits, int dtype, int ds, F f) {
-#define KIVI_DS(B, T)                                                                             \
-    return ds == 128 ? f.template operator()<B, T, 128>()                                        \
-         : ds == 64  ? f.template operator()<B, T, 64>() : f.template operator()<B, T, 32>();
-    if (bits == 2 && dtype == KIVI_F16) { KIVI_DS(2, KIVI_F16) }
-    if (bits == 2) { KIVI_DS(2, KIVI_BF16) }
-    if (dtype == KIVI_F16) { KIVI_DS(4, KIVI_F16) }
-    KIVI_DS(4, KIVI_BF16)
+cudaError_t dispatch(int bits, int dtype, int ds, int g, F f) {
+#define KIVI_DS(B, T, G)                                                                             \
+    return ds == 128 ? f.template operator()<B, T, 128, G>()                                        \
+         : ds == 64  ? f.template operator()<B, T, 64, G>() : f.template operator()<B, T, 32, G>();
+#define KIVI_G(B, T) \
+    if (g == 64) { KIVI_DS(B, T, 64) } \
+    KIVI_DS(B, T, 32)
+    if (bits == 2 && dtype == KIVI_F16) { KIVI_G(2, KIVI_F16) }
+    if (bits == 2) { KIVI_G(2, KIVI_BF16) }
+    if (dtype == KIVI_F16) { KIVI_G(4, KIVI_F16) }
+    KIVI_G(4, KIVI_BF16)
+#undef KIVI_G
 #undef KIVI_DS
 }
+
+// Slice widths instantiated: keys (G = 32) 32, 64, 128; keys (G = 64) and values 32, 64
+// where they hold whole channel groups.
+template <int DS, int G>
+constexpr bool key_slice_ok() { return G == 32 || DS == 64; }
+template <int DS, int G>
+constexpr bool value_slice_ok() { return DS != 128 && DS % G == 0; }
 
 int64_t blocks_for(int64_t warps) { return (warps + kWarps - 1) / kWarps; }
 
@@ -588,10 +609,12 @@ int64_t blocks_for(int64_t warps) { return (warps + kWarps - 1) / kWarps; }
 
 cudaError_t launch_quant_keys(const CodecArgs& a, cudaStream_t stream) {
     if (a.n_streams == 0 || a.n_tokens == 0) return cudaSuccess;
-    const int ds = key_slice_width(a.D);
-    const int64_t units = static_cast<int64_t>(a.n_streams) * (a.n_tokens / kGroup) * (a.D / ds);
-    return dispatch(a.bits, a.dtype, ds, [&]<int B, int T, int DS>() {
-        quant_keys_kernel<B, T, DS><<<static_cast<unsigned>(blocks_for(units)), kThreads, 0, stream>>>(a);
+    const int ds = key_slice_width(a.D, a.G);
+    const int64_t units = static_cast<int64_t>(a.n_streams) * (a.n_tokens / a.G) * (a.D / ds);
+    return dispatch(a.bits, a.dtype, ds, a.G, [&]<int B, int T, int DS, int G>() {
+        if constexpr (key_slice_ok<DS, G>()) {
+            quant_keys_kernel<B, T, DS, G><<<static_cast<unsigned>(blocks_for(units)), kThreads, 0, stream>>>(a);
+        }
         return cudaGetLastError();
     });
 }
@@ -599,11 +622,11 @@ cudaError_t launch_quant_keys(const CodecArgs& a, cudaStream_t stream) {
 cudaError_t launch_quant_values(const CodecArgs& a, cudaStream_t stream) {
     if (a.n_streams == 0 || a.n_tokens == 0) return cudaSuccess;
     const int ds = slice_width(a.D);
-    const int64_t runs = (a.n_tokens + kGroup - 1) / kGroup;
+    const int64_t runs = (a.n_tokens + kTile - 1) / kTile;
     const int64_t units = static_cast<int64_t>(a.n_streams) * runs * (a.D / ds);
-    return dispatch(a.bits, a.dtype, ds, [&]<int B, int T, int DS>() {
-        if constexpr (DS != 128) {
-            quant_values_kernel<B, T, DS><<<static_cast<unsigned>(blocks_for(units)), kThreads, 0, stream>>>(a);
+    return dispatch(a.bits, a.dtype, ds, a.G, [&]<int B, int T, int DS, int G>() {
+        if constexpr (value_slice_ok<DS, G>()) {
+            quant_values_kernel<B, T, DS, G><<<static_cast<unsigned>(blocks_for(units)), kThreads, 0, stream>>>(a);
         }
         return cudaGetLastError();
     });
@@ -611,22 +634,28 @@ cudaError_t launch_quant_values(const CodecArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_append_flush(const AppendArgs& a, cudaStream_t stream) {
     if (a.nseq == 0) return cudaSuccess;
-    const int max_groups = (a.max_new + kGroup - 1) / kGroup;
+    const int max_groups = (a.max_new + a.G - 1) / a.G;
     if (max_groups > 0) {
         // keys and values in two launches, so that each keeps one code path in the
-        // instruction cache; one warp per (group, slice), kUnitsPerWarp of them per warp
-        auto grid_for = [&](int ds) {
-            const int64_t units = static_cast<int64_t>(max_groups) * (a.D / ds);
-            return dim3(static_cast<unsigned>(blocks_for((units + kUnitsPerWarp - 1) / kUnitsPerWarp)), a.H, a.nseq);
+        // instruction cache; one warp per unit, kUnitsPerWarp of them per warp
+        auto grid_for = [&](int64_t per_seq_units) {
+            return dim3(static_cast<unsigned>(blocks_for((per_seq_units + kUnitsPerWarp - 1) / kUnitsPerWarp)), a.H,
+                        a.nseq);
         };
-        const int dk = key_slice_width(a.D), dv = slice_width(a.D);
-        cudaError_t e = dispatch(a.bits, a.dtype, dk, [&]<int B, int T, int DS>() {
-            append_pack_kernel<B, T, DS, 0><<<grid_for(DS), kThreads, 0, stream>>>(a);
+        const int dk = key_slice_width(a.D, a.G), dv = slice_width(a.D);
+        cudaError_t e = dispatch(a.kb, a.dtype, dk, a.G, [&]<int B, int T, int DS, int G>() {
+            if constexpr (key_slice_ok<DS, G>()) {
+                append_pack_kernel<B, T, DS, G, 0><<<grid_for(static_cast<int64_t>(max_groups) * (a.D / DS)), kThreads, 0,
+                                                     stream>>>(a);
+            }
             return cudaGetLastError();
         });
         if (e != cudaSuccess) return e;
-        e = dispatch(a.bits, a.dtype, dv, [&]<int B, int T, int DS>() {
-            if constexpr (DS != 128) append_pack_kernel<B, T, DS, 1><<<grid_for(DS), kThreads, 0, stream>>>(a);
+        e = dispatch(a.vb, a.dtype, dv, a.G, [&]<int B, int T, int DS, int G>() {
+            if constexpr (value_slice_ok<DS, G>()) {
+                append_pack_kernel<B, T, DS, G, 1><<<grid_for(static_cast<int64_t>(max_groups) * (G / kTile) * (a.D / DS)),
+                                                     kThreads, 0, stream>>>(a);
+            }
             return cudaGetLastError();
         });
         if (e != cudaSuccess) return e;

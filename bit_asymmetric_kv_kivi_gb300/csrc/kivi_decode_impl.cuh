@@ -1,0 +1,1189 @@
+// Split-K decode attention over the KIVI packed cache (sm_103a).
+//
+// One query token per sequence attends to every cached token: packed tokens
+// are dequantized on the fly as c*s + z (keys: scale/zero per (group of G
+// tokens, channel); values: per (token, group of G channels)), residual
+// tokens are read as stored. "KIVI: Asymmetric 2-Bit KV Cache Quantization
+// Guide", sections "Step 2" (dequantize during attention) and "Production
+// Serving and vLLM Deployment Trade-offs in 2026" (on-the-fly dequantization
+// in SRAM); "KIVI: A Tuning-Free Asymmetric 2bit Quantization for KV Cache",
+// abstract (decode is bound by loading the cache).
+//
+// Two kernels share the split bookkeeping:
+//
+//  * decode_mma_kernel (Hq/Hkv = 1, 2, 4): the dot products run on the tensor
+//    cores (mma.sync m16n8k16, f16 operands, fp32 accumulation). A CTA owns a
+//    range of 32-token tiles of the packed tokens of one (sequence, kv head)
+//    (a key group of G = 64 is two tiles), or residual tokens of it. Each of its four warps
+//    streams its groups through a private cp.async ring of shared-memory
+//    stages and keeps its own online-softmax state.
+//      - Scores: S[token][head] = sum_d c[token][d] * Q[d][head] + bias[head],
+//        Q = q * s_k (softmax scale and log2(e) folded into q). Codes are the
+//        A operand, unpacked to exact f16 integers (one lop3 + one fma per
+//        pair). Q is the B operand as an f16 hi + lo pair (two columns per
+//        head), built with an exact-error product in f16, so the sum carries
+//        about 22 bits; bias = sum_d q z_k is one more small MMA.
+//      - Values: O[d][head] += sum_t c[t][d] * P'[t][head] with
+//        P' = p * s_v[t][group(d)] (hi + lo again), channels as M; the
+//        sum_t p z_v term is a small MMA of its own.
+//    q is rescaled by a power of two so that max|q| lies in (1/2, 1]; with
+//    |x| <= 65504 no f16 operand can overflow.
+//  * decode_split_kernel (any Hq/Hkv, used for 8): CUDA-core FMAs, lane = token.
+//
+// Every split writes (m, l, acc[128]) for its query heads to the workspace;
+// the last CTA of a (sequence, kv head) to finish (an atomic ticket, no
+// waiting) merges the splits with the log-sum-exp rescaling and writes the
+// fp32 output.
+//
+// This header holds the kernels as templates over the key and value code widths
+// (KB, VB), the input type, the query group and G; each translation unit that
+// includes it instantiates one (KB, VB) pair (launch_decode_kv), so that the
+// instantiations compile in parallel.
+#pragma once
+#include <math_constants.h>
+
+#include "kivi_internal.cuh"
+
+namespace kivi {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kD = 128;          // head_dim handled by these kernels
+constexpr int kCpl = kD / 32;    // channels per lane in the lane-layout value accumulator
+constexpr int kStages = 4;       // cp.async ring depth per warp (decode_mma_kernel)
+constexpr int kPtLd = 40;        // row stride (floats) of the per-warp probability transpose
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// f16x2 from two floats (round to nearest even): `lo` in bits 0-15, `hi` in 16-31.
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+__device__ __forceinline__ float h2_lo(uint32_t v) { return __half2float(__ushort_as_half(static_cast<uint16_t>(v))); }
+__device__ __forceinline__ float h2_hi(uint32_t v) { return __half2float(__ushort_as_half(static_cast<uint16_t>(v >> 16))); }
+
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Codes at bits I*BITS and 16 + I*BITS of w as an exact f16 pair (low, high half).
+// The field is OR-ed into the mantissa of 1024.0 and the 1024 removed by one fma
+// (the field's position scaled away by a power of two); fields that reach past the
+// 10 mantissa bits are taken from ws = w >> (DIRECT * BITS).
+template <int BITS, int I>
+__device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t ws) {
+    constexpr int kDirect = (10 - BITS) / BITS + 1;               // fields wholly inside bits 0..9
+    constexpr int kPos = I < kDirect ? I * BITS : (I - kDirect) * BITS;
+    constexpr uint32_t kMask = ((((1u << BITS) - 1u) << kPos) * 0x00010001u);
+    constexpr uint32_t kScale = static_cast<uint32_t>((15 - kPos) << 10) * 0x00010001u;          // 2^-pos
+    constexpr uint32_t kBias = static_cast<uint32_t>(0x8000 | ((25 - kPos) << 10)) * 0x00010001u;  // -2^(10-pos)
+    const uint32_t src = I < kDirect ? w : ws;
+    uint32_t h;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(h) : "r"(src), "r"(kMask), "r"(0x64006400u));  // (src & mask) | magic
+    return hfma2(h, kScale, kBias);
+}
+
+// code_pair for a slot index known only after unrolling (folds to one case).
+template <int BITS>
+__device__ __forceinline__ uint32_t code_slot(uint32_t w, uint32_t ws, int s) {
+    constexpr int kN = 16 / BITS;
+    switch (s % kN) {
+        case 0: return code_pair<BITS, 0>(w, ws);
+        case 1: return code_pair<BITS, 1 % kN>(w, ws);
+        case 2: return code_pair<BITS, 2 % kN>(w, ws);
+        case 3: return code_pair<BITS, 3 % kN>(w, ws);
+        case 4: return code_pair<BITS, 4 % kN>(w, ws);
+        case 5: return code_pair<BITS, 5 % kN>(w, ws);
+        case 6: return code_pair<BITS, 6 % kN>(w, ws);
+        default: return code_pair<BITS, 7 % kN>(w, ws);
+    }
+}
+
+template <int BITS>
+struct CodeShift {
+    static constexpr int kValue = ((10 - BITS) / BITS + 1) * BITS;   // 10 (2-bit), 8 (4-bit)
+};
+
+// ---------------------------------------------------------------- lane-layout pieces
+
+// One 32-token tile of residual tokens [ts, min(ts+32, t1)) for one warp, lane = token:
+// scores against the widened stored keys, online-softmax update and value accumulation
+// into the lane-layout state (lane owns channels [4 lane, 4 lane + 4)). Every global
+// load of the tile is issued before its first use (the key row, then the lane's value
+// slices of all 32 tokens), so a tile waits for memory twice, not once per token.
+template <int DT, int GQ>
+__device__ __forceinline__ void residual_tile(const uint16_t* kres, const uint16_t* vres, int ring, int64_t ts,
+                                              int64_t t1, const float* qs, int lane, float (&m)[GQ], float (&l)[GQ],
+                                              float (&acc)[GQ][kCpl]) {
+    const int64_t p = ts + lane;
+    const bool valid = p < t1;
+    const int ntok = static_cast<int>(t1 - ts < 32 ? t1 - ts : 32);
+    const int slot0 = static_cast<int>(ts % ring);
+    float sc[GQ];
+#pragma unroll
+    for (int hh = 0; hh < GQ; ++hh) sc[hh] = 0.0f;
+    {
+        uint4 kr[kD / 8];
+        const int slot = slot0 + lane >= ring ? slot0 + lane - ring : slot0 + lane;
+        const uint4* krow = reinterpret_cast<const uint4*>(kres + static_cast<int64_t>(slot) * kD);
+#pragma unroll
+        for (int w = 0; w < kD / 8; ++w) kr[w] = valid ? __ldg(krow + w) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int w = 0; w < kD / 8; ++w) {
+            const uint32_t words[4] = {kr[w].x, kr[w].y, kr[w].z, kr[w].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float k0 = widen<DT>(static_cast<uint16_t>(words[e] & 0xffffu));
+                const float k1 = widen<DT>(static_cast<uint16_t>(words[e] >> 16));
+                const int d = 8 * w + 2 * e;
+#pragma unroll
+                for (int hh = 0; hh < GQ; ++hh) sc[hh] = fmaf(qs[hh * kD + d + 1], k1, fmaf(qs[hh * kD + d], k0, sc[hh]));
+            }
+        }
+    }
+    uint2 vr[32];
+#pragma unroll
+    for (int tau = 0; tau < 32; ++tau) {
+        const int slot = slot0 + tau >= ring ? slot0 + tau - ring : slot0 + tau;
+        vr[tau] = tau < ntok ? __ldg(reinterpret_cast<const uint2*>(vres + static_cast<int64_t>(slot) * kD + lane * kCpl))
+                             : make_uint2(0, 0);
+    }
+    float pr[GQ];
+#pragma unroll
+    for (int hh = 0; hh < GQ; ++hh) {
+        const float tmax = warp_max(valid ? sc[hh] : -CUDART_INF_F);
+        const float mnew = fmaxf(m[hh], tmax);
+        const float alpha = exp2f(m[hh] - mnew);
+        pr[hh] = valid ? exp2f(sc[hh] - mnew) : 0.0f;
+        l[hh] = l[hh] * alpha + warp_sum(pr[hh]);
+#pragma unroll
+        for (int c = 0; c < kCpl; ++c) acc[hh][c] *= alpha;
+        m[hh] = mnew;
+    }
+#pragma unroll
+    for (int tau = 0; tau < 32; ++tau) {
+        const float v[kCpl] = {widen<DT>(static_cast<uint16_t>(vr[tau].x & 0xffffu)),
+                               widen<DT>(static_cast<uint16_t>(vr[tau].x >> 16)),
+                               widen<DT>(static_cast<uint16_t>(vr[tau].y & 0xffffu)),
+                               widen<DT>(static_cast<uint16_t>(vr[tau].y >> 16))};
+#pragma unroll
+        for (int hh = 0; hh < GQ; ++hh) {
+            const float pt = __shfl_sync(kFull, pr[hh], tau);   // 0 for tokens past t1
+#pragma unroll
+            for (int c = 0; c < kCpl; ++c) acc[hh][c] = fmaf(pt, v[c], acc[hh][c]);
+        }
+    }
+}
+
+// Lane-layout warp state into the CTA merge arrays.
+template <int GQ>
+__device__ __forceinline__ void store_lane_state(int warp, int lane, const float (&m)[GQ], const float (&l)[GQ],
+                                                 const float (&acc)[GQ][kCpl], float* red_m, float* red_l,
+                                                 float* red_acc) {
+#pragma unroll
+    for (int hh = 0; hh < GQ; ++hh) {
+        if (lane == 0) {
+            red_m[warp * GQ + hh] = m[hh];
+            red_l[warp * GQ + hh] = l[hh];
+        }
+#pragma unroll
+        for (int c = 0; c < kCpl; ++c) red_acc[(warp * GQ + hh) * kD + lane * kCpl + c] = acc[hh][c];
+    }
+}
+
+// Merges the four warps' states of this split (red_* in shared memory, filled and
+// synchronized by the caller), then either writes the output (single split) or
+// the split's partial record; the last CTA of (b, h) to arrive merges all splits.
+template <int GQ>
+__device__ __forceinline__ void finish_split(const DecodeArgs& a, int b, int h, int split, int nsplit,
+                                             float* out_bh, const float* red_m, const float* red_l,
+                                             const float* red_acc, int* s_last) {
+    const int tid = threadIdx.x;
+    const int64_t rec_stride = kD + 4;
+    float* part_bh =
+        a.partials + (static_cast<int64_t>(b) * a.Hq + static_cast<int64_t>(h) * GQ) * a.max_splits * rec_stride;
+    for (int i = tid; i < GQ * kD; i += kThreads) {
+        const int hh = i / kD, d = i - hh * kD;
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w * GQ + hh]);
+        float den = 0.0f, num = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float f = exp2f(red_m[w * GQ + hh] - M);
+            den = fmaf(red_l[w * GQ + hh], f, den);
+            num = fmaf(red_acc[(w * GQ + hh) * kD + d], f, num);
+        }
+        if (nsplit == 1) {
+            out_bh[i] = num / den;
+        } else {
+            float* rec = part_bh + (static_cast<int64_t>(hh) * a.max_splits + split) * rec_stride;
+            rec[d] = num;
+            if (d == 0) {
+                rec[kD] = M;
+                rec[kD + 1] = den;
+            }
+        }
+    }
+    if (nsplit == 1) return;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const int ticket = atomicAdd(&a.counters[static_cast<int64_t>(b) * a.H + h], 1);
+        *s_last = ticket == nsplit - 1;
+    }
+    __syncthreads();
+    if (!*s_last) return;
+    __threadfence();
+    for (int i = tid; i < GQ * kD; i += kThreads) {
+        const int hh = i / kD, d = i - hh * kD;
+        const float* rec = part_bh + static_cast<int64_t>(hh) * a.max_splits * rec_stride;
+        float M = -CUDART_INF_F, den = 0.0f, num = 0.0f;
+        for (int s = 0; s < nsplit; ++s) {
+            const float ms = __ldcg(rec + s * rec_stride + kD);
+            const float Mn = fmaxf(M, ms);
+            const float fo = exp2f(M - Mn), fs = exp2f(ms - Mn);
+            den = den * fo + __ldcg(rec + s * rec_stride + kD + 1) * fs;
+            num = num * fo + __ldcg(rec + s * rec_stride + d) * fs;
+            M = Mn;
+        }
+        out_bh[i] = num / den;
+    }
+    if (tid == 0) a.counters[static_cast<int64_t>(b) * a.H + h] = 0;
+}
+
+// ---------------------------------------------------------------- persistent schedule
+
+// decode_mma_kernel runs one CTA per resident slot. The work of all (sequence, kv head)
+// streams, sequence-major, is a row of units: a stream's packed tokens in 32-token tiles
+// (one unit each) then its residual tokens in 32-token tiles (kResidualWeight units each,
+// about their cost relative to a packed tile). CTA c takes units [c U / Ceff, (c+1) U / Ceff), which
+// may span streams; each stream is charged kStreamOverhead units ahead of its packed tiles
+// for its setup and merge, which no segment holds. The part of a stream's packed tiles (or
+// of its residual tiles) that one CTA holds is a segment; its partial record sits at index
+// 2 s + part + c (s the stream, part 0 for packed and 1 for residual tiles), unique because each step to the next segment raises the
+// stream, the part or the CTA, and below 2 S + Ceff. The last CTA to finish a segment of
+// a stream (an atomic ticket, no waiting) merges the stream's records.
+constexpr int kResidualWeight = 4;
+constexpr int kStreamOverhead = 32;      // units charged per stream for its setup and merge
+constexpr int kMinUnitsPerCta = 8;
+constexpr int kMaxCtas = kDecodeMaxCtas;
+
+struct SeqWork {
+    int64_t L, np, ng, rt, u;   // tokens, packed tokens, packed tiles, residual tiles, units
+    bool bad;
+};
+
+template <int G>
+__device__ __forceinline__ SeqWork seq_work(const DecodeArgs& a, int b) {
+    SeqWork w;
+    w.L = a.kv_len[b];
+    w.bad = w.L < 0 || w.L > a.max_kv_len || n_packed(w.L, a.R, G) > a.seqs[b].cap_tokens;
+    w.np = w.ng = w.rt = w.u = 0;
+    if (w.bad || w.L == 0) return w;
+    w.np = n_packed(w.L, a.R, G);
+    w.ng = w.np / kTile;
+    w.rt = (w.L - w.np + kTile - 1) / kTile;
+    w.u = kStreamOverhead + w.ng + kResidualWeight * w.rt;
+    return w;
+}
+
+// The CTA whose range holds unit x: the largest c with c U / Ceff <= x.
+__device__ __forceinline__ int64_t owner(int64_t x, int64_t U, int64_t Ceff) { return ((x + 1) * Ceff - 1) / U; }
+
+// The segments of one stream: CTAs [cg0, cg1] hold its packed tiles, [cr0, cr1] its residual tiles
+// (empty ranges when first > last).
+struct StreamSegs {
+    int64_t s, cg0, cg1, cr0, cr1;
+    int nseg;
+};
+
+// Merges the four warps' states of one segment (red_* in shared memory, filled and
+// synchronized by the caller), then writes the output (the stream's only segment) or
+// the segment's partial record; the last CTA of the stream to arrive merges them all.
+// An empty state (m = -inf, l = 0) contributes nothing. scratch: shared memory for
+// GQ * nseg floats from scratch[0] and GQ before it, free once red_* have been read.
+template <int GQ>
+__device__ __forceinline__ void finish_segment(const DecodeArgs& a, const StreamSegs& ss, int64_t seg, float* out_s,
+                                               const float* red_m, const float* red_l, const float* red_acc,
+                                               int* s_last, float* scratch) {
+    const int tid = threadIdx.x;
+    constexpr int64_t rec = kD + 4;
+    for (int i = tid; i < GQ * kD; i += kThreads) {
+        const int hh = i / kD, d = i - hh * kD;
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w * GQ + hh]);
+        float den = 0.0f, num = 0.0f;
+        if (M != -CUDART_INF_F) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float f = exp2f(red_m[w * GQ + hh] - M);
+                den = fmaf(red_l[w * GQ + hh], f, den);
+                num = fmaf(red_acc[(w * GQ + hh) * kD + d], f, num);
+            }
+        }
+        if (ss.nseg == 1) {
+            out_s[i] = num / den;
+        } else {
+            float* r = a.partials + (seg * GQ + hh) * rec;
+            r[d] = num;
+            if (d == 0) {
+                r[kD] = M;
+                r[kD + 1] = den;
+            }
+        }
+    }
+    if (ss.nseg == 1) return;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) *s_last = atomicAdd(&a.counters[ss.s], 1) == ss.nseg - 1;
+    __syncthreads();
+    if (!*s_last) return;
+    __threadfence();
+    // the stream's records: k-th segment -> record index; one warp per head finds the
+    // running max and the weights exp2(m - M) of all records at once (loads in parallel),
+    // then every output sums its records with independent loads
+    const int ng_cnt = static_cast<int>(ss.cg1 - ss.cg0 + 1);
+    auto rec_at = [&](int k, int hh) {
+        const int64_t idx = k < ng_cnt ? 2 * ss.s + ss.cg0 + k : 2 * ss.s + 1 + ss.cr0 + (k - ng_cnt);
+        return a.partials + (idx * GQ + hh) * rec;
+    };
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int hh = warp; hh < GQ; hh += kWarps) {
+        float M = -CUDART_INF_F;
+        for (int k = lane; k < ss.nseg; k += 32) M = fmaxf(M, __ldcg(rec_at(k, hh) + kD));
+        M = warp_max(M);
+        float den = 0.0f;
+        for (int k = lane; k < ss.nseg; k += 32) {
+            const float* r = rec_at(k, hh);
+            const float ms = __ldcg(r + kD);
+            const float f = ms == -CUDART_INF_F ? 0.0f : exp2f(ms - M);
+            scratch[k * GQ + hh] = f;
+            den = fmaf(__ldcg(r + kD + 1), f, den);
+        }
+        den = warp_sum(den);
+        if (lane == 0) scratch[-GQ + hh] = den;
+    }
+    __syncthreads();
+    for (int i = tid; i < GQ * kD; i += kThreads) {
+        const int hh = i / kD, d = i - hh * kD;
+        float num = 0.0f;
+#pragma unroll 8
+        for (int k = 0; k < ss.nseg; ++k) num = fmaf(scratch[k * GQ + hh], __ldcg(rec_at(k, hh) + d), num);
+        out_s[i] = num / scratch[-GQ + hh];
+    }
+    if (tid == 0) a.counters[ss.s] = 0;
+}
+
+// ---------------------------------------------------------------- CUDA-core kernel
+
+// Splits over [0, L) in chunks of a.chunk tokens; four warps take 32-token tiles
+// round-robin, lane = token. Key side per packed tile: q'[hq][d] = q[hq][d] * s_k[d]
+// and bias[hq] = sum_d q[hq][d] * z_k[d], so a token's score is bias + sum_d q'[d] c[d].
+template <int KB, int VB, int DT, int GQ, int G>
+__global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
+    constexpr int kq = (1 << KB) - 1, vq = (1 << VB) - 1;
+    constexpr int kKWords = kD * KB / 32;         // 32-bit words per packed key row
+    constexpr int kVWords = kD * VB / 32;         // and value row
+    constexpr int kPerWord = 32 / KB;             // key codes per word
+    constexpr int kNg = kD / G;                   // value channel groups per token
+
+    __shared__ float qs[GQ * kD];                                 // q * scale * log2(e)
+    __shared__ float qk[kWarps][GQ][kD];                          // per warp: q' of the current key group
+    __shared__ uint32_t vcode[kWarps][kTile][kVWords];            // per warp: value code rows of the tile
+    __shared__ float vsc[kWarps][kTile][kNg], vzr[kWarps][kTile][kNg];
+    __shared__ float red_m[kWarps * GQ], red_l[kWarps * GQ];
+    __shared__ int s_last;
+
+    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int Hq = a.Hq, ring = a.R + G;
+    const kivi_seq& sq = a.seqs[b];
+    const int cap = sq.cap_tokens;
+    const int64_t L = a.kv_len[b];
+    float* out_bh = a.out + (static_cast<int64_t>(b) * Hq + static_cast<int64_t>(h) * GQ) * kD;
+
+    const bool bad = L < 0 || L > a.max_kv_len || n_packed(L, a.R, G) > cap;
+    if (bad || L == 0) {
+        if (split == 0) {
+            for (int i = tid; i < GQ * kD; i += kThreads) out_bh[i] = bad ? CUDART_NAN_F : 0.0f;
+            if (bad && h == 0 && tid == 0) set_status(a.status, KIVI_ERR_LENGTH);
+        }
+        return;
+    }
+    const int nsplit = static_cast<int>((L + a.chunk - 1) / a.chunk);
+    if (split >= nsplit) return;
+    const int64_t t0 = static_cast<int64_t>(split) * a.chunk;
+    const int64_t t1 = min(t0 + a.chunk, L);
+    const int64_t np = n_packed(L, a.R, G);
+
+    const uint16_t* q = static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(b) * Hq + h * GQ) * kD;
+    for (int i = tid; i < GQ * kD; i += kThreads) qs[i] = widen<DT>(q[i]) * a.scale_log2;
+    __syncthreads();
+
+    float m[GQ], l[GQ], acc[GQ][kCpl];
+#pragma unroll
+    for (int hh = 0; hh < GQ; ++hh) {
+        m[hh] = -CUDART_INF_F;
+        l[hh] = 0.0f;
+#pragma unroll
+        for (int c = 0; c < kCpl; ++c) acc[hh][c] = 0.0f;
+    }
+
+    const uint16_t* kres = static_cast<const uint16_t*>(sq.k_res) + static_cast<int64_t>(h) * ring * kD;
+    const uint16_t* vres = static_cast<const uint16_t*>(sq.v_res) + static_cast<int64_t>(h) * ring * kD;
+
+    for (int64_t ts = t0 + 32 * warp; ts < t1; ts += 32 * kWarps) {
+        if (ts >= np) {   // residual tile (np and ts are multiples of 32)
+            residual_tile<DT, GQ>(kres, vres, ring, ts, t1, qs, lane, m, l, acc);
+            __syncwarp();
+            continue;
+        }
+        const GroupAddr ga = tile_addr(sq, a.H, h, ts / kTile, kD, KB, VB, G);   // packed tiles hold no residual
+        const uint16_t* ksc = ga.ks;
+        const uint16_t* kzr = ga.kz;
+        float sc[GQ], bias[GQ];
+#pragma unroll
+        for (int hh = 0; hh < GQ; ++hh) bias[hh] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kD / 32; ++i) {
+            const int d = lane + 32 * i;
+            const float s = f16_bits_to_float(ksc[d]), z = f16_bits_to_float(kzr[d]);
+#pragma unroll
+            for (int hh = 0; hh < GQ; ++hh) {
+                qk[warp][hh][d] = qs[hh * kD + d] * s;
+                bias[hh] = fmaf(qs[hh * kD + d], z, bias[hh]);
+            }
+        }
+#pragma unroll
+        for (int hh = 0; hh < GQ; ++hh) sc[hh] = warp_sum(bias[hh]);
+        const uint4* vrow = reinterpret_cast<const uint4*>(ga.vc + lane * (kD * VB / 8));
+#pragma unroll
+        for (int w = 0; w < kVWords / 4; ++w)
+            *reinterpret_cast<uint4*>(&vcode[warp][lane][4 * w]) = __ldg(vrow + w);
+#pragma unroll
+        for (int k = 0; k < kNg; ++k) {
+            vsc[warp][lane][k] = f16_bits_to_float(ga.vs[lane * kNg + k]);
+            vzr[warp][lane][k] = f16_bits_to_float(ga.vz[lane * kNg + k]);
+        }
+        __syncwarp();
+        const uint4* krow = reinterpret_cast<const uint4*>(ga.kc + lane * (kD * KB / 8));
+#pragma unroll
+        for (int w4 = 0; w4 < kKWords / 4; ++w4) {
+            const uint4 v4 = __ldg(krow + w4);
+            const uint32_t words[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+#pragma unroll
+                for (int i = 0; i < kPerWord; ++i) {
+                    const int d = (4 * w4 + e) * kPerWord + i;
+                    const float c = static_cast<float>((words[e] >> (i * KB)) & kq);
+#pragma unroll
+                    for (int hh = 0; hh < GQ; ++hh) sc[hh] = fmaf(qk[warp][hh][d], c, sc[hh]);
+                }
+            }
+        }
+        float pr[GQ];
+#pragma unroll
+        for (int hh = 0; hh < GQ; ++hh) {
+            const float tmax = warp_max(sc[hh]);
+            const float mnew = fmaxf(m[hh], tmax);
+            const float alpha = exp2f(m[hh] - mnew);
+            pr[hh] = exp2f(sc[hh] - mnew);
+            l[hh] = l[hh] * alpha + warp_sum(pr[hh]);
+#pragma unroll
+            for (int c = 0; c < kCpl; ++c) acc[hh][c] *= alpha;
+            m[hh] = mnew;
+        }
+        // lane owns channels [4 lane, 4 lane + 4): value channel group lane / 8
+        const int kg = (lane * kCpl) / G;
+        for (int tau = 0; tau < 32; ++tau) {
+            const uint32_t bitsv = (vcode[warp][tau][(lane * kCpl * VB) / 32] >> ((lane * kCpl * VB) % 32));
+            const float s = vsc[warp][tau][kg], z = vzr[warp][tau][kg];
+            float v[kCpl];
+#pragma unroll
+            for (int c = 0; c < kCpl; ++c) v[c] = fmaf(static_cast<float>((bitsv >> (c * VB)) & vq), s, z);
+#pragma unroll
+            for (int hh = 0; hh < GQ; ++hh) {
+                const float pt = __shfl_sync(kFull, pr[hh], tau);
+#pragma unroll
+                for (int c = 0; c < kCpl; ++c) acc[hh][c] = fmaf(pt, v[c], acc[hh][c]);
+            }
+        }
+        __syncwarp();
+    }
+
+    __syncthreads();
+    float* red_acc = &qk[0][0][0];   // [kWarps][GQ][kD]
+    store_lane_state<GQ>(warp, lane, m, l, acc, red_m, red_l, red_acc);
+    __syncthreads();
+    finish_split<GQ>(a, b, h, split, nsplit, out_bh, red_m, red_l, red_acc, &s_last);
+}
+
+// ---------------------------------------------------------------- tensor-core kernel
+
+template <int KB, int VB>
+struct MmaLayout {
+    static constexpr int kKRowBytes = kD * KB / 8;                       // packed key row: 32 or 64 bytes
+    static constexpr int kVRowBytes = kD * VB / 8;                       // and value row
+    // kc, vc, ks, kz, vs, vz; each 64-byte channel span of ks and kz is padded to 80 bytes so
+    // that the four spans read together fall on distinct shared-memory banks; vs and vz take
+    // 256 bytes each (128 used when G = 64)
+    static constexpr int kMetaPad = 320;
+    static constexpr int kCodeBytes = kTile * (kKRowBytes + kVRowBytes);
+    static constexpr int kStage = kCodeBytes + 2 * kMetaPad + 2 * 256;
+    static constexpr int kNslot = 16 / KB;                               // key code pairs per 32-bit word
+    static constexpr int kStageBytes = kWarps * kStages * kStage;
+    static constexpr int kSmemBytes(int gq) {
+        return kStageBytes + (gq * kD + kWarps * 4 * kPtLd + 2 * kWarps * gq + 8) * 4;
+    }
+};
+
+// Thread (gid = lane / 4, t = lane % 4) follows the mma.sync
+// m16n8k16 fragment layout. Logical k index 2t+8e+{0,1} of key k-step ks maps to
+// the code pair of slot s = 2 ks + e in thread t's 32-channel span of the row:
+// channels 32t + m*2*NSLOT + i and + NSLOT, with m = s / NSLOT, i = s % NSLOT.
+struct MmaSmem {
+    unsigned char* stages;   // [warp][stage][STAGE]
+    float* qs;               // [GQ][kD]
+    float* pt_all;           // [warp][4][kPtLd]
+    float* red_m;            // [warp][GQ]
+    float* red_l;            // [warp][GQ]
+    int* s_misc;             // [8]
+    float* red_acc;          // [warp][GQ][kD], aliases the stages once they are drained
+    __device__ MmaSmem(unsigned char* smem, int stage_bytes, int gq) {
+        stages = smem;
+        qs = reinterpret_cast<float*>(smem + stage_bytes);
+        pt_all = qs + gq * kD;
+        red_m = pt_all + kWarps * 4 * kPtLd;
+        red_l = red_m + kWarps * gq;
+        s_misc = reinterpret_cast<int*>(red_l + kWarps * gq);
+        red_acc = reinterpret_cast<float*>(smem);
+    }
+};
+
+// q of stream (b, h) into shared memory, scaled by softmax_scale * log2(e); the caller's
+// earlier use of qs must be over (a CTA barrier) before this runs.
+template <int DT, int GQ>
+__device__ __forceinline__ void load_q(const DecodeArgs& a, float* qs, int b, int h) {
+    const uint16_t* q = static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(b) * a.Hq + h * GQ) * kD;
+    for (int i = threadIdx.x; i < GQ * kD; i += kThreads) qs[i] = widen<DT>(q[i]) * a.scale_log2;
+}
+
+// Residual tiles [t0, t1) of stream (b, h) (tile i = tokens np + 32 i ..), lane-layout
+// CUDA-core path; leaves the merged warp states in red_* (synchronized).
+template <int DT, int GQ, int G>
+__device__ __forceinline__ void residual_segment(const DecodeArgs& a, const MmaSmem& sm, int b, int h,
+                                                 const SeqWork& w, int64_t t0, int64_t t1) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, ring = a.R + G;
+    const kivi_seq& sq = a.seqs[b];
+    float m[GQ], l[GQ], acc[GQ][kCpl];
+#pragma unroll
+    for (int hh = 0; hh < GQ; ++hh) {
+        m[hh] = -CUDART_INF_F;
+        l[hh] = 0.0f;
+#pragma unroll
+        for (int c = 0; c < kCpl; ++c) acc[hh][c] = 0.0f;
+    }
+    const uint16_t* kres = static_cast<const uint16_t*>(sq.k_res) + static_cast<int64_t>(h) * ring * kD;
+    const uint16_t* vres = static_cast<const uint16_t*>(sq.v_res) + static_cast<int64_t>(h) * ring * kD;
+    for (int64_t i = t0 + warp; i < t1; i += kWarps) {
+        residual_tile<DT, GQ>(kres, vres, ring, w.np + kTile * i, w.L, sm.qs, lane, m, l, acc);
+        __syncwarp();
+    }
+    store_lane_state<GQ>(warp, lane, m, l, acc, sm.red_m, sm.red_l, sm.red_acc);
+    __syncthreads();
+}
+
+// Packed tiles [ga, gb) of stream (b, h) on the tensor cores; leaves the merged warp states
+// in red_* (synchronized). qs holds the stream's q.
+template <int KB, int VB, int DT, int GQ, int G>
+__device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem& sm, int b, int h, int64_t ga,
+                                              int64_t gb) {
+    using Lay = MmaLayout<KB, VB>;
+    constexpr int RBK = Lay::kKRowBytes, RBV = Lay::kVRowBytes;
+    constexpr int STAGE = Lay::kStage;
+    constexpr int NSLOT = Lay::kNslot;
+    constexpr int SHIFTK = CodeShift<KB>::kValue, SHIFTV = CodeShift<VB>::kValue;
+    constexpr int TPG = G / kTile;            // tiles per key group
+    constexpr int NVG = kD / G;               // value channel groups per token
+    constexpr int VMETA = kTile * NVG * 2;    // bytes of value scales (or zeros) of one tile
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const kivi_seq& sq = a.seqs[b];
+    const int cap = sq.cap_tokens;
+    unsigned char* stages = sm.stages;
+    float* qs = sm.qs;
+    float* pt_all = sm.pt_all;
+    float* red_m = sm.red_m;
+    float* red_l = sm.red_l;
+    int* s_misc = sm.s_misc;
+    float* red_acc = sm.red_acc;
+    const int gid = lane >> 2, t = lane & 3;
+    const int hh = gid >> 1, part = gid & 1;     // B column gid = (head hh, hi/lo part)
+    const bool hv = GQ >= 4 || hh < GQ;   // this thread's B column belongs to a real head
+
+    // q prescale: a power of two putting max |q| in (1/2, 1]
+    float qmax_abs = 0.0f;
+    for (int i = tid; i < GQ * kD; i += kThreads) qmax_abs = fmaxf(qmax_abs, fabsf(qs[i]));
+    qmax_abs = warp_max(qmax_abs);
+    if (lane == 0) reinterpret_cast<float*>(s_misc)[1 + warp] = qmax_abs;
+    __syncthreads();
+    qmax_abs = fmaxf(fmaxf(reinterpret_cast<float*>(s_misc)[1], reinterpret_cast<float*>(s_misc)[2]),
+                     fmaxf(reinterpret_cast<float*>(s_misc)[3], reinterpret_cast<float*>(s_misc)[4]));
+    int qexp = 0;
+    if (qmax_abs > 0.0f) frexpf(qmax_abs, &qexp);
+    const float qpre = ldexpf(1.0f, -qexp), qpost = ldexpf(1.0f, qexp);
+
+    // per-thread constants of the key-side B operand (column gid, thread t's span)
+    uint32_t cY[16], cX[16], cZ[16], cB[16];
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+        const int c0 = 32 * t + (s / NSLOT) * 2 * NSLOT + (s % NSLOT), c1 = c0 + NSLOT;
+        const float v0 = hv ? qs[(hv ? hh : 0) * kD + c0] * qpre : 0.0f;
+        const float v1 = hv ? qs[(hv ? hh : 0) * kD + c1] * qpre : 0.0f;
+        const uint32_t qh = pack_h2(v0, v1);
+        const uint32_t ql = pack_h2(v0 - h2_lo(qh), v1 - h2_hi(qh));
+        cY[s] = qh;
+        cX[s] = part ? ql : 0u;
+        cZ[s] = part ? (qh ^ 0x80008000u) : 0u;
+        cB[s] = part ? ql : qh;
+    }
+    // value side: byte / half-word selectors of this thread's four channels per channel group
+    const uint32_t g3 = static_cast<uint32_t>(gid & 3);
+    const uint32_t sel_v = VB == 2 ? (g3 | (g3 << 4) | ((4 + g3) << 8) | ((4 + g3) << 12))
+                                   : ((gid & 1) ? 0x7632u : 0x5410u);
+    const int vbyte = VB == 2 ? 4 * (gid >> 2) : 4 * (gid >> 1);   // byte offset of the word in a 32-channel block
+    const uint32_t sel_z = (gid & 1) ? 0x7632u : 0x5410u;
+
+    float m_run = -CUDART_INF_F, l_run = 0.0f;
+    float cv[8][4], cz[4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cv[i][0] = cv[i][1] = cv[i][2] = cv[i][3] = 0.0f;
+    cz[0] = cz[1] = cz[2] = cz[3] = 0.0f;
+
+    const int64_t g0 = ga, g1 = gb;
+    const int64_t gfirst = g0 + warp;
+    const int n_my = gfirst < g1 ? static_cast<int>((g1 - gfirst + kWarps - 1) / kWarps) : 0;
+    unsigned char* my_st = stages + warp * kStages * STAGE;
+    float* pt = pt_all + warp * 4 * kPtLd;
+
+    // Tile j's code rows and value metadata sit at row-tile index rt of (32 code rows,
+    // VMETA bytes of each kind of value metadata), its key scales and zeros at group index
+    // kg of (256 bytes of each) from these bases: rt = j, kg = j / TPG in a contiguous
+    // sequence (bases at head h); rt = (page * H + h) * TPG + j mod TPG, kg = page * H + h
+    // in a paged one (bases at the pools; see group_addr), page = block_table[j / TPG].
+    const bool paged = seq_paged(sq);
+    const int64_t hc = paged ? 0 : static_cast<int64_t>(h) * cap;   // head offset in tokens
+    const unsigned char* kc_base = sq.k_codes + hc * RBK;
+    const unsigned char* vc_base = sq.v_codes + hc * RBV;
+    const unsigned char* ks_base = reinterpret_cast<const unsigned char*>(sq.k_scale + hc / G * kD);
+    const unsigned char* kz_base = reinterpret_cast<const unsigned char*>(sq.k_zero + hc / G * kD);
+    const unsigned char* vs_base = reinterpret_cast<const unsigned char*>(sq.v_scale + hc * NVG);
+    const unsigned char* vz_base = reinterpret_cast<const unsigned char*>(sq.v_zero + hc * NVG);
+
+    // Per-lane cp.async plan of one tile: code rows as 16-byte chunks (lane + 32k), then one
+    // chunk of key scale / zero (lanes 0-15 / 16-31) and of value scale / zero (lanes 0-15 /
+    // 16-31 for G = 32; lanes 0-7 / 8-15 for G = 64).
+    constexpr int kKChunks = RBK / 16, kVChunks = RBV / 16;   // per lane, per code block
+    constexpr int VL = VMETA / 16;                             // lanes per kind of value metadata
+    const int half = lane >> 4, off16 = (lane & 15) * 16;
+    const int vhalf = (lane / VL) & 1, voff16 = (lane % VL) * 16;
+    const bool v_issue = lane < 2 * VL;
+    const unsigned char* kc_lane = kc_base + lane * 16;
+    const unsigned char* vc_lane = vc_base + lane * 16;
+    const unsigned char* km_lane = (half ? kz_base : ks_base) + off16;
+    const unsigned char* vm_lane = (vhalf ? vz_base : vs_base) + voff16;
+    const int km_dst = Lay::kCodeBytes + half * Lay::kMetaPad + (off16 >> 6) * 80 + (off16 & 63);
+    const int vm_dst = Lay::kCodeBytes + 2 * Lay::kMetaPad + vhalf * 256 + voff16;
+    auto issue = [&](int slot, int64_t j, int32_t page) {
+        unsigned char* dst = my_st + slot * STAGE;
+        int64_t rt, kg;
+        if (paged) {
+            kg = static_cast<int64_t>(page) * a.H + h;
+            rt = kg * TPG + (TPG > 1 ? j % TPG : 0);
+        } else {
+            rt = j;
+            kg = TPG > 1 ? j / TPG : j;
+        }
+#pragma unroll
+        for (int k = 0; k < kKChunks; ++k)
+            cp_async16(dst + lane * 16 + 512 * k, kc_lane + rt * (kTile * RBK) + 512 * k);
+#pragma unroll
+        for (int k = 0; k < kVChunks; ++k)
+            cp_async16(dst + kTile * RBK + lane * 16 + 512 * k, vc_lane + rt * (kTile * RBV) + 512 * k);
+        cp_async16(dst + km_dst, km_lane + kg * 256);
+        if (v_issue) cp_async16(dst + vm_dst, vm_lane + rt * VMETA);
+    };
+
+    // page of this warp's i-th tile (paged sequences); the in-loop issue uses an entry
+    // loaded one iteration earlier, so the table read stays off the critical path
+    auto page_of = [&](int i) -> int32_t {
+        return paged ? sq.block_table[(gfirst + static_cast<int64_t>(kWarps) * i) / TPG] : 0;
+    };
+#pragma unroll
+    for (int i = 0; i < kStages - 1; ++i) {
+        if (i < n_my) issue(i, gfirst + static_cast<int64_t>(kWarps) * i, page_of(i));
+        cp_async_commit();
+    }
+    int32_t pg_ahead = kStages - 1 < n_my ? page_of(kStages - 1) : 0;
+
+    for (int it = 0; it < n_my; ++it) {
+        {
+            const int nxt = it + kStages - 1;
+            if (nxt < n_my) {
+                issue(nxt % kStages, gfirst + static_cast<int64_t>(kWarps) * nxt, pg_ahead);
+                pg_ahead = nxt + 1 < n_my ? page_of(nxt + 1) : 0;
+            }
+            cp_async_commit();
+        }
+        cp_async_wait<kStages - 1>();
+        __syncwarp();
+        const unsigned char* st = my_st + (it % kStages) * STAGE;
+        const unsigned char* kc = st;
+        const unsigned char* vc = st + kTile * RBK;
+        const unsigned char* ksm = st + Lay::kCodeBytes;
+        const unsigned char* kzm = ksm + Lay::kMetaPad;
+        const unsigned char* vsm = kzm + Lay::kMetaPad;    // [32 tokens][NVG] fp16
+        const unsigned char* vzm = vsm + 256;
+
+        // ---- key scale / zero pairs of this thread's span
+        uint32_t sp[16], zp[16];
+        {
+            uint32_t R[16], Z[16];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 r4 = *reinterpret_cast<const uint4*>(ksm + 80 * t + 16 * i);
+                const uint4 z4 = *reinterpret_cast<const uint4*>(kzm + 80 * t + 16 * i);
+                R[4 * i] = r4.x; R[4 * i + 1] = r4.y; R[4 * i + 2] = r4.z; R[4 * i + 3] = r4.w;
+                Z[4 * i] = z4.x; Z[4 * i + 1] = z4.y; Z[4 * i + 2] = z4.z; Z[4 * i + 3] = z4.w;
+            }
+#pragma unroll
+            for (int s = 0; s < 16; ++s) {
+                const int rel = (s / NSLOT) * 2 * NSLOT + (s % NSLOT);
+                const uint32_t sel = (rel & 1) ? 0x7632u : 0x5410u;
+                sp[s] = prmt(R[rel >> 1], R[(rel + NSLOT) >> 1], sel);
+                zp[s] = prmt(Z[rel >> 1], Z[(rel + NSLOT) >> 1], sel);
+            }
+        }
+
+        // ---- bias: every row of A is z_k, B = q (hi / lo column)
+        // two accumulators (even / odd k-steps) halve the dependent MMA chain
+        float cb[4] = {0.0f, 0.0f, 0.0f, 0.0f}, cb2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int ks = 0; ks < 8; ks += 2) {
+            mma_f16(cb, zp[2 * ks], zp[2 * ks], zp[2 * ks + 1], zp[2 * ks + 1], cB[2 * ks], cB[2 * ks + 1]);
+            mma_f16(cb2, zp[2 * ks + 2], zp[2 * ks + 2], zp[2 * ks + 3], zp[2 * ks + 3], cB[2 * ks + 2], cB[2 * ks + 3]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) cb[i] += cb2[i];
+
+        // ---- scores: A = key codes (tokens gid + 8r), B = (q * s_k) hi / lo
+        float c0[4] = {cb[0], cb[1], cb[2], cb[3]}, c1[4] = {cb[0], cb[1], cb[2], cb[3]};
+        float c0o[4] = {0.0f, 0.0f, 0.0f, 0.0f}, c1o[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // odd k-steps
+        {
+            uint32_t cw[4][KB], cws[4][KB];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const unsigned char* row = kc + (gid + 8 * r) * RBK;
+                if constexpr (KB == 2) {
+                    const uint2 v = *reinterpret_cast<const uint2*>(row + 8 * t);
+                    cw[r][0] = v.x; cw[r][1] = v.y;
+                } else {
+                    const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * t);
+                    cw[r][0] = v.x; cw[r][1] = v.y; cw[r][2] = v.z; cw[r][3] = v.w;
+                }
+#pragma unroll
+                for (int w = 0; w < KB; ++w) cws[r][w] = cw[r][w] >> SHIFTK;
+            }
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const int s0 = 2 * ks, s1 = 2 * ks + 1;
+                const uint32_t b0 = hfma2(cX[s0], sp[s0], hfma2(cY[s0], sp[s0], hmul2(cZ[s0], sp[s0])));
+                const uint32_t b1 = hfma2(cX[s1], sp[s1], hfma2(cY[s1], sp[s1], hmul2(cZ[s1], sp[s1])));
+                const int w0 = s0 / NSLOT, w1 = s1 / NSLOT;
+                uint32_t a0, a1, a2, a3;
+a0 = code_slot<KB>(cw[0][w0], cws[0][w0], s0);
+                a1 = code_slot<KB>(cw[1][w0], cws[1][w0], s0);
+                a2 = code_slot<KB>(cw[0][w1], cws[0][w1], s1);
+                a3 = code_slot<KB>(cw[1][w1], cws[1][w1], s1);
+                if (ks & 1) mma_f16(c0o, a0, a1, a2, a3, b0, b1); else mma_f16(c0, a0, a1, a2, a3, b0, b1);
+                a0 = code_slot<KB>(cw[2][w0], cws[2][w0], s0);
+                a1 = code_slot<KB>(cw[3][w0], cws[3][w0], s0);
+                a2 = code_slot<KB>(cw[2][w1], cws[2][w1], s1);
+                a3 = code_slot<KB>(cw[3][w1], cws[3][w1], s1);
+                if (ks & 1) mma_f16(c1o, a0, a1, a2, a3, b0, b1); else mma_f16(c1, a0, a1, a2, a3, b0, b1);
+            }
+        }
+
+        // ---- online softmax for head t over tokens gid, gid+8, gid+16, gid+24
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            c0[i] += c0o[i];
+            c1[i] += c1o[i];
+        }
+        float S[4] = {(c0[0] + c0[1]) * qpost, (c0[2] + c0[3]) * qpost, (c1[0] + c1[1]) * qpost,
+                      (c1[2] + c1[3]) * qpost};
+        float tmax = fmaxf(fmaxf(S[0], S[1]), fmaxf(S[2], S[3]));
+        tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 4));
+        tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
+        tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
+        const float mnew = fmaxf(m_run, tmax);
+        if (__any_sync(kFull, mnew > m_run)) {
+            const float alpha = exp2f(m_run - mnew);
+            l_run *= alpha;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                cv[i][0] *= alpha; cv[i][1] *= alpha; cv[i][2] *= alpha; cv[i][3] *= alpha;
+            }
+            cz[0] *= alpha; cz[1] *= alpha; cz[2] *= alpha; cz[3] *= alpha;
+            m_run = mnew;
+        }
+        float p[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) p[r] = (GQ >= 4 || t < GQ) ? exp2f(S[r] - m_run) : 0.0f;
+        l_run += (p[0] + p[1]) + (p[2] + p[3]);
+#pragma unroll
+        // token 8r + j goes to column 8r + 2 (j % 4) + j / 4: the value side pairs tokens
+        // (8r + t', 8r + t' + 4), which then sit side by side
+        for (int r = 0; r < 4; ++r) pt[t * kPtLd + 8 * r + 2 * (gid & 3) + (gid >> 2)] = p[r];
+        __syncwarp();
+
+        // ---- value side B operands: P' = p * s_v (hi / lo), and p (hi / lo) for the z_v term
+        uint32_t vb[2][2][4], bp[2][2], za[2][2];
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int tau0 = 16 * k2 + 8 * e + t;      // pair (tau0, tau0 + 4)
+                const float2 pp = hv ? *reinterpret_cast<const float2*>(pt + (hv ? hh : 0) * kPtLd + 16 * k2 + 8 * e + 2 * t)
+                                     : make_float2(0.0f, 0.0f);
+                const uint32_t ph = pack_h2(pp.x, pp.y);
+                const uint32_t pl = pack_h2(pp.x - h2_lo(ph), pp.y - h2_hi(ph));
+                const uint32_t xp = part ? pl : 0u, zn = part ? (ph ^ 0x80008000u) : 0u;
+                bp[k2][e] = part ? pl : ph;
+                // scales of tokens tau0 and tau0 + 4 for each 32-channel block kg (its
+                // channel group is kg / TPG)
+                uint32_t s0w[NVG / 2 > 0 ? NVG / 2 : 1], s1w[NVG / 2 > 0 ? NVG / 2 : 1];
+                if constexpr (NVG == 4) {
+                    const uint2 x0 = *reinterpret_cast<const uint2*>(vsm + tau0 * 8);
+                    const uint2 x1 = *reinterpret_cast<const uint2*>(vsm + (tau0 + 4) * 8);
+                    s0w[0] = x0.x; s0w[1] = x0.y; s1w[0] = x1.x; s1w[1] = x1.y;
+                } else {
+                    s0w[0] = *reinterpret_cast<const uint32_t*>(vsm + tau0 * 4);
+                    s1w[0] = *reinterpret_cast<const uint32_t*>(vsm + (tau0 + 4) * 4);
+                }
+#pragma unroll
+                for (int kg = 0; kg < 4; ++kg) {
+                    const int vg = kg / TPG;
+                    const uint32_t svp = prmt(s0w[vg >> 1], s1w[vg >> 1], (vg & 1) ? 0x7632u : 0x5410u);
+                    vb[k2][e][kg] = hfma2(xp, svp, hfma2(ph, svp, hmul2(zn, svp)));
+                }
+                // rows of the zero-point MMA: channel group gid (gid < NVG)
+                const uint32_t zw0 = *reinterpret_cast<const uint32_t*>(vzm + tau0 * (2 * NVG) + 4 * ((gid & 3) >> 1));
+                const uint32_t zw1 = *reinterpret_cast<const uint32_t*>(vzm + (tau0 + 4) * (2 * NVG) + 4 * ((gid & 3) >> 1));
+                za[k2][e] = gid < NVG ? prmt(zw0, zw1, sel_z) : 0u;
+            }
+        }
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) mma_f16(cz, za[k2][0], 0u, za[k2][1], 0u, bp[k2][0], bp[k2][1]);
+
+        // ---- value codes (A = codes^T, rows = channels of one channel group) and P' V
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) {
+#pragma unroll
+            for (int kg = 0; kg < 4; ++kg) {
+                uint32_t wv[2], wvs[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int tau0 = 16 * k2 + 8 * e + t;
+                    const int off = kg * (RBV / 4) + vbyte;
+                    const uint32_t x0 = *reinterpret_cast<const uint32_t*>(vc + tau0 * RBV + off);
+                    const uint32_t x1 = *reinterpret_cast<const uint32_t*>(vc + (tau0 + 4) * RBV + off);
+                    wv[e] = prmt(x0, x1, sel_v);
+                    wvs[e] = wv[e] >> SHIFTV;
+                }
+                // m-tile 2kg + u: rows gid (slot 2u) and gid + 8 (slot 2u + 1)
+                mma_f16(cv[2 * kg], code_pair<VB, 0>(wv[0], wvs[0]), code_pair<VB, 1>(wv[0], wvs[0]),
+                        code_pair<VB, 0>(wv[1], wvs[1]), code_pair<VB, 1>(wv[1], wvs[1]), vb[k2][0][kg],
+                        vb[k2][1][kg]);
+                mma_f16(cv[2 * kg + 1], code_pair<VB, 2>(wv[0], wvs[0]), code_pair<VB, 3>(wv[0], wvs[0]),
+                        code_pair<VB, 2>(wv[1], wvs[1]), code_pair<VB, 3>(wv[1], wvs[1]), vb[k2][0][kg],
+                        vb[k2][1][kg]);
+            }
+        }
+        __syncwarp();
+    }
+    cp_async_wait<0>();
+
+    // ---- warp state -> merge arrays (red_acc aliases the stages: wait for every warp)
+    float l_tot = l_run;
+    l_tot += __shfl_xor_sync(kFull, l_tot, 4);
+    l_tot += __shfl_xor_sync(kFull, l_tot, 8);
+    l_tot += __shfl_xor_sync(kFull, l_tot, 16);
+    float zk[4];
+    const float zmine = cz[0] + cz[1];     // (channel group gid, head t) for gid < NVG
+#pragma unroll
+    for (int kg = 0; kg < 4; ++kg) zk[kg] = __shfl_sync(kFull, zmine, 4 * (kg / TPG) + t);
+    __syncthreads();
+    if (GQ >= 4 || t < GQ) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            const int kg = mt >> 1;
+            const int ch = 32 * kg + 4 * gid + 2 * (mt & 1);
+            red_acc[(warp * GQ + t) * kD + ch] = cv[mt][0] + cv[mt][1] + zk[kg];
+            red_acc[(warp * GQ + t) * kD + ch + 1] = cv[mt][2] + cv[mt][3] + zk[kg];
+        }
+        if (gid == 0) {
+            red_m[warp * GQ + t] = m_run;
+            red_l[warp * GQ + t] = l_tot;
+        }
+    }
+    __syncthreads();
+}
+
+template <int KB, int VB, int DT, int GQ, int G>
+__global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_kernel(DecodeArgs a) {
+    static_assert(GQ == 1 || GQ == 2 || GQ == 4, "one n8 tile holds hi and lo of up to four heads");
+    extern __shared__ __align__(16) unsigned char smem[];
+    const MmaSmem sm(smem, MmaLayout<KB, VB>::kStageBytes, GQ);
+    int64_t* sched = reinterpret_cast<int64_t*>(smem);   // scan scratch: the stages are idle until the walk
+    const int tid = threadIdx.x;
+    const int C = gridDim.x, c = blockIdx.x, H = a.H;
+
+    // sequences without work: zeros for an empty one, NaN and a status for a bad length
+    for (int b = c; b < a.nseq; b += C) {
+        const SeqWork w = seq_work<G>(a, b);
+        if (w.u != 0) continue;
+        float* o = a.out + static_cast<int64_t>(b) * a.Hq * kD;
+        for (int i = tid; i < a.Hq * kD; i += kThreads) o[i] = w.bad ? CUDART_NAN_F : 0.0f;
+        if (w.bad && tid == 0) set_status(a.status, KIVI_ERR_LENGTH);
+    }
+
+    // units before each thread's run of sequences (exclusive scan), the total U, and this
+    // CTA's range [lo, hi)
+    const int per = (a.nseq + kThreads - 1) / kThreads;
+    const int b_lo = tid * per < a.nseq ? tid * per : a.nseq;
+    const int b_hi = b_lo + per < a.nseq ? b_lo + per : a.nseq;
+    int64_t mine = 0;
+    for (int b = b_lo; b < b_hi; ++b) mine += static_cast<int64_t>(H) * seq_work<G>(a, b).u;
+    // the walk state lives in shared memory and is read back (volatile) around each
+    // segment, so that the hot loops do not hold it in registers: lo, hi, U, Ceff, the
+    // first unit of sequence b, b, h (b = nseq ends the walk)
+    __shared__ int64_t walk[7];
+    volatile int64_t* vw = walk;
+    sched[tid] = mine;
+    __syncthreads();
+    if (tid == 0) {
+        vw[5] = a.nseq;
+        int64_t run = 0;
+        for (int i = 0; i < kThreads; ++i) {
+            const int64_t v = sched[i];
+            sched[i] = run;
+            run += v;
+        }
+        sched[kThreads] = run;
+    }
+    __syncthreads();
+    const int64_t U = sched[kThreads];
+    const int64_t by_size = U / kMinUnitsPerCta > 1 ? U / kMinUnitsPerCta : 1;
+    const int64_t Ceff = C < by_size ? C : by_size;
+    if (U == 0 || c >= Ceff) return;
+    const int64_t lo = c * U / Ceff, hi = (c + 1) * U / Ceff;
+    const int64_t start = sched[tid];
+    if (mine > 0 && lo >= start && lo < start + mine) {
+        int64_t p = start;
+        for (int b = b_lo; b < b_hi; ++b) {
+            const int64_t ub = static_cast<int64_t>(H) * seq_work<G>(a, b).u;
+            if (lo < p + ub) {
+                vw[0] = lo;
+                vw[1] = hi;
+                vw[2] = U;
+                vw[3] = Ceff;
+                vw[4] = p;
+                vw[5] = b;
+                vw[6] = 0;
+                break;
+            }
+            p += ub;
+        }
+    }
+    __syncthreads();
+
+    // stream (vw[5], vw[6]) and the part of it this CTA holds: [x0, x1) in its units
+    // (x0, x1 count from the stream's first group; x1 <= x0: no work here)
+    struct Cur {
+        int b, h;
+        int64_t Ps, Ws, x0, x1;   // first unit of the stream and of its groups
+        SeqWork w;
+    };
+    auto current = [&]() {
+        Cur k;
+        k.b = static_cast<int>(vw[5]);
+        k.h = static_cast<int>(vw[6]);
+        k.w = seq_work<G>(a, k.b);
+        k.Ps = vw[4] + k.h * k.w.u;
+        k.Ws = k.Ps + kStreamOverhead;
+        const int64_t lo_ = vw[0], hi_ = vw[1];
+        k.x0 = (lo_ > k.Ws ? lo_ : k.Ws) - k.Ws;
+        k.x1 = (hi_ < k.Ps + k.w.u ? hi_ : k.Ps + k.w.u) - k.Ws;
+        return k;
+    };
+    auto finish = [&](int part) {
+        const Cur k = current();
+        const int64_t U_ = vw[2], Ceff_ = vw[3];
+        StreamSegs ss;
+        ss.s = static_cast<int64_t>(k.b) * H + k.h;
+        ss.cg0 = owner(k.Ws, U_, Ceff_);
+        ss.cg1 = k.w.ng > 0 ? owner(k.Ws + k.w.ng - 1, U_, Ceff_) : ss.cg0 - 1;
+        ss.cr0 = owner(k.Ws + k.w.ng, U_, Ceff_);
+        ss.cr1 = k.w.rt > 0 ? owner(k.Ps + k.w.u - 1, U_, Ceff_) : ss.cr0 - 1;
+        ss.nseg = static_cast<int>((ss.cg1 - ss.cg0 + 1) + (ss.cr1 - ss.cr0 + 1));
+        float* out_s = a.out + (static_cast<int64_t>(k.b) * a.Hq + static_cast<int64_t>(k.h) * GQ) * kD;
+        finish_segment<GQ>(a, ss, 2 * ss.s + part + c, out_s, sm.red_m, sm.red_l, sm.red_acc, &sm.s_misc[0],
+                           reinterpret_cast<float*>(smem) + GQ * (kWarps + 1) * kD + GQ);
+    };
+
+    while (true) {
+        {
+            const int b = static_cast<int>(vw[5]);
+            if (b >= a.nseq || vw[4] >= vw[1]) break;
+        }
+        Cur k = current();
+        if (k.Ps >= vw[1]) break;
+        if (k.w.u != 0 && k.x1 > k.x0) {
+            if (k.x0 < k.w.ng) {
+                __syncthreads();   // the previous segment is done with qs and the shared arrays
+                load_q<DT, GQ>(a, sm.qs, k.b, k.h);
+                __syncthreads();
+                group_segment<KB, VB, DT, GQ, G>(a, sm, k.b, k.h, k.x0, k.x1 < k.w.ng ? k.x1 : k.w.ng);
+                finish(0);
+                k = current();
+            }
+            if (k.x1 > k.w.ng) {
+                const int64_t u0 = (k.x0 > k.w.ng ? k.x0 : k.w.ng) - k.w.ng, u1 = k.x1 - k.w.ng;
+                __syncthreads();
+                load_q<DT, GQ>(a, sm.qs, k.b, k.h);
+                __syncthreads();
+                residual_segment<DT, GQ, G>(a, sm, k.b, k.h, k.w, (u0 + kResidualWeight - 1) / kResidualWeight,
+                                         (u1 + kResidualWeight - 1) / kResidualWeight);
+                finish(1);
+            }
+        }
+        __syncthreads();   // every thread has read the walk state of this stream
+        if (tid == 0) {
+            const int b = static_cast<int>(vw[5]), h = static_cast<int>(vw[6]);
+            if (h + 1 < H) {
+                vw[6] = h + 1;
+            } else {
+                vw[4] = vw[4] + static_cast<int64_t>(H) * seq_work<G>(a, b).u;
+                vw[5] = b + 1;
+                vw[6] = 0;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// Resident CTAs of a kernel on the current device (SM count x blocks per SM), cached per
+// device; at most kMaxCtas.
+template <typename K>
+int resident_ctas(K kernel, int smem, int* cache) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev] > 0) return cache[dev];
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem) != cudaSuccess) return 0;
+    int n = sms * (per_sm > 0 ? per_sm : 1);
+    n = n > kMaxCtas ? kMaxCtas : n;
+    cache[dev] = n;
+    return n;
+}
+
+template <int KB, int VB, int DT, int GQ, int G>
+cudaError_t launch_mma(const DecodeArgs& a, cudaStream_t stream) {
+    constexpr int smem = MmaLayout<KB, VB>::kSmemBytes(GQ);
+    static int ctas[64] = {};
+    const cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<KB, VB, DT, GQ, G>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int n = resident_ctas(decode_mma_kernel<KB, VB, DT, GQ, G>, smem, ctas);
+    if (n <= 0) return cudaErrorInvalidValue;
+    decode_mma_kernel<KB, VB, DT, GQ, G><<<n, kThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <int KB, int VB, int DT, int G>
+cudaError_t launch_gq(const DecodeArgs& a, cudaStream_t stream) {
+    switch (a.Hq / a.H) {
+        case 1: return launch_mma<KB, VB, DT, 1, G>(a, stream);
+        case 2: return launch_mma<KB, VB, DT, 2, G>(a, stream);
+        case 4: return launch_mma<KB, VB, DT, 4, G>(a, stream);
+        case 8:
+            decode_split_kernel<KB, VB, DT, 8, G><<<dim3(a.max_splits, a.H, a.nseq), kThreads, 0, stream>>>(a);
+            break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+// Decode for one pair of code widths: dispatches the input type and G.
+template <int KB, int VB>
+cudaError_t launch_kv(const DecodeArgs& a, cudaStream_t stream) {
+    if (a.nseq == 0) return cudaSuccess;
+    if (a.G == 64) {
+        return a.dtype == KIVI_F16 ? launch_gq<KB, VB, KIVI_F16, 64>(a, stream)
+                                   : launch_gq<KB, VB, KIVI_BF16, 64>(a, stream);
+    }
+    return a.dtype == KIVI_F16 ? launch_gq<KB, VB, KIVI_F16, 32>(a, stream) : launch_gq<KB, VB, KIVI_BF16, 32>(a, stream);
+}
+
+}  // namespace
+}  // namespace kivi

@@ -12,7 +12,9 @@
 
 namespace kivi {
 
-constexpr int kGroup = 32;          // G: tokens per key group, channels per value group
+// G (tokens per key group, channels per value group) is 32 or 64. Kernels work in
+// tiles of 32 tokens: a packed group is one or two whole tiles.
+constexpr int kTile = 32;
 constexpr int kMaxHeadDim = 256;
 
 // ---------------------------------------------------------------- formats
@@ -63,14 +65,15 @@ __device__ __forceinline__ uint32_t encode(float x, float z, float s, int qmax) 
 
 // ---------------------------------------------------------------- cache state
 
-__host__ __device__ __forceinline__ int64_t n_packed(int64_t L, int R) {
+__host__ __device__ __forceinline__ int64_t n_packed(int64_t L, int R, int G) {
     const int64_t over = L - R;
-    return over <= 0 ? 0 : (over / kGroup) * kGroup;
+    return over <= 0 ? 0 : (over / G) * G;
 }
 
 // Addresses of packed group j of kv head h of a sequence, in either layout of kivi.h:
-// its G key code rows, D key scales and zeros, G value code rows and G x (D / G) value
-// scales and zeros. page is block_table[j] for a paged sequence (ignored otherwise).
+// its G key code rows (kb bits per code), D key scales and zeros, G value code rows (vb
+// bits per code) and G x (D / G) value scales and zeros. page is block_table[j] for a
+// paged sequence (ignored otherwise).
 struct GroupAddr {
     uint8_t* kc;
     uint16_t* ks;
@@ -83,23 +86,23 @@ struct GroupAddr {
 __device__ __forceinline__ bool seq_paged(const kivi_seq& sq) { return (sq.flags & KIVI_SEQ_PAGED) != 0; }
 
 __device__ __forceinline__ GroupAddr group_addr(const kivi_seq& sq, int H, int h, int64_t j, int32_t page, int D,
-                                                int bits) {
-    const int64_t rb = static_cast<int64_t>(D) * bits / 8, ng = D / kGroup;
+                                                int kb, int vb, int G) {
+    const int64_t ng = D / G;
     int64_t row0, meta;   // first code row of the group, and its (head, group) metadata row
     if (seq_paged(sq)) {
         const int64_t pg = static_cast<int64_t>(page) * H + h;
-        row0 = pg * kGroup;
+        row0 = pg * G;
         meta = pg;
     } else {
         const int64_t cap = sq.cap_tokens;
-        row0 = h * cap + j * kGroup;
-        meta = h * (cap / kGroup) + j;
+        row0 = h * cap + j * G;
+        meta = h * (cap / G) + j;
     }
     GroupAddr a;
-    a.kc = sq.k_codes + row0 * rb;
+    a.kc = sq.k_codes + row0 * (static_cast<int64_t>(D) * kb / 8);
     a.ks = sq.k_scale + meta * D;
     a.kz = sq.k_zero + meta * D;
-    a.vc = sq.v_codes + row0 * rb;
+    a.vc = sq.v_codes + row0 * (static_cast<int64_t>(D) * vb / 8);
     a.vs = sq.v_scale + row0 * ng;
     a.vz = sq.v_zero + row0 * ng;
     return a;
@@ -109,6 +112,20 @@ __device__ __forceinline__ int32_t group_page(const kivi_seq& sq, int64_t j) {
     return seq_paged(sq) ? sq.block_table[j] : 0;
 }
 
+// The same for 32-token tile jt of the packed tokens (group jt / (G / 32)): its code
+// rows and value metadata rows, and the key scales and zeros of its group.
+__device__ __forceinline__ GroupAddr tile_addr(const kivi_seq& sq, int H, int h, int64_t jt, int D, int kb, int vb,
+                                               int G) {
+    const int tpg = G / kTile;
+    const int64_t j = jt / tpg, sub = (jt - j * tpg) * kTile;
+    GroupAddr a = group_addr(sq, H, h, j, group_page(sq, j), D, kb, vb, G);
+    a.kc += sub * (static_cast<int64_t>(D) * kb / 8);
+    a.vc += sub * (static_cast<int64_t>(D) * vb / 8);
+    a.vs += sub * (D / G);
+    a.vz += sub * (D / G);
+    return a;
+}
+
 __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
     if (status != nullptr) atomicCAS(status, 0, code);
 }
@@ -116,7 +133,7 @@ __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
 // ---------------------------------------------------------------- launchers
 
 struct CodecArgs {
-    int bits, D, dtype;
+    int bits, G, D, dtype;
     int n_streams, n_tokens;
     const void* x;
     uint8_t* codes;
@@ -128,7 +145,7 @@ cudaError_t launch_quant_keys(const CodecArgs& a, cudaStream_t stream);
 cudaError_t launch_quant_values(const CodecArgs& a, cudaStream_t stream);
 
 struct AppendArgs {
-    int bits, D, R, H, dtype;
+    int kb, vb, G, D, R, H, dtype;
     int nseq, max_new;
     const kivi_seq* seqs;
     int32_t* kv_len;
@@ -141,7 +158,7 @@ struct AppendArgs {
 cudaError_t launch_append_flush(const AppendArgs& a, cudaStream_t stream);
 
 struct DecodeArgs {
-    int bits, D, R, Hq, H, dtype;
+    int kb, vb, G, D, R, Hq, H, dtype;
     int nseq, max_kv_len;
     int chunk, max_splits;          // tokens per split (multiple of 32), splits per sequence
     const kivi_seq* seqs;
@@ -154,10 +171,18 @@ struct DecodeArgs {
     int32_t* status;
 };
 
+// Bound on the persistent decode grid (CTAs); sizes its workspace.
+constexpr int kDecodeMaxCtas = 1024;
+
 // Split policy and workspace layout shared by kivi_decode_workspace_bytes and the launch.
 void decode_plan(int nseq, int H, int Hq, int D, int max_kv_len, int* chunk, int* max_splits,
                  size_t* counter_bytes, size_t* partial_bytes);
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+// One per pair of key / value code widths, each in a translation unit of its own.
+cudaError_t launch_decode_k2v2(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_k2v4(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_k4v2(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_k4v4(const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace kivi

@@ -47,12 +47,12 @@ def dequant(cfg: Config, x: torch.Tensor, axis: str) -> torch.Tensor:
     S, T, D = x.shape
     if axis == "channel":
         codes, scale, zero = quant_keys(cfg, x)
-        s = f16(scale).repeat_interleave(GROUP, dim=1)               # [S][T][D]
-        z = f16(zero).repeat_interleave(GROUP, dim=1)
+        s = f16(scale).repeat_interleave(cfg.group, dim=1)               # [S][T][D]
+        z = f16(zero).repeat_interleave(cfg.group, dim=1)
     else:
         codes, scale, zero = quant_values(cfg, x)
-        s = f16(scale).repeat_interleave(GROUP, dim=2)               # [S][T][D]
-        z = f16(zero).repeat_interleave(GROUP, dim=2)
+        s = f16(scale).repeat_interleave(cfg.group, dim=2)               # [S][T][D]
+        z = f16(zero).repeat_interleave(cfg.group, dim=2)
     return unpack(codes, cfg.bits, D).to(torch.float64) * s + z
 
 

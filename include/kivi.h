@@ -30,20 +30,22 @@
  *  - fp16 scale and zero bit patterns are stored as uint16_t.
  *
  * Quantization rule (the codec; the guide's "Step 1" with the zero point
- * taken as the group minimum itself). For a group of G = 32 values x_i,
+ * taken as the group minimum itself). For a group of G values x_i,
  * widened exactly to fp32:
  *     mn = min x_i, mx = max x_i
  *     s  = fp16_rn( (mx - mn) / qmax )     qmax = 2^bits - 1, IEEE fp32 sub/div
  *     z  = fp16_rn( mn )
  *     c_i = clamp( rint( (x_i - float(z)) / float(s) ), 0, qmax )  (c_i = 0 if s == 0)
  *     dequantized value = c_i * s + z
- * Keys: one group per (kv head, 32 consecutive tokens aligned to position 0,
- * channel). Values: one group per (kv head, token, 32 consecutive channels).
- * Domain: finite inputs with |x| <= 65504 (scale and zero are fp16).
+ * Keys: one group per (kv head, G consecutive tokens aligned to position 0,
+ * channel), coded at k_bits. Values: one group per (kv head, token, G
+ * consecutive channels), coded at v_bits. Domain: finite inputs with
+ * |x| <= 65504 (scale and zero are fp16).
  *
  * Packing rule: a token row holds its D codes, channel d in byte
  * d*bits/8 at bit offset (d mod (8/bits))*bits, lowest bits first
- * (four 2-bit codes, or two 4-bit codes, per byte).
+ * (four 2-bit codes, or two 4-bit codes, per byte); bits is k_bits for key
+ * rows and v_bits for value rows.
  *
  * Cache state of one sequence holding L tokens (a pure function of L):
  *     n_packed(L) = G * floor(max(L - R, 0) / G)     packed tokens [0, n_packed)
@@ -53,7 +55,9 @@
  * (the guide's fp16 window that is "grouped and packed" once tokens slide
  * past it; G = 32 and R = 128 by default, "KV cache quantization with KIVI
  * INT2 setup guide 2026", section "KIVI: Per-Channel Key, Per-Token Value
- * Quantization Explained").
+ * Quantization Explained"; G = 64, R = 64 and separate k_bits / v_bits in
+ * the config example of "KV-Cache Quantization: I Ran the Experiments So You
+ * Don't Have To", section "Component 4" (serving architecture and manifests)).
  */
 #ifndef KIVI_H
 #define KIVI_H
@@ -65,7 +69,7 @@
 extern "C" {
 #endif
 
-#define KIVI_ABI_VERSION 2
+#define KIVI_ABI_VERSION 3
 
 typedef enum kivi_status {
     KIVI_OK = 0,
@@ -84,10 +88,11 @@ typedef enum kivi_dtype {
 
 /* Configuration (host memory). */
 typedef struct kivi_cfg {
-    int32_t bits;          /* code width: 2 or 4 */
-    int32_t group;         /* G: must be 32 */
+    int32_t k_bits;        /* key code width: 2 or 4 */
+    int32_t v_bits;        /* value code width: 2 or 4 */
+    int32_t group;         /* G: 32 or 64 */
     int32_t residual;      /* R: residual window, a positive multiple of G */
-    int32_t head_dim;      /* D: multiple of 32, at most 256 (decode attention: 128) */
+    int32_t head_dim;      /* D: multiple of G, at most 256 (decode attention: 128) */
     int32_t num_q_heads;   /* Hq (attention only), a multiple of num_kv_heads */
     int32_t num_kv_heads;  /* Hkv */
     int32_t dtype;         /* kivi_dtype of K, V, q and the residual ring */
@@ -99,10 +104,10 @@ typedef struct kivi_cfg {
  * can hold up to cap + R + G - 1 tokens.
  *
  * Contiguous layout (flags = 0): the packed buffers belong to this sequence.
- *   k_codes [Hkv][cap][D*bits/8]  u8     packed key rows
+ *   k_codes [Hkv][cap][D*k_bits/8]  u8   packed key rows
  *   k_scale [Hkv][cap/G][D]       fp16   per (key group, channel)
  *   k_zero  [Hkv][cap/G][D]       fp16
- *   v_codes [Hkv][cap][D*bits/8]  u8     packed value rows
+ *   v_codes [Hkv][cap][D*v_bits/8]  u8   packed value rows
  *   v_scale [Hkv][cap][D/G]       fp16   per (token, channel group)
  *   v_zero  [Hkv][cap][D/G]       fp16
  *
@@ -110,8 +115,8 @@ typedef struct kivi_cfg {
  * pages that any number of sequences may share. A page holds one packed group
  * of G tokens for every kv head, laid out like a contiguous sequence with
  * cap = G:
- *   k_codes [pages][Hkv][G][D*bits/8], k_scale, k_zero [pages][Hkv][D],
- *   v_codes [pages][Hkv][G][D*bits/8], v_scale, v_zero [pages][Hkv][G][D/G]
+ *   k_codes [pages][Hkv][G][D*k_bits/8], k_scale, k_zero [pages][Hkv][D],
+ *   v_codes [pages][Hkv][G][D*v_bits/8], v_scale, v_zero [pages][Hkv][G][D/G]
  * block_table [cap/G] int32 (device memory) gives the page of each packed
  * group of the sequence, in order; the caller keeps the pages of different
  * sequences apart. Packed groups are written once (when they leave the
@@ -146,7 +151,7 @@ typedef struct kivi_seq {
  * Per-channel key quantization ("The Three Structural Innovations of KIVI",
  * item 1: key elements grouped along the sequence for each channel).
  *   x     [n_streams][n_tokens][D] dtype, n_tokens a multiple of G
- *   codes [n_streams][n_tokens][D*bits/8]
+ *   codes [n_streams][n_tokens][D*k_bits/8]
  *   scale, zero [n_streams][n_tokens/G][D] fp16
  * Errors: KIVI_ERR_ARG for a bad config, NULL pointers, negative sizes or
  * n_tokens % G != 0. n_streams == 0 or n_tokens == 0 is a no-op.
@@ -157,9 +162,9 @@ kivi_status kivi_quant_keys(const kivi_cfg* cfg, int32_t n_streams, int32_t n_to
 
 /*
  * Per-token value quantization (same section, item 2: value elements
- * grouped along the channels of each token), 32 channels per group.
+ * grouped along the channels of each token), G channels per group.
  *   x     [n_streams][n_tokens][D] dtype, any n_tokens >= 0
- *   codes [n_streams][n_tokens][D*bits/8]
+ *   codes [n_streams][n_tokens][D*v_bits/8]
  *   scale, zero [n_streams][n_tokens][D/G] fp16
  */
 kivi_status kivi_quant_values(const kivi_cfg* cfg, int32_t n_streams, int32_t n_tokens,

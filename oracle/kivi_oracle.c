@@ -38,8 +38,9 @@
  *  - keys: one group per (G consecutive tokens, channel), aligned to absolute
  *    position 0; values: one group per (token, G consecutive channels);
  *    G = 32 by default, 64 in the config example of "KV-Cache Quantization:
- *    I Ran the Experiments So You Don't Have To" (which also sets R = 64 and
- *    separate key and value widths, k_bits and v_bits);
+ *    I Ran the Experiments So You Don't Have To", section "Component 4"
+ *    (which also sets R = 64 and separate key and value widths, k_bits and
+ *    v_bits);
  *  - the residual ring has R+G slots and position p lives in slot p mod (R+G);
  *    a group is flushed when the residual reaches R+G tokens;
  *  - query head hq reads kv head hq / (Hq/Hkv); no mask; the decode query

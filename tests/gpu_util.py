@@ -29,9 +29,14 @@ def host_bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
 
 
-def configs(bits, dtype, hq, h, D=128, R=128):
-    return (kivi.Config(bits=bits, head_dim=D, num_q_heads=hq, num_kv_heads=h, dtype=KIVI_DT[dtype], residual=R),
-            oracle.Cfg(bits=bits, head_dim=D, num_q_heads=hq, num_kv_heads=h, dtype=ORC_DT[dtype], residual=R))
+def configs(bits, dtype, hq, h, D=128, R=128, G=32, kb=None, vb=None):
+    """Library and oracle configs of one setting (kb / vb default to bits)."""
+    kb = bits if kb is None else kb
+    vb = bits if vb is None else vb
+    return (kivi.Config(k_bits=kb, v_bits=vb, head_dim=D, num_q_heads=hq, num_kv_heads=h, dtype=KIVI_DT[dtype],
+                        residual=R, group=G),
+            oracle.Cfg(k_bits=kb, v_bits=vb, head_dim=D, num_q_heads=hq, num_kv_heads=h, dtype=ORC_DT[dtype],
+                       residual=R, group=G))
 
 
 def assert_state_equal(cache: "kivi.KVCache", b: int, ref: "oracle.SeqCache") -> None:

@@ -30,7 +30,7 @@ def test_exports_every_declared_symbol(lib):
     assert "kivi_decode_attn" in names and len(names) >= 10
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.kivi_abi_version() == 2
+    assert lib.kivi_abi_version() == 3
 
 
 def test_status_strings(lib):
@@ -41,22 +41,28 @@ def test_status_strings(lib):
 
 def test_seq_bytes_and_n_packed(lib):
     import oracle
-    for bits in (2, 4):
+    for kb, vb, G, R in ((2, 2, 32, 128), (4, 4, 32, 128), (2, 4, 64, 64), (4, 2, 64, 128), (2, 4, 32, 64)):
         for dt in (kivi.F16, kivi.BF16):
-            cfg = kivi.Config(bits=bits, num_q_heads=32, num_kv_heads=8, dtype=dt)
-            ocfg = oracle.Cfg(bits=bits, num_q_heads=32, num_kv_heads=8, dtype=dt)
-            for cap in (0, 32, 4096, 32768):
+            cfg = kivi.Config(k_bits=kb, v_bits=vb, group=G, residual=R, num_q_heads=32, num_kv_heads=8, dtype=dt)
+            ocfg = oracle.Cfg(k_bits=kb, v_bits=vb, group=G, residual=R, num_q_heads=32, num_kv_heads=8, dtype=dt)
+            for cap in (0, 64, 4096, 32768):
                 assert cfg.seq_bytes(cap) == oracle.seq_bytes(ocfg, cap)
                 assert sum(cfg.seq_buffer_bytes(cap)) == cfg.seq_bytes(cap)
-            for L in (0, 1, 127, 128, 159, 160, 161, 1024, 16384 + 511):
+            kc, ks, kz, vc, vs, vz, kr, vr = cfg.seq_buffer_bytes(4096)
+            assert kc == 8 * 4096 * 128 * kb // 8 and vc == 8 * 4096 * 128 * vb // 8
+            assert ks == kz == 8 * (4096 // G) * 128 * 2 and vs == vz == 8 * 4096 * (128 // G) * 2
+            assert kr == vr == 8 * (R + G) * 128 * 2
+            for L in (0, 1, 63, 64, 127, 128, 159, 160, 161, 1024, 16384 + 511):
                 assert cfg.n_packed(L) == oracle.n_packed(ocfg, L)
     assert kivi.Config(group=16).seq_bytes(64) == -1
+    assert kivi.Config(group=64).seq_bytes(32) == -1          # capacity not a multiple of G
     assert kivi.Config().n_packed(-1) == -1
 
 
-@pytest.mark.parametrize("bad", [dict(bits=3), dict(group=64), dict(residual=100), dict(head_dim=96 + 1),
-                                 dict(head_dim=512), dict(num_q_heads=6, num_kv_heads=4), dict(dtype=7),
-                                 dict(residual=0), dict(num_kv_heads=0)])
+@pytest.mark.parametrize("bad", [dict(bits=3), dict(k_bits=8), dict(v_bits=1), dict(group=48), dict(group=128),
+                                 dict(residual=100), dict(group=64, residual=96), dict(group=64, head_dim=96),
+                                 dict(head_dim=96 + 1), dict(head_dim=512), dict(num_q_heads=6, num_kv_heads=4),
+                                 dict(dtype=7), dict(residual=0), dict(num_kv_heads=0)])
 def test_bad_config_rejected_before_launch(lib, bad):
     cfg = kivi.Config(**bad).c()
     P = ctypes.c_void_p
@@ -95,6 +101,25 @@ def test_bad_arguments_rejected_before_launch(lib):
     assert lib.kivi_quant_keys(cfg, 0, 32, null, null, null, null, None) == kivi.OK
     assert lib.kivi_append_flush(cfg, 0, null, null, null, null, null, 0, null, None) == kivi.OK
     assert lib.kivi_decode_attn(cfg, 0, null, null, null, null, 0.1, 0, null, 0, null, None) == kivi.OK
+
+
+def test_cfg_struct_matches_header(tmp_path):
+    """The binding's kivi_cfg fields: same size and offsets as the C struct."""
+    import subprocess
+    src = tmp_path / "cfg.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "kivi.h"\n'
+                   'int main(void) { printf("%zu %zu %zu %zu %zu\\n", sizeof(kivi_cfg), '
+                   'offsetof(kivi_cfg, k_bits), offsetof(kivi_cfg, v_bits), offsetof(kivi_cfg, group), '
+                   'offsetof(kivi_cfg, dtype)); return 0; }\n')
+    exe = tmp_path / "cfg"
+    subprocess.run(["gcc", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
+    size, kb, vb, grp, dt = map(int, subprocess.run([str(exe)], capture_output=True, text=True,
+                                                     check=True).stdout.split())
+    C = kivi._Cfg
+    assert size == ctypes.sizeof(C)
+    assert (kb, vb, grp, dt) == (C.k_bits.offset, C.v_bits.offset, C.group.offset, C.dtype.offset)
+    c = kivi.Config(k_bits=4, v_bits=2, group=64, residual=64).c()
+    assert (c.k_bits, c.v_bits, c.group, c.residual) == (4, 2, 64, 64)
 
 
 def test_seq_record_layout_matches_header(tmp_path):

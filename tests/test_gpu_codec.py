@@ -22,15 +22,19 @@ def structured(rng, S, T, D, dtype):
     return to_dtype_bits(x, dtype)
 
 
+# (G, D): every slice width of each group size (D a multiple of G)
+GD_KEYS = [(32, D) for D in (32, 64, 96, 128, 160, 192, 256)] + [(64, D) for D in (64, 128, 192, 256)]
+
+
 @pytest.mark.parametrize("bits", [2, 4])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("D", [32, 64, 96, 128, 160, 192, 256])
-def test_quant_keys_bitexact(bits, dtype, D):
-    rng = np.random.default_rng(100 + bits + D)
-    S, T = 3, 160
-    kcfg, ocfg = configs(bits, dtype, 1, 1, D)
+@pytest.mark.parametrize("G,D", GD_KEYS)
+def test_quant_keys_bitexact(bits, dtype, G, D):
+    rng = np.random.default_rng(100 + bits + D + G)
+    S, T = 3, 5 * G
+    kcfg, ocfg = configs(bits, dtype, 1, 1, D, G=G)
     xb = structured(rng, S, T, D, dtype)
-    xb[1, 32:64, :] = xb[1, 32, :]          # a group of identical tokens: every channel constant
+    xb[1, G:2 * G, :] = xb[1, G, :]         # a group of identical tokens: every channel constant
     codes, scale, zero = kivi.quant_keys(kcfg, dev_tensor(xb, dtype))
     rc, rs, rz = oracle.quant_keys(ocfg, xb)
     np.testing.assert_array_equal(codes.cpu().numpy(), rc)
@@ -40,11 +44,13 @@ def test_quant_keys_bitexact(bits, dtype, D):
 
 @pytest.mark.parametrize("bits", [2, 4])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("D,T", [(32, 1), (64, 45), (96, 70), (128, 97), (192, 32), (224, 5), (256, 33)])
-def test_quant_values_bitexact(bits, dtype, D, T):
-    rng = np.random.default_rng(200 + bits + D)
+@pytest.mark.parametrize("G,D,T", [(32, 32, 1), (32, 64, 45), (32, 96, 70), (32, 128, 97), (32, 192, 32),
+                                   (32, 224, 5), (32, 256, 33), (64, 64, 3), (64, 128, 97), (64, 192, 40),
+                                   (64, 256, 65)])
+def test_quant_values_bitexact(bits, dtype, G, D, T):
+    rng = np.random.default_rng(200 + bits + D + G)
     S = 4
-    kcfg, ocfg = configs(bits, dtype, 1, 1, D)
+    kcfg, ocfg = configs(bits, dtype, 1, 1, D, G=G)
     xb = structured(rng, S, max(T, 6), D, dtype)[:, :T].copy()
     codes, scale, zero = kivi.quant_values(kcfg, dev_tensor(xb, dtype))
     rc, rs, rz = oracle.quant_values(ocfg, xb)
@@ -84,13 +90,14 @@ def test_empty_inputs_are_noops():
 
 @pytest.mark.parametrize("bits", [2, 4])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_exact_ties_take_the_exact_division(bits, dtype):
+@pytest.mark.parametrize("G", [32, 64])
+def test_exact_ties_take_the_exact_division(bits, dtype, G):
     """Values exactly half-way between two grid points (x = z + (c + 1/2) s) must round
     half to even like the oracle: the kernels divide exactly near such ties."""
-    rng = np.random.default_rng(400 + bits)
-    S, T, D, G = 2, 64, 128, 32
+    rng = np.random.default_rng(400 + bits + G)
+    S, T, D = 2, 2 * G, 128
     qmax = (1 << bits) - 1
-    kcfg, ocfg = configs(bits, dtype, 1, 1, D)
+    kcfg, ocfg = configs(bits, dtype, 1, 1, D, G=G)
     s = np.ldexp(1.0, rng.integers(-4, 2, size=(S, T // G, D)))
     z = rng.integers(-20, 20, size=s.shape) * s
     c = rng.integers(0, qmax, size=(S, T, D)) + 0.5 * (rng.random((S, T, D)) < 0.5)
@@ -112,18 +119,18 @@ def test_exact_ties_take_the_exact_division(bits, dtype):
 
 @pytest.mark.parametrize("bits", [2, 4])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("D", [32, 64, 96, 128, 192, 256])
-def test_signed_zero_extremes_bitexact(bits, dtype, D):
+@pytest.mark.parametrize("G,D", [(32, 32), (32, 64), (32, 96), (32, 128), (32, 192), (32, 256), (64, 64), (64, 128)])
+def test_signed_zero_extremes_bitexact(bits, dtype, G, D):
     """Groups whose minimum or maximum is a zero of either sign, at every channel-slice
     width: the stored zero must follow the first zero seen, like the oracle."""
-    rng = np.random.default_rng(500 + bits + D)
-    S, T = 2, 96
-    kcfg, ocfg = configs(bits, dtype, 1, 1, D)
+    rng = np.random.default_rng(500 + bits + D + G)
+    S, T = 2, 3 * G
+    kcfg, ocfg = configs(bits, dtype, 1, 1, D, G=G)
     x = np.abs(rng.standard_normal((S, T, D))) + 0.25
-    x[:, 32:64] *= -1.0                                         # middle group: maximum is a zero
+    x[:, G:2 * G] *= -1.0                                       # middle group: maximum is a zero
     zeros = rng.random((S, T, D)) < 0.15
     x[zeros] = np.where(rng.random(zeros.sum()) < 0.5, 0.0, -0.0)
-    x[1, 64:96, : D // 2] = np.where(rng.random((32, D // 2)) < 0.5, 0.0, -0.0)   # all-zero groups
+    x[1, 2 * G:, : D // 2] = np.where(rng.random((G, D // 2)) < 0.5, 0.0, -0.0)   # all-zero groups
     xb = to_dtype_bits(x, dtype)
     assert np.any(xb == 0x8000)
     codes, scale, zero = kivi.quant_keys(kcfg, dev_tensor(xb, dtype))
@@ -140,15 +147,16 @@ def test_signed_zero_extremes_bitexact(bits, dtype, D):
 
 @pytest.mark.parametrize("bits", [2, 4])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_tiny_magnitudes_bitexact(bits, dtype):
+@pytest.mark.parametrize("G", [32, 64])
+def test_tiny_magnitudes_bitexact(bits, dtype, G):
     """Groups whose scale falls in the fp16 subnormal range (and, for bf16, whose
     minimum does too): the rounded scale and zero can push a group's end codes past
     0 or qmax before the clamp, which the kernels must handle like the oracle."""
-    rng = np.random.default_rng(600 + bits)
-    S, T, D = 3, 64, 128
-    kcfg, ocfg = configs(bits, dtype, 1, 1, D)
-    mag = 10.0 ** rng.uniform(-8.5, -4.0, size=(S, T // 32, 1, D))
-    x = (rng.standard_normal((S, T // 32, 32, D)) * mag).reshape(S, T, D)
+    rng = np.random.default_rng(600 + bits + G)
+    S, T, D = 3, 2 * G, 128
+    kcfg, ocfg = configs(bits, dtype, 1, 1, D, G=G)
+    mag = 10.0 ** rng.uniform(-8.5, -4.0, size=(S, T // G, 1, D))
+    x = (rng.standard_normal((S, T // G, G, D)) * mag).reshape(S, T, D)
     x[0] += 3e-6                                                    # offset groups: z rounds coarsely
     xb = to_dtype_bits(x, dtype)
     codes, scale, zero = kivi.quant_keys(kcfg, dev_tensor(xb, dtype))
@@ -156,7 +164,7 @@ def test_tiny_magnitudes_bitexact(bits, dtype):
     np.testing.assert_array_equal(host_bits(scale), rs)
     np.testing.assert_array_equal(host_bits(zero), rz)
     np.testing.assert_array_equal(codes.cpu().numpy(), rc)
-    xv = np.swapaxes(x.reshape(S, T // 32, 32, D), 2, 3).reshape(S, T, D)   # the same groups along channels
+    xv = np.swapaxes(x.reshape(S, T // G, G, D), 2, 3).reshape(S, T, D)   # the same groups along channels
     xvb = to_dtype_bits(xv, dtype)
     codes, scale, zero = kivi.quant_values(kcfg, dev_tensor(xvb, dtype))
     rc, rs, rz = oracle.quant_values(ocfg, xvb)

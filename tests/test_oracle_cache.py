@@ -30,7 +30,8 @@ def _rand_kv(rng, H, n, D, dtype="f16"):
 
 
 # (k_bits, v_bits, G, R): the default setting, the config example of "KV-Cache
-# Quantization: I Ran the Experiments So You Don't Have To" (G = R = 64), and mixed widths
+# Quantization: I Ran the Experiments So You Don't Have To", section "Component 4"
+# (G = R = 64), and mixed widths
 VARIANTS = [(2, 2, 32, 128), (4, 4, 32, 128), (2, 2, 64, 64), (4, 2, 32, 64), (2, 4, 64, 128)]
 
 
