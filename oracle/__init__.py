@@ -91,6 +91,9 @@ def lib():
             L.orc_decode_seq.argtypes = [ctypes.POINTER(_Cfg), ctypes.POINTER(_Seq), ctypes.c_int64, P,
                                          ctypes.c_double, P, ctypes.c_int, ctypes.c_int]
             L.orc_decode_seq.restype = None
+            L.orc_decode_multi_seq.argtypes = [ctypes.POINTER(_Cfg), ctypes.POINTER(_Seq), ctypes.c_int64,
+                                               ctypes.c_int, P, ctypes.c_double, P]
+            L.orc_decode_multi_seq.restype = ctypes.c_int
             L.orc_n_packed.argtypes = [ctypes.POINTER(_Cfg), ctypes.c_int64]
             L.orc_n_packed.restype = ctypes.c_int64
             L.orc_kv_bytes_plain.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
@@ -255,6 +258,18 @@ class SeqCache:
         nhq = Hq - hq0 if nhq is None else nhq
         out = np.full((Hq, self.cfg.head_dim), np.nan, np.float64)
         lib().orc_decode_seq(self.cfg.c(), self._c(), self.L, _p(q), float(scale), _p(out), hq0, nhq)
+        return out
+
+    def decode_multi(self, q_bits: np.ndarray, scale: float) -> np.ndarray:
+        """q_bits [n_query][Hq][D]: the n_query newest tokens' queries, query i attending causally
+        to positions [0, L - n_query + i] -> out [n_query][Hq][D] fp64."""
+        q = _u16(q_bits)
+        nq = q.shape[0]
+        assert q.shape[1:] == (self.cfg.num_q_heads, self.cfg.head_dim)
+        out = np.full(q.shape, np.nan, np.float64)
+        rc = lib().orc_decode_multi_seq(self.cfg.c(), self._c(), self.L, nq, _p(q), float(scale), _p(out))
+        if rc != OK:
+            raise ValueError(f"orc_decode_multi_seq: status {rc}")
         return out
 
 

@@ -397,14 +397,17 @@ static void token_kv(const orc_cfg* cfg, const orc_seq* s, int h, int64_t p, int
 }
 
 /*
- * Decode attention of one sequence holding L tokens, for the query heads
- * [hq0, hq0 + nhq): out[hq][d] = sum_t softmax_t(scale * q.k_t) v_t[d].
+ * Attention of one query over the first Lvis tokens of a sequence that holds
+ * L >= Lvis tokens, for the query heads [hq0, hq0 + nhq):
+ *   out[hq][d] = sum_{t < Lvis} softmax_t(scale * q.k_t) v_t[d]
+ * Tokens are read as the cache holds them at length L (packed below
+ * n_packed(L), residual above). Lvis == L is decode attention.
  *   q   [Hq][D] dtype bit patterns
  *   out [Hq][D] fp64 (rows outside [hq0, hq0+nhq) untouched)
- * L == 0 gives zeros.
+ * Lvis == 0 gives zeros.
  */
-void orc_decode_seq(const orc_cfg* cfg, const orc_seq* s, int64_t L, const uint16_t* q,
-                    double scale, double* out, int hq0, int nhq) {
+static void attend_prefix(const orc_cfg* cfg, const orc_seq* s, int64_t L, int64_t Lvis, const uint16_t* q,
+                          double scale, double* out, int hq0, int nhq) {
     const int D = cfg->head_dim, Hq = cfg->num_q_heads, H = cfg->num_kv_heads;
     const int g = Hq / H;
     const int64_t n_packed = orc_n_packed(cfg, L);
@@ -414,10 +417,10 @@ void orc_decode_seq(const orc_cfg* cfg, const orc_seq* s, int64_t L, const uint1
         double* qd = (double*)malloc(sizeof(double) * D);
         double* k = (double*)malloc(sizeof(double) * D);
         double* v = (double*)malloc(sizeof(double) * D);
-        double* score = (double*)malloc(sizeof(double) * (L > 0 ? L : 1));
+        double* score = (double*)malloc(sizeof(double) * (Lvis > 0 ? Lvis : 1));
         for (int d = 0; d < D; ++d) qd[d] = (double)widen(q[(int64_t)hq * D + d], cfg->dtype);
         double m = -INFINITY;
-        for (int64_t p = 0; p < L; ++p) {
+        for (int64_t p = 0; p < Lvis; ++p) {
             token_kv(cfg, s, h, p, n_packed, k, v);
             double acc = 0.0;
             for (int d = 0; d < D; ++d) acc += qd[d] * k[d];
@@ -426,16 +429,40 @@ void orc_decode_seq(const orc_cfg* cfg, const orc_seq* s, int64_t L, const uint1
         }
         double denom = 0.0;
         for (int d = 0; d < D; ++d) out[(int64_t)hq * D + d] = 0.0;
-        for (int64_t p = 0; p < L; ++p) {
+        for (int64_t p = 0; p < Lvis; ++p) {
             token_kv(cfg, s, h, p, n_packed, k, v);
             double w = exp(score[p] - m);
             denom += w;
             for (int d = 0; d < D; ++d) out[(int64_t)hq * D + d] += w * v[d];
         }
-        if (L > 0)
+        if (Lvis > 0)
             for (int d = 0; d < D; ++d) out[(int64_t)hq * D + d] /= denom;
         free(qd); free(k); free(v); free(score);
     }
+}
+
+/* Decode attention of one sequence holding L tokens: every query head attends to
+ * all L tokens (no mask; the query is the newest token). */
+void orc_decode_seq(const orc_cfg* cfg, const orc_seq* s, int64_t L, const uint16_t* q,
+                    double scale, double* out, int hq0, int nhq) {
+    attend_prefix(cfg, s, L, L, q, scale, out, hq0, nhq);
+}
+
+/*
+ * Attention of the n_query newest tokens of one sequence holding L >= n_query
+ * tokens (speculative verification, chunked prefill): query i sits at position
+ * L - n_query + i and attends causally to positions [0, L - n_query + i].
+ *   q   [n_query][Hq][D] dtype bit patterns
+ *   out [n_query][Hq][D] fp64
+ * Returns ORC_ERR_ARG when n_query < 1 or L < n_query.
+ */
+int orc_decode_multi_seq(const orc_cfg* cfg, const orc_seq* s, int64_t L, int n_query, const uint16_t* q,
+                         double scale, double* out) {
+    const int64_t row = (int64_t)cfg->num_q_heads * cfg->head_dim;
+    if (n_query < 1 || L < n_query) return ORC_ERR_ARG;
+    for (int i = 0; i < n_query; ++i)
+        attend_prefix(cfg, s, L, L - n_query + 1 + i, q + i * row, scale, out + i * row, 0, cfg->num_q_heads);
+    return ORC_OK;
 }
 
 /* ------------------------------------------------------------------ */

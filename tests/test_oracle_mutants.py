@@ -15,7 +15,7 @@ import oracle
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(os.path.dirname(HERE), "oracle", "kivi_oracle.c")
-PINS = ["tests/test_oracle_codec.py", "tests/test_oracle_cache.py"]
+PINS = ["tests/test_oracle_codec.py", "tests/test_oracle_cache.py", "tests/test_oracle_multi.py"]
 
 MUTANTS = {
     # packing: bits of a byte filled from the top instead of the bottom
@@ -39,6 +39,10 @@ MUTANTS = {
                     "const int kq = (1 << kb) - 1, vq = (1 << kb) - 1, ring = R + G;"),
     # dequantized keys read at the value width
     "key_read_width": ("k[d] = (double)get_code(kr, d, kb)", "k[d] = (double)get_code(kr, d, vb)"),
+    # multi-query: a query does not see its own token
+    "causal_excludes_self": ("attend_prefix(cfg, s, L, L - n_query + 1 + i,", "attend_prefix(cfg, s, L, L - n_query + i,"),
+    # multi-query: no causal mask
+    "no_causal_mask": ("attend_prefix(cfg, s, L, L - n_query + 1 + i,", "attend_prefix(cfg, s, L, L + 0 * i,"),
     # value metadata indexed with 32-channel groups whatever G is
     "value_group_fixed": ("int64_t mv = ((int64_t)h * cap + p) * (D / G) + d / G;",
                           "int64_t mv = ((int64_t)h * cap + p) * (D / G) + d / 32 % (D / G);"),
