@@ -329,6 +329,101 @@ def run_gpu(args, rank, world, local_rank):
     return res, wl
 
 
+def run_gpu_multi(args, rank, world, local_rank):
+    """Verification steps (--n-query N): each step appends N tokens per sequence (the draft
+    tokens of a speculative decoder) and runs kivi_decode_multi_attn for their N queries,
+    each attending causally to the cache. Returns the JSON line's fields."""
+    import torch
+    import synth
+    import bit_asymmetric_kv_kivi_gb300 as kivi
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    wl = workload_spec(args)
+    B, Hq, H, D, N = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, args.n_query
+    kb, vb = kv_bits(args, wl)
+    G = wl.group
+    L0s = list(wl.lengths)
+    n_steps = args.warmup + args.steps
+    max_len = max(L0s) + n_steps * N
+    cap = ((max_len + G - 1) // G) * G
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
+    cfg = kivi.Config(k_bits=kb, v_bits=vb, group=G, residual=wl.residual, head_dim=D, num_q_heads=Hq,
+                      num_kv_heads=H, dtype=kivi.BF16 if wl.dtype == "bf16" else kivi.F16)
+    cache = kivi.KVCache(cfg, B, cap, device, paged=args.paged, page_seed=1)
+    ks, vs = zip(*(gen_sequence_kv(wl, b, L0s[b], device) for b in range(B)))
+    cache.append(list(ks), list(vs))
+    del ks, vs
+    # each step's N new tokens per sequence, contiguous [Hkv][N][D], and its queries [B][N][Hq][D]
+    kst, vst = [], []
+    for b in range(B):
+        kall = torch.stack([synth.torch_kv_head_major(wl, b, h, L0s[b], n_steps * N, "k", device) for h in range(H)])
+        vall = torch.stack([synth.torch_kv_head_major(wl, b, h, L0s[b], n_steps * N, "v", device) for h in range(H)])
+        kst.append([kall[:, s * N:(s + 1) * N].contiguous() for s in range(n_steps)])
+        vst.append([vall[:, s * N:(s + 1) * N].contiguous() for s in range(n_steps)])
+    kptr = [torch.tensor([kst[b][s].data_ptr() for b in range(B)], dtype=torch.int64, device=device)
+            for s in range(n_steps)]
+    vptr = [torch.tensor([vst[b][s].data_ptr() for b in range(B)], dtype=torch.int64, device=device)
+            for s in range(n_steps)]
+    q = [torch.from_numpy(np.stack([wl.query(s * N + i) for i in range(N)], axis=1).view(np.int16)).view(tdt).to(device)
+         for s in range(n_steps)]
+    nn = torch.full((B,), N, dtype=torch.int32, device=device)
+    out = torch.empty((B, N, Hq, D), dtype=torch.float32, device=device)
+    cache.decode_multi(q[0], out, wl.softmax_scale, max_kv_len=max_len)    # sizes the workspace
+    stream = torch.cuda.current_stream(device)
+    cache_bytes = attn_bytes(wl, L0s, kb, vb)
+    flush = cache_bytes < 256 << 20
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=device) if flush else None
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+
+    def step(s, e=None):
+        if e is not None:
+            e[0].record(stream)
+        cache.append_ptrs(kptr[s], vptr[s], nn, N)
+        if e is not None:
+            e[1].record(stream)
+        cache.decode_multi(q[s], out, wl.softmax_scale, max_kv_len=max_len)
+        if e is not None:
+            e[2].record(stream)
+
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize()
+    with ClockSampler(smi_id(device)) as clk:
+        for i in range(args.steps):
+            if flush:
+                flush_buf.zero_()
+            step(args.warmup + i, ev[i])
+        torch.cuda.synchronize()
+    assert int(cache.status.item()) == 0, cache.status.item()
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    lens = [[L + (args.warmup + i + 1) * N for L in L0s] for i in range(args.steps)]
+    pairs = [sum(N * L - N * (N - 1) // 2 for L in ls) for ls in lens]      # (query, visible token) pairs
+    nbytes = [attn_bytes(wl, ls, kb, vb) for ls in lens]
+    total_ms = sum(step_ms)
+    value = sum(pairs) * world / (total_ms / 1e3)
+    avg_ms = sum(attn_ms) / len(attn_ms)
+    achieved = sum(nbytes) / len(nbytes) / (avg_ms / 1e3) / 1e9
+    peak, peak_kind = measured_hbm_peak()
+    return {
+        "metric": f"verification step ({N} queries per sequence): query x KV-token pairs/s", "value": value,
+        "unit": "query-KV-pairs/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD_NAMES[args.workload]} with {N} draft tokens appended and verified per step: "
+                               f"{B} sequences from {L0s[0]} tokens, {Hq} query / {H} kv heads, {kb}/{vb}-bit K/V, "
+                               f"G={G}, R={wl.residual}, {wl.dtype}", "n_query": N,
+                   "l2": "flushed before every step" if flush else "no flush: the cache is larger than L2",
+                   "layout": "paged" if args.paged else "contiguous"},
+        "roofline": {"bound": "hbm", "kernel": "decode_multi_kernel", "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "avg_launch_ms": avg_ms,
+                     "algorithmic_bytes_per_launch": sum(nbytes) / len(nbytes), "traffic": None},
+        "attn_pairs_per_s": sum(pairs) / (sum(attn_ms) / 1e3),
+        "gpu_launches": 4 * args.steps, "clocks": clk.summary(),
+    }
+
+
 def run_e2e(args, cache, wl, device, L_start, max_len, out_dev):
     """Same step, with the step's inputs copied host -> device from pinned memory and the
     attention output copied back, inside the timed region."""
@@ -416,6 +511,8 @@ def main():
     ap.add_argument("--workload", type=int, default=2, choices=[0, 1, 2, 3, 4],
                     help="0 tiny, 1 Llama-2-7B MHA, 2 Llama-3-8B GQA (default), 3 streaming, 4 long varlen")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--n-query", type=int, default=0,
+                    help="time verification steps instead: append N tokens per sequence, then multi-query attention")
     ap.add_argument("--paged", action="store_true",
                     help="packed cache in shared G-token pages behind block tables (random page order)")
     args = ap.parse_args()
@@ -459,6 +556,13 @@ def main():
     import torch
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if args.n_query:
+        line = run_gpu_multi(args, rank, world, local_rank)
+        if rank == 0:
+            print(json.dumps(line))
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
     res, wl = run_gpu(args, rank, world, local_rank)
 
     dev = torch.device("cuda", local_rank)

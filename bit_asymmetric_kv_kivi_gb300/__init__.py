@@ -70,6 +70,11 @@ def lib() -> ctypes.CDLL:
             L.kivi_decode_attn.restype = I32
             L.kivi_decode_workspace_bytes.argtypes = [CFG, I32, I32]
             L.kivi_decode_workspace_bytes.restype = ctypes.c_size_t
+            L.kivi_decode_multi_attn.argtypes = [CFG, I32, P, P, I32, P, P, ctypes.c_float, I32, P, ctypes.c_size_t,
+                                                 P, P]
+            L.kivi_decode_multi_attn.restype = I32
+            L.kivi_decode_multi_workspace_bytes.argtypes = [CFG, I32, I32, I32]
+            L.kivi_decode_multi_workspace_bytes.restype = ctypes.c_size_t
             L.kivi_seq_buffer_bytes.argtypes = [CFG, I32, ctypes.POINTER(ctypes.c_size_t)]
             L.kivi_seq_buffer_bytes.restype = I32
             L.kivi_seq_bytes.argtypes = [CFG, I32]
@@ -163,6 +168,9 @@ class Config:
 
     def decode_workspace_bytes(self, nseq: int, max_kv_len: int) -> int:
         return int(lib().kivi_decode_workspace_bytes(self.c(), nseq, max_kv_len))
+
+    def decode_multi_workspace_bytes(self, nseq: int, n_query: int, max_kv_len: int) -> int:
+        return int(lib().kivi_decode_multi_workspace_bytes(self.c(), nseq, n_query, max_kv_len))
 
 
 # ---------------------------------------------------------------- codec
@@ -297,6 +305,27 @@ class KVCache:
         _check(lib().kivi_decode_attn(cfg.c(), self.nseq, _ptr(self.seqs), _ptr(self.kv_len), _ptr(q), _ptr(out),
                                       float(scale), int(mkl), _ptr(ws), ws.numel(), _ptr(self.status),
                                       _stream(self.device)), "kivi_decode_attn")
+        return out
+
+    def decode_multi(self, q: torch.Tensor, out: torch.Tensor | None = None, softmax_scale: float | None = None,
+                     max_kv_len: int | None = None) -> torch.Tensor:
+        """Multi-query attention of each sequence's n_query newest tokens (already appended),
+        query i attending causally to positions [0, kv_len - n_query + i].
+        q [nseq][n_query][Hq][D] (cfg dtype) -> out [nseq][n_query][Hq][D] fp32."""
+        _require_cuda(q, "q")
+        cfg = self.cfg
+        nq = int(q.shape[1])
+        if out is None:
+            out = torch.empty((self.nseq, nq, cfg.num_q_heads, cfg.head_dim), dtype=torch.float32, device=q.device)
+        scale = 1.0 / cfg.head_dim ** 0.5 if softmax_scale is None else softmax_scale
+        mkl = self.max_len if max_kv_len is None else max_kv_len
+        need = cfg.decode_multi_workspace_bytes(self.nseq, nq, mkl)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=self.device)
+        ws = self._ws
+        _check(lib().kivi_decode_multi_attn(cfg.c(), self.nseq, _ptr(self.seqs), _ptr(self.kv_len), nq, _ptr(q),
+                                            _ptr(out), float(scale), int(mkl), _ptr(ws), ws.numel(),
+                                            _ptr(self.status), _stream(self.device)), "kivi_decode_multi_attn")
         return out
 
     # -------------------------------------------------------------- inspection

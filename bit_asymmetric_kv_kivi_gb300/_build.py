@@ -18,7 +18,8 @@ OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libkivi.so")
 OBJ_DIR = os.path.join(PKG, "_build")
 SOURCES = ["kivi_abi.cu", "kivi_codec.cu", "kivi_decode.cu", "kivi_decode_k2v2.cu", "kivi_decode_k2v4.cu",
-           "kivi_decode_k4v2.cu", "kivi_decode_k4v4.cu", "kivi_noalloc.cu"]
+           "kivi_decode_k4v2.cu", "kivi_decode_k4v4.cu", "kivi_multi_k2v2.cu", "kivi_multi_k2v4.cu",
+           "kivi_multi_k4v2.cu", "kivi_multi_k4v4.cu", "kivi_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++20", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
               "--expt-relaxed-constexpr", f"-I{ROOT}/include"]

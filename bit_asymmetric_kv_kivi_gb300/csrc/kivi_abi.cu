@@ -130,6 +130,7 @@ kivi_status kivi_decode_attn(const kivi_cfg* cfg, int32_t nseq, const kivi_seq* 
     a.dtype = cfg->dtype;
     a.nseq = nseq;
     a.max_kv_len = max_kv_len;
+    a.n_query = 1;
     a.seqs = seqs_dev;
     a.kv_len = kv_len_dev;
     a.q = q_dev;
@@ -139,6 +140,53 @@ kivi_status kivi_decode_attn(const kivi_cfg* cfg, int32_t nseq, const kivi_seq* 
     a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace_dev) + cb);
     a.status = status_dev;
     return from_cuda(kivi::launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t kivi_decode_multi_workspace_bytes(const kivi_cfg* cfg, int32_t nseq, int32_t n_query, int32_t max_kv_len) {
+    if (!cfg_ok(cfg) || nseq < 0 || max_kv_len < 0 || n_query < 1) return 0;
+    int chunk, max_splits;
+    size_t cb, pb;
+    kivi::multi_plan(nseq, cfg->num_kv_heads, cfg->num_q_heads, cfg->head_dim, n_query, max_kv_len, &chunk,
+                     &max_splits, &cb, &pb);
+    return cb + pb;
+}
+
+kivi_status kivi_decode_multi_attn(const kivi_cfg* cfg, int32_t nseq, const kivi_seq* seqs_dev,
+                                   const int32_t* kv_len_dev, int32_t n_query, const void* q_dev, float* out_dev,
+                                   float softmax_scale, int32_t max_kv_len, void* workspace_dev,
+                                   size_t workspace_bytes, int32_t* status_dev, void* stream) {
+    if (!cfg_ok(cfg)) return KIVI_ERR_ARG;
+    if (nseq < 0 || nseq > 65535 || max_kv_len < 0 || n_query < 1 || !isfinite(softmax_scale)) return KIVI_ERR_ARG;
+    const int g = cfg->num_q_heads / cfg->num_kv_heads;
+    if (cfg->head_dim != 128 || static_cast<int64_t>(n_query) * g > 32) return KIVI_ERR_UNSUPPORTED;
+    if (nseq == 0) return KIVI_OK;
+    if (seqs_dev == nullptr || kv_len_dev == nullptr || q_dev == nullptr || out_dev == nullptr)
+        return KIVI_ERR_ARG;
+    kivi::DecodeArgs a;
+    size_t cb, pb;
+    kivi::multi_plan(nseq, cfg->num_kv_heads, cfg->num_q_heads, cfg->head_dim, n_query, max_kv_len, &a.chunk,
+                     &a.max_splits, &cb, &pb);
+    if (workspace_dev == nullptr || workspace_bytes < cb + pb) return KIVI_ERR_WORKSPACE;
+    a.kb = cfg->k_bits;
+    a.vb = cfg->v_bits;
+    a.G = cfg->group;
+    a.D = cfg->head_dim;
+    a.R = cfg->residual;
+    a.Hq = cfg->num_q_heads;
+    a.H = cfg->num_kv_heads;
+    a.dtype = cfg->dtype;
+    a.nseq = nseq;
+    a.max_kv_len = max_kv_len;
+    a.n_query = n_query;
+    a.seqs = seqs_dev;
+    a.kv_len = kv_len_dev;
+    a.q = q_dev;
+    a.out = out_dev;
+    a.scale_log2 = softmax_scale * 1.4426950408889634f;
+    a.counters = static_cast<int32_t*>(workspace_dev);
+    a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace_dev) + cb);
+    a.status = status_dev;
+    return from_cuda(kivi::launch_multi(a, static_cast<cudaStream_t>(stream)));
 }
 
 kivi_status kivi_seq_buffer_bytes(const kivi_cfg* cfg, int32_t cap_tokens, size_t bytes_out[8]) {

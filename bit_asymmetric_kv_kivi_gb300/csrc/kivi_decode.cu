@@ -34,4 +34,28 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     return a.vb == 2 ? launch_decode_k4v2(a, stream) : launch_decode_k4v4(a, stream);
 }
 
+// Multi-query attention: packed splits of a whole number of 32-token tiles, about an eighth
+// of the longest sequence in 256-token steps between 1024 and 4096 tokens, plus one split
+// for the residual window; one record of kD + 4 floats per (split, virtual head), the
+// virtual heads padded to whole warps of four.
+void multi_plan(int nseq, int H, int Hq, int D, int n_query, int max_kv_len, int* chunk, int* max_splits,
+                size_t* counter_bytes, size_t* partial_bytes) {
+    *counter_bytes = ((static_cast<size_t>(nseq) * H * sizeof(int32_t) + 255) / 256) * 256;
+    const int V = H > 0 ? n_query * (Hq / H) : 0;
+    const int w = V <= 4 ? 1 : V <= 8 ? 2 : V <= 16 ? 4 : 8;
+    const int64_t eighth = (static_cast<int64_t>(max_kv_len) + 7) / 8;
+    int64_t c = ((eighth + 255) / 256) * 256;
+    c = c < 1024 ? 1024 : (c > 4096 ? 4096 : c);
+    const int64_t ms = (max_kv_len <= 0 ? 0 : (max_kv_len + c - 1) / c) + 1;
+    *chunk = static_cast<int>(c);
+    *max_splits = static_cast<int>(ms);
+    *partial_bytes = static_cast<size_t>(nseq) * H * ms * (4 * w) * (D + 4) * sizeof(float);
+}
+
+cudaError_t launch_multi(const DecodeArgs& a, cudaStream_t stream) {
+    if (a.nseq == 0) return cudaSuccess;
+    if (a.kb == 2) return a.vb == 2 ? launch_multi_k2v2(a, stream) : launch_multi_k2v4(a, stream);
+    return a.vb == 2 ? launch_multi_k4v2(a, stream) : launch_multi_k4v4(a, stream);
+}
+
 }  // namespace kivi

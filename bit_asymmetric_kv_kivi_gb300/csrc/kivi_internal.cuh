@@ -160,6 +160,7 @@ cudaError_t launch_append_flush(const AppendArgs& a, cudaStream_t stream);
 struct DecodeArgs {
     int kb, vb, G, D, R, Hq, H, dtype;
     int nseq, max_kv_len;
+    int n_query;                    // queries per sequence (1 for decode; multi-query attention)
     int chunk, max_splits;          // tokens per split (multiple of 32), splits per sequence
     const kivi_seq* seqs;
     const int32_t* kv_len;
@@ -179,6 +180,15 @@ void decode_plan(int nseq, int H, int Hq, int D, int max_kv_len, int* chunk, int
                  size_t* counter_bytes, size_t* partial_bytes);
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// Multi-query attention (kivi_decode_multi_attn): split plan and workspace, and the launch.
+void multi_plan(int nseq, int H, int Hq, int D, int n_query, int max_kv_len, int* chunk, int* max_splits,
+                size_t* counter_bytes, size_t* partial_bytes);
+cudaError_t launch_multi(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_multi_k2v2(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_multi_k2v4(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_multi_k4v2(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_multi_k4v4(const DecodeArgs& a, cudaStream_t stream);
 // One per pair of key / value code widths, each in a translation unit of its own.
 cudaError_t launch_decode_k2v2(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_k2v4(const DecodeArgs& a, cudaStream_t stream);

@@ -226,6 +226,39 @@ kivi_status kivi_decode_attn(const kivi_cfg* cfg, int32_t nseq, const kivi_seq* 
 size_t kivi_decode_workspace_bytes(const kivi_cfg* cfg, int32_t nseq, int32_t max_kv_len);
 
 /*
+ * Multi-query attention over the packed cache: the n_query newest tokens of
+ * each sequence (already appended with kivi_append_flush) attend causally, as
+ * when a target model verifies n_query draft tokens (speculative decoding) or
+ * a prefill runs in chunks. The pages that describe KIVI show one query per
+ * step; this entry point reads the same cache the same way ("KIVI: Asymmetric
+ * 2-Bit KV Cache Quantization Guide", section "Step 2": dequantize during
+ * attention), with the causal mask as this library's reading.
+ *   out[b][i][hq][:] = sum_{t <= p_i} softmax_t(softmax_scale * q[b][i][hq] . k_t) v_t,
+ *   p_i = kv_len_b - n_query + i
+ * Query head hq reads kv head hq / (Hq / Hkv). Packed tokens are dequantized as
+ * c*s + z, residual tokens read as stored; every masked token lies in the
+ * residual window. fp32 accumulation and output.
+ *   q_dev      [nseq][n_query][Hq][D] dtype
+ *   out_dev    [nseq][n_query][Hq][D] fp32
+ *   n_query    queries per sequence, 1 <= n_query and n_query * Hq / Hkv <= 32
+ *   max_kv_len, workspace_dev, workspace_bytes, status_dev: as kivi_decode_attn, with
+ *              kivi_decode_multi_workspace_bytes() for the size
+ * Device error KIVI_ERR_LENGTH: kv_len_b < n_query, kv_len_b > max_kv_len or
+ * more tokens than the sequence can hold; that sequence's output rows are NaN.
+ * Errors: KIVI_ERR_ARG for n_query < 1; KIVI_ERR_UNSUPPORTED unless D == 128
+ * and n_query * Hq / Hkv <= 32.
+ */
+kivi_status kivi_decode_multi_attn(const kivi_cfg* cfg, int32_t nseq, const kivi_seq* seqs_dev,
+                                   const int32_t* kv_len_dev, int32_t n_query, const void* q_dev,
+                                   float* out_dev, float softmax_scale, int32_t max_kv_len,
+                                   void* workspace_dev, size_t workspace_bytes, int32_t* status_dev,
+                                   void* stream);
+
+/* Workspace bytes kivi_decode_multi_attn needs; 0 on a bad config or n_query < 1. */
+size_t kivi_decode_multi_workspace_bytes(const kivi_cfg* cfg, int32_t nseq, int32_t n_query,
+                                         int32_t max_kv_len);
+
+/*
  * Decode attention that allocates nothing and takes no workspace argument.
  * The pages that describe KIVI have no counterpart of this entry point; it
  * exists for callers that cannot call cudaMalloc: processes whose device

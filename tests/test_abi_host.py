@@ -103,6 +103,22 @@ def test_bad_arguments_rejected_before_launch(lib):
     assert lib.kivi_decode_attn(cfg, 0, null, null, null, null, 0.1, 0, null, 0, null, None) == kivi.OK
 
 
+def test_multi_query_arguments_rejected_before_launch(lib):
+    cfg = kivi.Config(num_q_heads=8, num_kv_heads=2).c()
+    P = ctypes.c_void_p
+    one = P(16)
+    need = lib.kivi_decode_multi_workspace_bytes(cfg, 2, 4, 5000)
+    assert need > lib.kivi_decode_multi_workspace_bytes(cfg, 2, 1, 5000) > 0
+    assert lib.kivi_decode_multi_workspace_bytes(cfg, 2, 0, 5000) == 0
+    call = lambda nq, ws=need: lib.kivi_decode_multi_attn(cfg, 2, one, one, nq, one, one, 0.1, 5000, one, ws, one, None)
+    assert call(0) == kivi.ERR_ARG
+    assert call(9) == kivi.ERR_UNSUPPORTED          # 9 queries x group 4 > 32 (query, head) pairs
+    assert call(4, need - 1) == kivi.ERR_WORKSPACE
+    assert lib.kivi_decode_multi_attn(kivi.Config(head_dim=64).c(), 1, one, one, 1, one, one, 0.1, 10, one, 1 << 20,
+                                      one, None) == kivi.ERR_UNSUPPORTED
+    assert lib.kivi_decode_multi_attn(cfg, 0, None, None, 4, None, None, 0.1, 0, None, 0, None, None) == kivi.OK
+
+
 def test_cfg_struct_matches_header(tmp_path):
     """The binding's kivi_cfg fields: same size and offsets as the C struct."""
     import subprocess

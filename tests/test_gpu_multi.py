@@ -1,0 +1,140 @@
+"""GPU parity of kivi_decode_multi_attn (the n_query newest tokens of each sequence
+attending causally to the packed cache) against the oracle's fp64 multi-query
+attention: max |out - oracle| <= 2e-3 over every output element, for both code widths
+and their mix, G = 32 and 64, query groups 1/2/4/8 and n_query from 1 to 32 / group,
+at the edge lengths of the packed / residual split; the paged layout equal to the
+contiguous one bit for bit; short sequences and bad lengths."""
+import numpy as np
+import pytest
+import torch
+
+import bit_asymmetric_kv_kivi_gb300 as kivi
+import oracle
+import synth
+from gpu_util import ATTN_TOL, configs, dev_tensor, record_error
+
+pytestmark = pytest.mark.gpu
+
+
+def build(wl, kcfg, ocfg, cap, paged=False):
+    cache = kivi.KVCache(kcfg, wl.batch, cap, paged=paged, page_seed=3, spare_pages=2)
+    refs, ks, vs = [], [], []
+    for b, L in enumerate(wl.lengths):
+        K, V = wl.kv_seq(b, 0, L)
+        ks.append(dev_tensor(K, wl.dtype))
+        vs.append(dev_tensor(V, wl.dtype))
+        r = oracle.SeqCache(ocfg, cap)
+        assert r.append(K, V) == oracle.OK
+        refs.append(r)
+    cache.append(ks, vs)
+    return cache, refs
+
+
+def queries(wl, nq, step=0):
+    """[nseq][nq][Hq][D] bit patterns: the queries of the nq newest tokens."""
+    return np.stack([np.stack([wl.query(step + i, b) for i in range(nq)]) for b in range(wl.batch)])
+
+
+def check(wl, cache, refs, nq, step=0):
+    qb = queries(wl, nq, step)
+    out = cache.decode_multi(dev_tensor(qb, wl.dtype), softmax_scale=wl.softmax_scale).cpu().numpy()
+    assert int(cache.status.item()) == 0
+    worst = 0.0
+    for b, r in enumerate(refs):
+        want = r.decode_multi(qb[b], wl.softmax_scale)
+        worst = max(worst, float(np.max(np.abs(out[b] - want))))
+    record_error(worst)
+    assert worst <= ATTN_TOL, worst
+    return out
+
+
+CASES = [  # (k_bits, v_bits, G, R, query group, n_query)
+    (2, 2, 32, 128, 4, 1), (2, 2, 32, 128, 4, 2), (2, 2, 32, 128, 4, 4), (2, 2, 32, 128, 4, 8),
+    (2, 2, 32, 128, 1, 3), (2, 2, 32, 128, 1, 16), (2, 2, 32, 128, 1, 32), (2, 2, 32, 128, 2, 5),
+    (2, 2, 32, 128, 8, 1), (2, 2, 32, 128, 8, 4), (4, 4, 32, 128, 4, 4), (4, 4, 32, 128, 8, 2),
+    (2, 2, 64, 64, 4, 4), (4, 2, 64, 64, 2, 7), (2, 4, 32, 64, 4, 8), (4, 2, 32, 128, 1, 12),
+    (2, 4, 64, 128, 8, 3), (4, 4, 64, 64, 1, 1),
+]
+
+
+@pytest.mark.parametrize("kb,vb,G,R,g,nq", CASES)
+def test_multi_query_edge_lengths(kb, vb, G, R, g, nq):
+    dtype = ("f16", "bf16")[(kb + vb + g + nq) % 2]
+    H = 2
+    base = {nq, nq + 1, 31, 32, 33, R - 1, R, R + 1, R + G - 1, R + G, R + G + 1, R + 2 * G + nq, 700, 1000 + G // 2}
+    lengths = tuple(sorted(L for L in base if L >= nq))
+    wl = synth.Workload("multi", len(lengths), g * H, H, 128, lengths, dtype, seed=300 + g + nq + G + kb)
+    kcfg, ocfg = configs(2, dtype, g * H, H, G=G, R=R, kb=kb, vb=vb)
+    cache, refs = build(wl, kcfg, ocfg, 1024)
+    check(wl, cache, refs, nq)
+
+
+@pytest.mark.parametrize("g,nq", [(4, 4), (8, 2), (1, 8)])
+def test_multi_query_long_sequences_many_splits(g, nq):
+    """Sequences long enough for several packed splits (1024..4096 tokens each), mixed
+    lengths in one batch."""
+    H = 2
+    lengths = (9000, 4099, 12345, 300)
+    wl = synth.Workload("multi-long", len(lengths), g * H, H, 128, lengths, "bf16", seed=400 + g)
+    kcfg, ocfg = configs(2, "bf16", g * H, H)
+    cache, refs = build(wl, kcfg, ocfg, 12352)
+    check(wl, cache, refs, nq)
+
+
+def test_multi_query_one_query_matches_decode():
+    """n_query = 1 is decode attention: both entry points agree with the oracle and
+    with each other."""
+    H, g = 2, 4
+    lengths = (1, 150, 1000, 5000)
+    wl = synth.Workload("multi-one", len(lengths), g * H, H, 128, lengths, "f16", seed=410)
+    kcfg, ocfg = configs(2, "f16", g * H, H)
+    cache, refs = build(wl, kcfg, ocfg, 5120)
+    out = check(wl, cache, refs, 1)
+    dec = cache.decode(dev_tensor(queries(wl, 1)[:, 0], "f16"), softmax_scale=wl.softmax_scale).cpu().numpy()
+    assert np.max(np.abs(out[:, 0] - dec)) <= 1e-4
+
+
+def test_multi_query_after_streaming_appends_and_paged_layout():
+    """Verification steps as a speculative decoder runs them: append n_query draft tokens,
+    verify them, repeat (with flushes in between); the paged cache gives the same output
+    bit for bit."""
+    H, g, nq = 2, 4, 4
+    lengths = (130, 300, 1000)
+    wl = synth.Workload("multi-stream", len(lengths), g * H, H, 128, lengths, "bf16", seed=420)
+    kcfg, ocfg = configs(2, "bf16", g * H, H)
+    cap = 1536
+    cont, refs = build(wl, kcfg, ocfg, cap)
+    paged, _ = build(wl, kcfg, ocfg, cap, paged=True)
+    pos = list(lengths)
+    for step in range(12):
+        kn, vn = [], []
+        for b in range(wl.batch):
+            K, V = wl.kv_seq(b, pos[b], nq)
+            kn.append(dev_tensor(K, "bf16"))
+            vn.append(dev_tensor(V, "bf16"))
+            assert refs[b].append(K, V) == oracle.OK
+            pos[b] += nq
+        cont.append(kn, vn)
+        paged.append(kn, vn)
+        oc = check(wl, cont, refs, nq, step=10 * step)
+        qb = dev_tensor(queries(wl, nq, 10 * step), "bf16")
+        op = paged.decode_multi(qb, softmax_scale=wl.softmax_scale).cpu().numpy()
+        assert np.array_equal(oc, op), step
+
+
+def test_multi_query_bad_lengths():
+    """kv_len below n_query: NaN rows and KIVI_ERR_LENGTH for that sequence only; n_query
+    * group above 32 is refused before launch."""
+    H, g, nq = 1, 4, 6
+    lengths = (5, 200)
+    wl = synth.Workload("multi-bad", len(lengths), g * H, H, 128, lengths, "f16", seed=430)
+    kcfg, ocfg = configs(2, "f16", g * H, H)
+    cache, refs = build(wl, kcfg, ocfg, 256)
+    qb = queries(wl, nq)
+    out = cache.decode_multi(dev_tensor(qb, "f16"), softmax_scale=wl.softmax_scale).cpu().numpy()
+    assert int(cache.status.item()) == kivi.ERR_LENGTH
+    assert np.all(np.isnan(out[0]))
+    want = refs[1].decode_multi(qb[1], wl.softmax_scale)
+    assert np.max(np.abs(out[1] - want)) <= ATTN_TOL
+    with pytest.raises(kivi.KiviError):
+        cache.decode_multi(dev_tensor(np.zeros((2, 9, 4, 128), np.uint16), "f16"))
