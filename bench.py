@@ -579,9 +579,10 @@ def main():
     avg_bytes = sum(res["attn_bytes"]) / len(res["attn_bytes"])
     achieved = avg_bytes / (avg_attn_ms / 1e3) / 1e9
     peak, peak_kind = measured_hbm_peak()
-    # the decode kernel the library picks: tensor-core path for query groups of 1, 2 or 4
+    # the decode kernel the library picks: persistent tensor-core kernel for query groups of 1, 2
+    # or 4, the multi-query kernel (one query) for 8
     group = config["q_heads"] // config["kv_heads"]
-    kernel = "decode_mma_kernel" if group in (1, 2, 4) else "decode_split_kernel"
+    kernel = "decode_mma_kernel" if group in (1, 2, 4) else "decode_multi_kernel"
     per_unit = None if args.paged else NCU_TRAFFIC_BYTES_PER_UNIT.get(
         (kernel, kb, vb, wl.group, wl.residual, group, config["input_dtype"]))
     traffic = per_unit * sum(res["attn_units"]) / len(res["attn_units"]) if per_unit else None

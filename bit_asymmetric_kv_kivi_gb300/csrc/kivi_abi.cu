@@ -130,7 +130,7 @@ kivi_status kivi_decode_attn(const kivi_cfg* cfg, int32_t nseq, const kivi_seq* 
     a.dtype = cfg->dtype;
     a.nseq = nseq;
     a.max_kv_len = max_kv_len;
-    a.n_query = 1;
+    a.n_query = 0;
     a.seqs = seqs_dev;
     a.kv_len = kv_len_dev;
     a.q = q_dev;

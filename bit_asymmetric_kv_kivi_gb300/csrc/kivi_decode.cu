@@ -16,20 +16,17 @@ void decode_plan(int nseq, int H, int Hq, int D, int max_kv_len, int* chunk, int
         *partial_bytes = (2 * static_cast<size_t>(nseq) * H + kDecodeMaxCtas) * gq * (D + 4) * sizeof(float);
         return;
     }
-    // decode_split_kernel: splits of about an eighth of the longest sequence, in whole
-    // 256-token steps between 2048 and 4096 tokens (below that the per-CTA setup and merge
-    // dominate); the residual tokens are read inside the splits.
-    const int64_t eighth = (static_cast<int64_t>(max_kv_len) + 7) / 8;
-    int64_t c = ((eighth + 255) / 256) * 256;
-    c = c < 2048 ? 2048 : (c > 4096 ? 4096 : c);
-    const int64_t ms = max_kv_len <= 0 ? 1 : (max_kv_len + c - 1) / c;
-    *chunk = static_cast<int>(c);
-    *max_splits = static_cast<int>(ms);
-    *partial_bytes = static_cast<size_t>(nseq) * Hq * ms * (D + 4) * sizeof(float);
+    // query group 8: decode_multi_kernel with one query per sequence
+    multi_plan(nseq, H, Hq, D, 1, max_kv_len, chunk, max_splits, counter_bytes, partial_bytes);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     if (a.nseq == 0) return cudaSuccess;
+    if (a.Hq == 8 * a.H) {
+        DecodeArgs m = a;
+        m.n_query = 0;     // decode: one query per sequence, empty sequences give zeros
+        return launch_multi(m, stream);
+    }
     if (a.kb == 2) return a.vb == 2 ? launch_decode_k2v2(a, stream) : launch_decode_k2v4(a, stream);
     return a.vb == 2 ? launch_decode_k4v2(a, stream) : launch_decode_k4v4(a, stream);
 }

@@ -9,8 +9,6 @@
 // in SRAM); "KIVI: A Tuning-Free Asymmetric 2bit Quantization for KV Cache",
 // abstract (decode is bound by loading the cache).
 //
-// Two kernels share the split bookkeeping:
-//
 //  * decode_mma_kernel (Hq/Hkv = 1, 2, 4): the dot products run on the tensor
 //    cores (mma.sync m16n8k16, f16 operands, fp32 accumulation). A CTA owns a
 //    range of 32-token tiles of the packed tokens of one (sequence, kv head)
@@ -28,11 +26,12 @@
 //        sum_t p z_v term is a small MMA of its own.
 //    q is rescaled by a power of two so that max|q| lies in (1/2, 1]; with
 //    |x| <= 65504 no f16 operand can overflow.
-//  * decode_split_kernel (any Hq/Hkv, used for 8): CUDA-core FMAs, lane = token.
+//  * Hq/Hkv = 8 runs on decode_multi_kernel (kivi_multi_impl.cuh) with one
+//    query: its CTAs share each unpacked tile between two warps of four heads.
 //
-// Every split writes (m, l, acc[128]) for its query heads to the workspace;
+// Every segment writes (m, l, acc[128]) for its query heads to the workspace;
 // the last CTA of a (sequence, kv head) to finish (an atomic ticket, no
-// waiting) merges the splits with the log-sum-exp rescaling and writes the
+// waiting) merges the records with the log-sum-exp rescaling and writes the
 // fp32 output.
 //
 // This header holds the kernels as templates over the key and value code widths
@@ -237,67 +236,6 @@ __device__ __forceinline__ void store_lane_state(int warp, int lane, const float
     }
 }
 
-// Merges the four warps' states of this split (red_* in shared memory, filled and
-// synchronized by the caller), then either writes the output (single split) or
-// the split's partial record; the last CTA of (b, h) to arrive merges all splits.
-template <int GQ>
-__device__ __forceinline__ void finish_split(const DecodeArgs& a, int b, int h, int split, int nsplit,
-                                             float* out_bh, const float* red_m, const float* red_l,
-                                             const float* red_acc, int* s_last) {
-    const int tid = threadIdx.x;
-    const int64_t rec_stride = kD + 4;
-    float* part_bh =
-        a.partials + (static_cast<int64_t>(b) * a.Hq + static_cast<int64_t>(h) * GQ) * a.max_splits * rec_stride;
-    for (int i = tid; i < GQ * kD; i += kThreads) {
-        const int hh = i / kD, d = i - hh * kD;
-        float M = -CUDART_INF_F;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w * GQ + hh]);
-        float den = 0.0f, num = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const float f = exp2f(red_m[w * GQ + hh] - M);
-            den = fmaf(red_l[w * GQ + hh], f, den);
-            num = fmaf(red_acc[(w * GQ + hh) * kD + d], f, num);
-        }
-        if (nsplit == 1) {
-            out_bh[i] = num / den;
-        } else {
-            float* rec = part_bh + (static_cast<int64_t>(hh) * a.max_splits + split) * rec_stride;
-            rec[d] = num;
-            if (d == 0) {
-                rec[kD] = M;
-                rec[kD + 1] = den;
-            }
-        }
-    }
-    if (nsplit == 1) return;
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const int ticket = atomicAdd(&a.counters[static_cast<int64_t>(b) * a.H + h], 1);
-        *s_last = ticket == nsplit - 1;
-    }
-    __syncthreads();
-    if (!*s_last) return;
-    __threadfence();
-    for (int i = tid; i < GQ * kD; i += kThreads) {
-        const int hh = i / kD, d = i - hh * kD;
-        const float* rec = part_bh + static_cast<int64_t>(hh) * a.max_splits * rec_stride;
-        float M = -CUDART_INF_F, den = 0.0f, num = 0.0f;
-        for (int s = 0; s < nsplit; ++s) {
-            const float ms = __ldcg(rec + s * rec_stride + kD);
-            const float Mn = fmaxf(M, ms);
-            const float fo = exp2f(M - Mn), fs = exp2f(ms - Mn);
-            den = den * fo + __ldcg(rec + s * rec_stride + kD + 1) * fs;
-            num = num * fo + __ldcg(rec + s * rec_stride + d) * fs;
-            M = Mn;
-        }
-        out_bh[i] = num / den;
-    }
-    if (tid == 0) a.counters[static_cast<int64_t>(b) * a.H + h] = 0;
-}
-
 // ---------------------------------------------------------------- persistent schedule
 
 // decode_mma_kernel runs one CTA per resident slot. The work of all (sequence, kv head)
@@ -420,151 +358,6 @@ __device__ __forceinline__ void finish_segment(const DecodeArgs& a, const Stream
         out_s[i] = num / scratch[-GQ + hh];
     }
     if (tid == 0) a.counters[ss.s] = 0;
-}
-
-// ---------------------------------------------------------------- CUDA-core kernel
-
-// Splits over [0, L) in chunks of a.chunk tokens; four warps take 32-token tiles
-// round-robin, lane = token. Key side per packed tile: q'[hq][d] = q[hq][d] * s_k[d]
-// and bias[hq] = sum_d q[hq][d] * z_k[d], so a token's score is bias + sum_d q'[d] c[d].
-template <int KB, int VB, int DT, int GQ, int G>
-__global__ void __launch_bounds__(kThreads) decode_split_kernel(DecodeArgs a) {
-    constexpr int kq = (1 << KB) - 1, vq = (1 << VB) - 1;
-    constexpr int kKWords = kD * KB / 32;         // 32-bit words per packed key row
-    constexpr int kVWords = kD * VB / 32;         // and value row
-    constexpr int kPerWord = 32 / KB;             // key codes per word
-    constexpr int kNg = kD / G;                   // value channel groups per token
-
-    __shared__ float qs[GQ * kD];                                 // q * scale * log2(e)
-    __shared__ float qk[kWarps][GQ][kD];                          // per warp: q' of the current key group
-    __shared__ uint32_t vcode[kWarps][kTile][kVWords];            // per warp: value code rows of the tile
-    __shared__ float vsc[kWarps][kTile][kNg], vzr[kWarps][kTile][kNg];
-    __shared__ float red_m[kWarps * GQ], red_l[kWarps * GQ];
-    __shared__ int s_last;
-
-    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int Hq = a.Hq, ring = a.R + G;
-    const kivi_seq& sq = a.seqs[b];
-    const int cap = sq.cap_tokens;
-    const int64_t L = a.kv_len[b];
-    float* out_bh = a.out + (static_cast<int64_t>(b) * Hq + static_cast<int64_t>(h) * GQ) * kD;
-
-    const bool bad = L < 0 || L > a.max_kv_len || n_packed(L, a.R, G) > cap;
-    if (bad || L == 0) {
-        if (split == 0) {
-            for (int i = tid; i < GQ * kD; i += kThreads) out_bh[i] = bad ? CUDART_NAN_F : 0.0f;
-            if (bad && h == 0 && tid == 0) set_status(a.status, KIVI_ERR_LENGTH);
-        }
-        return;
-    }
-    const int nsplit = static_cast<int>((L + a.chunk - 1) / a.chunk);
-    if (split >= nsplit) return;
-    const int64_t t0 = static_cast<int64_t>(split) * a.chunk;
-    const int64_t t1 = min(t0 + a.chunk, L);
-    const int64_t np = n_packed(L, a.R, G);
-
-    const uint16_t* q = static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(b) * Hq + h * GQ) * kD;
-    for (int i = tid; i < GQ * kD; i += kThreads) qs[i] = widen<DT>(q[i]) * a.scale_log2;
-    __syncthreads();
-
-    float m[GQ], l[GQ], acc[GQ][kCpl];
-#pragma unroll
-    for (int hh = 0; hh < GQ; ++hh) {
-        m[hh] = -CUDART_INF_F;
-        l[hh] = 0.0f;
-#pragma unroll
-        for (int c = 0; c < kCpl; ++c) acc[hh][c] = 0.0f;
-    }
-
-    const uint16_t* kres = static_cast<const uint16_t*>(sq.k_res) + static_cast<int64_t>(h) * ring * kD;
-    const uint16_t* vres = static_cast<const uint16_t*>(sq.v_res) + static_cast<int64_t>(h) * ring * kD;
-
-    for (int64_t ts = t0 + 32 * warp; ts < t1; ts += 32 * kWarps) {
-        if (ts >= np) {   // residual tile (np and ts are multiples of 32)
-            residual_tile<DT, GQ>(kres, vres, ring, ts, t1, qs, lane, m, l, acc);
-            __syncwarp();
-            continue;
-        }
-        const GroupAddr ga = tile_addr(sq, a.H, h, ts / kTile, kD, KB, VB, G);   // packed tiles hold no residual
-        const uint16_t* ksc = ga.ks;
-        const uint16_t* kzr = ga.kz;
-        float sc[GQ], bias[GQ];
-#pragma unroll
-        for (int hh = 0; hh < GQ; ++hh) bias[hh] = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kD / 32; ++i) {
-            const int d = lane + 32 * i;
-            const float s = f16_bits_to_float(ksc[d]), z = f16_bits_to_float(kzr[d]);
-#pragma unroll
-            for (int hh = 0; hh < GQ; ++hh) {
-                qk[warp][hh][d] = qs[hh * kD + d] * s;
-                bias[hh] = fmaf(qs[hh * kD + d], z, bias[hh]);
-            }
-        }
-#pragma unroll
-        for (int hh = 0; hh < GQ; ++hh) sc[hh] = warp_sum(bias[hh]);
-        const uint4* vrow = reinterpret_cast<const uint4*>(ga.vc + lane * (kD * VB / 8));
-#pragma unroll
-        for (int w = 0; w < kVWords / 4; ++w)
-            *reinterpret_cast<uint4*>(&vcode[warp][lane][4 * w]) = __ldg(vrow + w);
-#pragma unroll
-        for (int k = 0; k < kNg; ++k) {
-            vsc[warp][lane][k] = f16_bits_to_float(ga.vs[lane * kNg + k]);
-            vzr[warp][lane][k] = f16_bits_to_float(ga.vz[lane * kNg + k]);
-        }
-        __syncwarp();
-        const uint4* krow = reinterpret_cast<const uint4*>(ga.kc + lane * (kD * KB / 8));
-#pragma unroll
-        for (int w4 = 0; w4 < kKWords / 4; ++w4) {
-            const uint4 v4 = __ldg(krow + w4);
-            const uint32_t words[4] = {v4.x, v4.y, v4.z, v4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-#pragma unroll
-                for (int i = 0; i < kPerWord; ++i) {
-                    const int d = (4 * w4 + e) * kPerWord + i;
-                    const float c = static_cast<float>((words[e] >> (i * KB)) & kq);
-#pragma unroll
-                    for (int hh = 0; hh < GQ; ++hh) sc[hh] = fmaf(qk[warp][hh][d], c, sc[hh]);
-                }
-            }
-        }
-        float pr[GQ];
-#pragma unroll
-        for (int hh = 0; hh < GQ; ++hh) {
-            const float tmax = warp_max(sc[hh]);
-            const float mnew = fmaxf(m[hh], tmax);
-            const float alpha = exp2f(m[hh] - mnew);
-            pr[hh] = exp2f(sc[hh] - mnew);
-            l[hh] = l[hh] * alpha + warp_sum(pr[hh]);
-#pragma unroll
-            for (int c = 0; c < kCpl; ++c) acc[hh][c] *= alpha;
-            m[hh] = mnew;
-        }
-        // lane owns channels [4 lane, 4 lane + 4): value channel group lane / 8
-        const int kg = (lane * kCpl) / G;
-        for (int tau = 0; tau < 32; ++tau) {
-            const uint32_t bitsv = (vcode[warp][tau][(lane * kCpl * VB) / 32] >> ((lane * kCpl * VB) % 32));
-            const float s = vsc[warp][tau][kg], z = vzr[warp][tau][kg];
-            float v[kCpl];
-#pragma unroll
-            for (int c = 0; c < kCpl; ++c) v[c] = fmaf(static_cast<float>((bitsv >> (c * VB)) & vq), s, z);
-#pragma unroll
-            for (int hh = 0; hh < GQ; ++hh) {
-                const float pt = __shfl_sync(kFull, pr[hh], tau);
-#pragma unroll
-                for (int c = 0; c < kCpl; ++c) acc[hh][c] = fmaf(pt, v[c], acc[hh][c]);
-            }
-        }
-        __syncwarp();
-    }
-
-    __syncthreads();
-    float* red_acc = &qk[0][0][0];   // [kWarps][GQ][kD]
-    store_lane_state<GQ>(warp, lane, m, l, acc, red_m, red_l, red_acc);
-    __syncthreads();
-    finish_split<GQ>(a, b, h, split, nsplit, out_bh, red_m, red_l, red_acc, &s_last);
 }
 
 // ---------------------------------------------------------------- tensor-core kernel
@@ -1166,12 +959,8 @@ cudaError_t launch_gq(const DecodeArgs& a, cudaStream_t stream) {
         case 1: return launch_mma<KB, VB, DT, 1, G>(a, stream);
         case 2: return launch_mma<KB, VB, DT, 2, G>(a, stream);
         case 4: return launch_mma<KB, VB, DT, 4, G>(a, stream);
-        case 8:
-            decode_split_kernel<KB, VB, DT, 8, G><<<dim3(a.max_splits, a.H, a.nseq), kThreads, 0, stream>>>(a);
-            break;
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 // Decode for one pair of code widths: dispatches the input type and G.

@@ -160,7 +160,7 @@ cudaError_t launch_append_flush(const AppendArgs& a, cudaStream_t stream);
 struct DecodeArgs {
     int kb, vb, G, D, R, Hq, H, dtype;
     int nseq, max_kv_len;
-    int n_query;                    // queries per sequence (1 for decode; multi-query attention)
+    int n_query;                    // queries per sequence of multi-query attention (0: decode)
     int chunk, max_splits;          // tokens per split (multiple of 32), splits per sequence
     const kivi_seq* seqs;
     const int32_t* kv_len;

@@ -30,7 +30,6 @@
 namespace kivi {
 namespace {
 
-constexpr int kMultiStages = 4;          // cp.async ring depth (CTA-wide)
 constexpr int kF16Pitch = 272;           // bytes per token row of the f16 tiles (256 + 16: no bank conflicts)
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const unsigned char* p) {
@@ -59,13 +58,15 @@ __host__ __device__ constexpr int pos_channel(int p) {
 
 template <int KB, int VB, int W>
 struct MultiLayout {
+    static constexpr int kStages = 4;                                  // cp.async ring depth (CTA-wide)
     static constexpr int kKRow = kD * KB / 8, kVRow = kD * VB / 8;
     static constexpr int kKMeta = kTile * kKRow + kTile * kVRow;      // stage: key scale, key zero (256 B each)
     static constexpr int kVMeta = kKMeta + 512;                        // value scale, value zero (256 B each)
     static constexpr int kStage = kVMeta + 512;
-    static constexpr int kF16 = kMultiStages * kStage;                 // f16 key tile, then value tile
-    static constexpr int kPerm = kF16 + 2 * kTile * kF16Pitch;         // key scale / zero pairs [2][8][4][2] u32
-    static constexpr int kQs = kPerm + 2 * 8 * 4 * 2 * 4;              // [4W][kD] f32
+    static constexpr int kF16 = kStages * kStage;                      // two buffers of (f16 key tile, value tile)
+    static constexpr int kF16Buf = 2 * kTile * kF16Pitch;
+    static constexpr int kPerm = kF16 + 2 * kF16Buf;                   // two of key scale / zero pairs [2][8][4][2] u32
+    static constexpr int kQs = kPerm + 2 * 2 * 8 * 4 * 2 * 4;          // [4W][kD] f32
     static constexpr int kPt = kQs + 4 * W * kD * 4;                   // [W][4][kPtLd] f32
     static constexpr int kMisc = kPt + W * 4 * kPtLd * 4;              // [8] ints
     static constexpr int kBytes = kMisc + 8 * 4;
@@ -161,29 +162,31 @@ __global__ void __launch_bounds__(32 * W, W >= 4 ? 12 / W : (W == 2 ? 5 : 8)) de
     constexpr int SHIFTK = CodeShift<KB>::kValue, SHIFTV = CodeShift<VB>::kValue;
     extern __shared__ __align__(16) unsigned char smem[];
     unsigned char* stages = smem;
-    unsigned char* kf = smem + Lay::kF16;                      // [32][kF16Pitch] f16 key codes
-    unsigned char* vf = kf + kTile * kF16Pitch;                // [32][kF16Pitch] f16 value codes
-    uint32_t* perm = reinterpret_cast<uint32_t*>(smem + Lay::kPerm);   // [scale / zero][ks][t][e]
+    constexpr int S = Lay::kStages;
+    unsigned char* kf = smem + Lay::kF16;                      // [buf][key, value][32][kF16Pitch] f16 codes
+    uint32_t* perm = reinterpret_cast<uint32_t*>(smem + Lay::kPerm);   // [buf][scale / zero][ks][t][e]
     float* qs_all = reinterpret_cast<float*>(smem + Lay::kQs);
     float* pt_all = reinterpret_cast<float*>(smem + Lay::kPt);
     int* s_misc = reinterpret_cast<int*>(smem + Lay::kMisc);
 
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nq = a.n_query;
+    // n_query == 0: decode attention (one query, an empty sequence gives zeros)
+    const int nq = a.n_query > 0 ? a.n_query : 1;
     const int g = a.Hq / a.H, V = nq * g;
     const kivi_seq& sq = a.seqs[b];
     const int64_t L = a.kv_len[b];
-    const bool bad = L < nq || L > a.max_kv_len || n_packed(L, a.R, G) > sq.cap_tokens;
+    const bool empty = a.n_query == 0 && L == 0;
+    const bool bad = (L < nq && !empty) || L > a.max_kv_len || n_packed(L, a.R, G) > sq.cap_tokens;
     // out[b][i][hq][d]; virtual head v = i * g + hh -> row (b * nq + i) * Hq + h * g + hh
     auto out_row = [&](int v) {
         const int i = v / g, hh = v - i * g;
         return a.out + ((static_cast<int64_t>(b) * nq + i) * a.Hq + static_cast<int64_t>(h) * g + hh) * kD;
     };
-    if (bad) {
+    if (bad || empty) {
         if (split == 0) {
-            for (int i = tid; i < V * kD; i += NT) out_row(i / kD)[i % kD] = CUDART_NAN_F;
-            if (h == 0 && tid == 0) set_status(a.status, KIVI_ERR_LENGTH);
+            for (int i = tid; i < V * kD; i += NT) out_row(i / kD)[i % kD] = bad ? CUDART_NAN_F : 0.0f;
+            if (bad && h == 0 && tid == 0) set_status(a.status, KIVI_ERR_LENGTH);
         }
         return;
     }
@@ -326,60 +329,46 @@ __global__ void __launch_bounds__(32 * W, W >= 4 ? 12 / W : (W == 2 ? 5 : 8)) de
         const uint32_t sel_z = (gid & 1) ? 0x7632u : 0x5410u;
         float* pt = pt_all + warp * 4 * kPtLd;
 
+        // unpack stage `slot` into f16 buffer `buf` (keys, values) and its key scale / zero pairs
+        auto unpack = [&](int slot, int buf) {
+            const unsigned char* st = stages + slot * Lay::kStage;
+            // ---- unpack the tile once: (row, 16-channel block) units of keys then values; a
+            // thread's UPT units load their words first, then unpack and store. Unit u = tid +
+            // k NT is a key unit for k < UPT / 2 and a value unit after (NT divides kTile * 8).
+            constexpr int UPT = 2 * kTile * 8 / NT, HALF = UPT / 2;
+            uint2 wd[UPT];
 #pragma unroll
-        for (int i = 0; i < kMultiStages - 1; ++i) {
-            if (i < n_my) issue(i, j0 + i);
-            cp_async_commit();
-        }
-        for (int it = 0; it < n_my; ++it) {
-            cp_async_wait<kMultiStages - 2>();
-            __syncthreads();   // stage it landed for every thread; the f16 tiles of it - 1 are consumed
-            {
-                const int nxt = it + kMultiStages - 1;
-                if (nxt < n_my) issue(nxt % kMultiStages, j0 + nxt);
-                cp_async_commit();
+            for (int k = 0; k < UPT; ++k) {
+                const int uu = tid + (k % HALF) * NT, r = uu >> 3, mblk = uu & 7;
+                const int bits = k < HALF ? KB : VB;
+                const unsigned char* row = k < HALF ? st + r * RBK : st + kTile * RBK + r * RBV;
+                wd[k] = bits == 2 ? make_uint2(*reinterpret_cast<const uint32_t*>(row + 4 * mblk), 0u)
+                                  : *reinterpret_cast<const uint2*>(row + 8 * mblk);
             }
-            const unsigned char* st = stages + (it % kMultiStages) * Lay::kStage;
-            // ---- unpack the tile once: (row, 16-channel block) units of keys then values
-#pragma unroll 1
-            for (int u = tid; u < 2 * kTile * 8; u += NT) {
-                const int side = u >= kTile * 8, uu = side ? u - kTile * 8 : u;
-                const int r = uu >> 3, mblk = uu & 7;
+#pragma unroll
+            for (int k = 0; k < UPT; ++k) {
+                const int uu = tid + (k % HALF) * NT, r = uu >> 3, mblk = uu & 7;
                 uint32_t pr[8];
-                if (side == 0) {
-                    const unsigned char* row = st + r * RBK;
-                    if constexpr (KB == 2) {
-                        const uint32_t w = *reinterpret_cast<const uint32_t*>(row + 4 * mblk), ws = w >> SHIFTK;
+                auto unpack_word = [&]<int B>(uint2 w2) {
+                    constexpr int SH = CodeShift<B>::kValue;
+                    if constexpr (B == 2) {
+                        const uint32_t w = w2.x, ws = w >> SH;
                         pr[0] = code_pair<2, 0>(w, ws); pr[1] = code_pair<2, 1>(w, ws);
                         pr[2] = code_pair<2, 2>(w, ws); pr[3] = code_pair<2, 3>(w, ws);
                         pr[4] = code_pair<2, 4>(w, ws); pr[5] = code_pair<2, 5>(w, ws);
                         pr[6] = code_pair<2, 6>(w, ws); pr[7] = code_pair<2, 7>(w, ws);
                     } else {
-                        const uint2 w2 = *reinterpret_cast<const uint2*>(row + 8 * mblk);
-                        const uint32_t s0 = w2.x >> SHIFTK, s1 = w2.y >> SHIFTK;
+                        const uint32_t s0 = w2.x >> SH, s1 = w2.y >> SH;
                         pr[0] = code_pair<4, 0>(w2.x, s0); pr[1] = code_pair<4, 1>(w2.x, s0);
                         pr[2] = code_pair<4, 2>(w2.x, s0); pr[3] = code_pair<4, 3>(w2.x, s0);
                         pr[4] = code_pair<4, 0>(w2.y, s1); pr[5] = code_pair<4, 1>(w2.y, s1);
                         pr[6] = code_pair<4, 2>(w2.y, s1); pr[7] = code_pair<4, 3>(w2.y, s1);
                     }
-                } else {
-                    const unsigned char* row = st + kTile * RBK + r * RBV;
-                    if constexpr (VB == 2) {
-                        const uint32_t w = *reinterpret_cast<const uint32_t*>(row + 4 * mblk), ws = w >> SHIFTV;
-                        pr[0] = code_pair<2, 0>(w, ws); pr[1] = code_pair<2, 1>(w, ws);
-                        pr[2] = code_pair<2, 2>(w, ws); pr[3] = code_pair<2, 3>(w, ws);
-                        pr[4] = code_pair<2, 4>(w, ws); pr[5] = code_pair<2, 5>(w, ws);
-                        pr[6] = code_pair<2, 6>(w, ws); pr[7] = code_pair<2, 7>(w, ws);
-                    } else {
-                        const uint2 w2 = *reinterpret_cast<const uint2*>(row + 8 * mblk);
-                        const uint32_t s0 = w2.x >> SHIFTV, s1 = w2.y >> SHIFTV;
-                        pr[0] = code_pair<4, 0>(w2.x, s0); pr[1] = code_pair<4, 1>(w2.x, s0);
-                        pr[2] = code_pair<4, 2>(w2.x, s0); pr[3] = code_pair<4, 3>(w2.x, s0);
-                        pr[4] = code_pair<4, 0>(w2.y, s1); pr[5] = code_pair<4, 1>(w2.y, s1);
-                        pr[6] = code_pair<4, 2>(w2.y, s1); pr[7] = code_pair<4, 3>(w2.y, s1);
-                    }
-                }
-                unsigned char* dst = (side ? vf : kf) + r * kF16Pitch + 32 * mblk;
+                };
+                if (k < HALF) unpack_word.template operator()<KB>(wd[k]);
+                else unpack_word.template operator()<VB>(wd[k]);
+                unsigned char* dst =
+                    kf + buf * Lay::kF16Buf + (k < HALF ? 0 : kTile * kF16Pitch) + r * kF16Pitch + 32 * mblk;
                 *reinterpret_cast<uint4*>(dst) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
                 *reinterpret_cast<uint4*>(dst + 16) = make_uint4(pr[4], pr[5], pr[6], pr[7]);
             }
@@ -390,18 +379,42 @@ __global__ void __launch_bounds__(32 * W, W >= 4 ? 12 / W : (W == 2 ? 5 : 8)) de
                 const int e = u & 1, tt = (u >> 1) & 3, ks = (u >> 3) & 7, kind = u >> 6;
                 const uint16_t* meta = reinterpret_cast<const uint16_t*>(st + Lay::kKMeta + 256 * kind);
                 const int p0 = 16 * ks + 2 * tt + 8 * e;
-                perm[u] = static_cast<uint32_t>(meta[pos_channel<KB>(p0)]) |
-                          (static_cast<uint32_t>(meta[pos_channel<KB>(p0 + 1)]) << 16);
+                perm[buf * 128 + u] = static_cast<uint32_t>(meta[pos_channel<KB>(p0)]) |
+                                      (static_cast<uint32_t>(meta[pos_channel<KB>(p0 + 1)]) << 16);
             }
-            __syncthreads();   // the f16 tiles and the pairs are ready
+        };
 
+        // Pipeline, one barrier per tile: iteration it unpacks tile it + 1 into the other f16
+        // buffer while the warps compute tile it; the barrier at its top makes tile it + 1's
+        // stage visible, tile it's unpack visible, and frees the stage and buffer of it - 1.
+#pragma unroll
+        for (int i = 0; i < S - 1; ++i) {
+            if (i < n_my) issue(i, j0 + i);
+            cp_async_commit();
+        }
+        cp_async_wait<S - 2>();
+        __syncthreads();
+        unpack(0, 0);
+        for (int it = 0; it < n_my; ++it) {
+            cp_async_wait<S - 3>();
+            __syncthreads();
+            {
+                const int nxt = it + S - 1;
+                if (nxt < n_my) issue(nxt % S, j0 + nxt);
+                cp_async_commit();
+            }
+            if (it + 1 < n_my) unpack((it + 1) % S, (it + 1) & 1);
+            const unsigned char* st = stages + (it % S) * Lay::kStage;
+            const unsigned char* kf_it = kf + (it & 1) * Lay::kF16Buf;
+            const unsigned char* vf_it = kf_it + kTile * kF16Pitch;
+            const uint32_t* perm_it = perm + (it & 1) * 128;
             const unsigned char* vsm = st + Lay::kVMeta;        // [32 tokens][NVG] fp16
             const unsigned char* vzm = vsm + 256;
             uint32_t sp[16], zp[16];
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-                const uint2 s2 = *reinterpret_cast<const uint2*>(perm + (ks * 4 + t) * 2);
-                const uint2 z2 = *reinterpret_cast<const uint2*>(perm + 64 + (ks * 4 + t) * 2);
+                const uint2 s2 = *reinterpret_cast<const uint2*>(perm_it + (ks * 4 + t) * 2);
+                const uint2 z2 = *reinterpret_cast<const uint2*>(perm_it + 64 + (ks * 4 + t) * 2);
                 sp[2 * ks] = s2.x; sp[2 * ks + 1] = s2.y;
                 zp[2 * ks] = z2.x; zp[2 * ks + 1] = z2.y;
             }
@@ -418,7 +431,7 @@ __global__ void __launch_bounds__(32 * W, W >= 4 ? 12 / W : (W == 2 ? 5 : 8)) de
             // ---- scores: A = key codes (ldmatrix, rows = tokens), B = (q * s_k) hi / lo
             float c0[4] = {cb[0], cb[1], cb[2], cb[3]}, c1[4] = {cb[0], cb[1], cb[2], cb[3]};
             float c0o[4] = {0.0f, 0.0f, 0.0f, 0.0f}, c1o[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            const unsigned char* ka = kf + (lane & 15) * kF16Pitch + 16 * (lane >> 4);
+            const unsigned char* ka = kf_it + (lane & 15) * kF16Pitch + 16 * (lane >> 4);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const int s0 = 2 * ks, s1 = 2 * ks + 1;
@@ -502,7 +515,7 @@ __global__ void __launch_bounds__(32 * W, W >= 4 ? 12 / W : (W == 2 ? 5 : 8)) de
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) mma_f16(cz, za[kk][0], 0u, za[kk][1], 0u, bp[kk][0], bp[kk][1]);
             // ---- values: A = value codes^T (ldmatrix.trans: rows = positions, k = tokens)
-            const unsigned char* va = vf + (8 * (lane >> 4) + (lane & 7)) * kF16Pitch + 16 * ((lane >> 3) & 1);
+            const unsigned char* va = vf_it + (8 * (lane >> 4) + (lane & 7)) * kF16Pitch + 16 * ((lane >> 3) & 1);
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
 #pragma unroll
@@ -577,7 +590,7 @@ cudaError_t launch_multi_w(const DecodeArgs& a, cudaStream_t stream) {
 template <int KB, int VB>
 cudaError_t launch_multi_kv(const DecodeArgs& a, cudaStream_t stream) {
     if (a.nseq == 0) return cudaSuccess;
-    const int V = a.n_query * (a.Hq / a.H);
+    const int V = (a.n_query > 0 ? a.n_query : 1) * (a.Hq / a.H);   // as multi_plan sized the records
     const int w = V <= 4 ? 1 : V <= 8 ? 2 : V <= 16 ? 4 : 8;
     auto by_g = [&]<int DT, int W>() {
         return a.G == 64 ? launch_multi_w<KB, VB, DT, W, 64>(a, stream) : launch_multi_w<KB, VB, DT, W, 32>(a, stream);

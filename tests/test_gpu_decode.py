@@ -77,8 +77,8 @@ def test_decode_empty_sequence_gives_zeros():
 def test_split_count_invariance(dtype):
     """The same sequences give the same attention however the work is cut: alone, next
     to each other, or behind other sequences that move the CTA boundaries (query group
-    4, persistent schedule); and with different split sizes (query group 8, split size
-    from max_kv_len). Agreement to 1e-4: the f16 hi+lo operands carry ~22 bits with an
+    4, persistent schedule); and with different split sizes (query group 8, whose split
+    size follows max_kv_len). Agreement to 1e-4: the f16 hi+lo operands carry ~22 bits with an
     absolute floor of 2^-25 on subnormal low parts, and each part's running max changes
     which terms sit at that floor."""
     lens = (9000, 5000)
@@ -108,7 +108,7 @@ def test_split_count_invariance(dtype):
     assert np.max(np.abs(outs[0] - outs[1])) <= 1e-4 and np.max(np.abs(outs[0] - outs[2])) <= 1e-4
     wl = synth.Workload("splits8", 2, 16, 2, 128, lens, dtype, seed=8)
     cache, refs = build(wl, 2, 9024)
-    a, _ = check_decode(wl, cache, refs, max_kv_len=9000)          # 2048-token splits
+    a, _ = check_decode(wl, cache, refs, max_kv_len=9000)          # 1280-token splits
     b, _ = check_decode(wl, cache, refs, max_kv_len=400000)        # 4096-token splits
     c, _ = check_decode(wl, cache, refs, max_kv_len=24000)         # 3072-token splits
     assert np.max(np.abs(a - b)) <= 1e-4 and np.max(np.abs(a - c)) <= 1e-4
