@@ -335,11 +335,19 @@ __global__ void __launch_bounds__(32 * W, W >= 4 ? 12 / W : (W == 2 ? 5 : 8)) de
             // ---- unpack the tile once: (row, 16-channel block) units of keys then values; a
             // thread's UPT units load their words first, then unpack and store. Unit u = tid +
             // k NT is a key unit for k < UPT / 2 and a value unit after (NT divides kTile * 8).
+            // Unit uu of a side covers row r, block mblk with r = 4 (uu >> 5) + (uu >> 2 & 3),
+            // mblk = (uu & 3) + 4 (uu >> 4 & 1): a warp's 32 loads hit 32 banks, and each
+            // quarter-warp's 16-byte stores (rows r, r + 1 x four blocks) hit 8 bank groups.
             constexpr int UPT = 2 * kTile * 8 / NT, HALF = UPT / 2;
+            auto unit_rm = [](int uu, int& r, int& mblk) {
+                r = 4 * (uu >> 5) + ((uu >> 2) & 3);
+                mblk = (uu & 3) + 4 * ((uu >> 4) & 1);
+            };
             uint2 wd[UPT];
 #pragma unroll
             for (int k = 0; k < UPT; ++k) {
-                const int uu = tid + (k % HALF) * NT, r = uu >> 3, mblk = uu & 7;
+                int r, mblk;
+                unit_rm(tid + (k % HALF) * NT, r, mblk);
                 const int bits = k < HALF ? KB : VB;
                 const unsigned char* row = k < HALF ? st + r * RBK : st + kTile * RBK + r * RBV;
                 wd[k] = bits == 2 ? make_uint2(*reinterpret_cast<const uint32_t*>(row + 4 * mblk), 0u)
@@ -347,7 +355,8 @@ __global__ void __launch_bounds__(32 * W, W >= 4 ? 12 / W : (W == 2 ? 5 : 8)) de
             }
 #pragma unroll
             for (int k = 0; k < UPT; ++k) {
-                const int uu = tid + (k % HALF) * NT, r = uu >> 3, mblk = uu & 7;
+                int r, mblk;
+                unit_rm(tid + (k % HALF) * NT, r, mblk);
                 uint32_t pr[8];
                 auto unpack_word = [&]<int B>(uint2 w2) {
                     constexpr int SH = CodeShift<B>::kValue;
