@@ -9,16 +9,17 @@
 // group and window sizes from "KV cache quantization with KIVI INT2 setup
 // guide 2026" (G = 32, R = 128).
 //
-// Design. One warp quantizes one G-token group tile (or, for values, up to
-// 32 tokens) over a slice of up to 128 channels, entirely in registers: no
-// shared memory and no block barriers. G is 32 or 64 (a template parameter). For keys a lane owns four channels and
-// loads them from every token row (each load instruction reads whole rows,
-// coalesced); for values a lane owns one token row. Minimum and maximum run on
-// packed pairs (min/max.f16x2 or .bf16x2); the codes come from one fused
-// multiply-add with a rounding constant and reach their bit position through the
-// accumulating add, so that an element costs about nine instructions. These
-// kernels stream 16 bits in and 2.5 (2-bit) bits out per element and are meant
-// to run at the HBM bound.
+// Design. One warp quantizes one G-token group tile (or, for values, up to 32
+// tokens) over a slice of up to 128 channels, entirely in registers: no shared
+// memory and no block barriers. G is 32 or 64 (a template parameter). For keys a
+// lane owns four channels and loads them from every token row (each load
+// instruction reads whole rows, coalesced); for values a lane owns one token row.
+// Minimum and maximum run on packed pairs (min/max.f16x2 or .bf16x2). The codes
+// come from a fused multiply-add with a rounding constant (twice, with 1/s
+// bracketed, to mark the rare elements whose code the exact division must decide)
+// and reach their bit position through the accumulating add. These kernels stream
+// 16 bits in and 2.5 (2-bit) bits out per element and are meant to run at the HBM
+// bound.
 #include "kivi_internal.cuh"
 
 namespace kivi {
@@ -38,10 +39,12 @@ __host__ __device__ constexpr int slice_width(int D) { return D % 64 == 0 ? 64 :
 __host__ __device__ constexpr int key_slice_width(int D, int G) {
     return G == 64 ? 64 : (D % 128 == 0 ? 128 : slice_width(D));
 }
-// Registers of elements per lane: DS * TOK / 64 for a DS-channel, TOK-token tile.
-template <int DS, int TOK>
+// Registers of elements per lane: DS * TOK / 64 for a DS-channel, TOK-token tile. Tiles
+// of 64 registers run two CTAs of eight warps per SM, smaller ones three; so do 4-bit
+// bf16 value tiles, whose fully unrolled 64 codes per lane do not fit 80 registers.
+template <int DS, int TOK, int BITS = 2, int DT = KIVI_F16>
 struct CtasPerSm {
-    static constexpr int kValue = DS * TOK / 64 >= 64 ? 2 : 3;
+    static constexpr int kValue = DS * TOK / 64 >= 64 || (BITS == 4 && DT == KIVI_BF16 && DS >= 64) ? 2 : 3;
 };
 
 template <int DT>
@@ -72,16 +75,19 @@ __device__ __forceinline__ uint32_t pick_max(uint32_t a, uint32_t b) {
     return widen<DT>(static_cast<uint16_t>(b)) > widen<DT>(static_cast<uint16_t>(a)) ? b : a;
 }
 
-// The fp32 quantizer of one group: zero z, scale s and r = 1/s (0 when s is 0 or inf).
+// The fp32 quantizer of one group: zero z, scale s, and r_lo, r_hi: r = 1/s (correctly
+// rounded; 0 when s is 0 or inf) moved down and up by 2^-21 of itself.
 struct Quantizer {
-    float z, r, s;
+    float z, s, r_lo, r_hi;
 };
 
 __device__ __forceinline__ Quantizer make_quantizer(const GroupParams& gp) {
     Quantizer q;
     q.z = gp.z;
     q.s = gp.s;
-    q.r = gp.s != 0.0f ? __frcp_rn(gp.s) : 0.0f;
+    const float r = gp.s != 0.0f ? __frcp_rn(gp.s) : 0.0f;
+    q.r_lo = __fmul_rn(r, 1.0f - 0x1p-21f);
+    q.r_hi = __fmul_rn(r, 1.0f + 0x1p-21f);
     return q;
 }
 
@@ -98,34 +104,35 @@ __host__ __device__ constexpr uint32_t magic_offset(int n, int bits) {
 }
 
 // The code of encode() as kMagic + code (an fp32 bit pattern), with the IEEE division
-// replaced by r = 1/s, plus a flag set when that may give a different code.
-// y = fma(d, r, kMagic) is kMagic + rint(d r) for the exact product d r, and f is
-// d r - rint(d r). The exact product is within 2^-23 |t| of the correctly rounded
-// quotient t = d / s (r is 1/s correctly rounded). Only the half-integers 0.5 ..
-// qmax - 0.5 (|t| < 16) can change a clamped code, and there the two differ by at
-// most 2e-6: the codes agree unless |f| > 0.5 - 1e-5, which sets near_tie (the caller
-// then recomputes with the exact division). There is no clamp: the caller checks with
-// codes_in_range() that every element of the group lands in [0, qmax] and otherwise
-// recomputes the group exactly. r == 0 (s == 0 or s = inf) gives code 0, as the
-// division does.
+// replaced by products with a bracket of 1/s, and a mark where that may give a
+// different code. fma(d, r_x, kMagic) is kMagic + rint(d r_x) for the exact product
+// d r_x. The correctly rounded quotient t = d / s lies within 2^-22 |t| of d / s's
+// exact value and of d r (r is 1/s correctly rounded), so inside [d r_lo, d r_hi] (the
+// bracket is 2^-21 wide on each side, less at most 2^-24 from rounding r_lo and r_hi).
+// rint is monotone, so when the two ends round to the same integer, so does t. When
+// they differ (a half-integer lies in the bracket) the bits of the two results differ
+// and are OR-ed into `mark`: the caller recomputes with the exact division. There is no
+// clamp: the caller checks with codes_in_range() that every element of the group lands
+// in [0, qmax] and otherwise recomputes the group exactly. r == 0 (s == 0 or s = inf)
+// gives code 0, as the division does.
 template <int BITS>
-__device__ __forceinline__ uint32_t code_bits(float x, const Quantizer& q, bool& near_tie) {
+__device__ __forceinline__ uint32_t code_bits(float x, const Quantizer& q, uint32_t& mark) {
     const float d = __fsub_rn(x, q.z);
-    const float y = __fmaf_rn(d, q.r, kMagic);
-    const float f = __fmaf_rn(d, q.r, -__fsub_rn(y, kMagic));
-    near_tie |= fabsf(f) > 0.5f - 1e-5f;
-    return __float_as_uint(y);
+    const uint32_t y_lo = __float_as_uint(__fmaf_rn(d, q.r_lo, kMagic));
+    const uint32_t y_hi = __float_as_uint(__fmaf_rn(d, q.r_hi, kMagic));
+    mark |= y_lo ^ y_hi;
+    return y_hi;
 }
 
 // Whether code_bits() gives codes in [0, qmax] for every element of a group with this
-// minimum and maximum: x -> fma(x - z, r, kMagic) is monotone (r >= 0), so checking the
-// two ends suffices. False only where the fp16 rounding of z or s pushes an end more
-// than half a step out (for instance inputs below the fp16 normal range).
+// minimum and maximum: x -> fma(x - z, r_hi, kMagic) is monotone (r_hi >= 0), so
+// checking the two ends suffices. False only where the fp16 rounding of z or s pushes an
+// end more than half a step out (for instance inputs below the fp16 normal range).
 template <int BITS>
 __device__ __forceinline__ bool codes_in_range(float mn, float mx, const Quantizer& q) {
     constexpr float qmax = static_cast<float>((1 << BITS) - 1);
-    const float ylo = __fmaf_rn(__fsub_rn(mn, q.z), q.r, kMagic);
-    const float yhi = __fmaf_rn(__fsub_rn(mx, q.z), q.r, kMagic);
+    const float ylo = __fmaf_rn(__fsub_rn(mn, q.z), q.r_hi, kMagic);
+    const float yhi = __fmaf_rn(__fsub_rn(mx, q.z), q.r_hi, kMagic);
     return ylo >= kMagic && yhi <= kMagic + qmax;
 }
 
@@ -267,13 +274,13 @@ __device__ __forceinline__ void keys_compute(const Tile<DS, G>& x, RowFn row, ui
     uint32_t tie_rows = in_range ? 0u : 0xffffffffu >> (32 - NT);   // rows to redo with the exact division
 #pragma unroll
     for (int i = 0; i < NT; ++i) {
-        bool tie = false;
+        uint32_t mark = 0u;
         uint32_t acc = magic_offset(4, BITS);
-        acc += code_bits<BITS>(half_at<DT>(x.w[2 * i], 0), qz[0], tie);
-        acc += code_bits<BITS>(half_at<DT>(x.w[2 * i], 1), qz[1], tie) << BITS;
-        acc += code_bits<BITS>(half_at<DT>(x.w[2 * i + 1], 0), qz[2], tie) << (2 * BITS);
-        acc += code_bits<BITS>(half_at<DT>(x.w[2 * i + 1], 1), qz[3], tie) << (3 * BITS);
-        tie_rows |= static_cast<uint32_t>(tie) << i;
+        acc += code_bits<BITS>(half_at<DT>(x.w[2 * i], 0), qz[0], mark);
+        acc += code_bits<BITS>(half_at<DT>(x.w[2 * i], 1), qz[1], mark) << BITS;
+        acc += code_bits<BITS>(half_at<DT>(x.w[2 * i + 1], 0), qz[2], mark) << (2 * BITS);
+        acc += code_bits<BITS>(half_at<DT>(x.w[2 * i + 1], 1), qz[3], mark) << (3 * BITS);
+        tie_rows |= static_cast<uint32_t>(mark != 0u) << i;
         uint8_t* dst = codes + static_cast<int64_t>(i * TS + j) * code_ld;
         if constexpr (BITS == 2) dst[cq] = static_cast<uint8_t>(acc);
         else reinterpret_cast<uint16_t*>(dst)[cq] = static_cast<uint16_t>(acc);
@@ -351,18 +358,18 @@ __device__ __forceinline__ void values_compute(const Tile<DS, 32>& x, const uint
             const Quantizer q = make_quantizer(gp);
             zq[k] = q.z;
             sq[k] = q.s;
-            bool tie = !codes_in_range<BITS>(fmn, fmx, q);
+            uint32_t mark = codes_in_range<BITS>(fmn, fmx, q) ? 0u : 1u;
 #pragma unroll
             for (int ww = 0; ww < WPG; ++ww) {
                 uint32_t acc = magic_offset(CPW, BITS);
 #pragma unroll
                 for (int e = 0; e < CPW; ++e) {
                     const int c = ww * CPW + e;
-                    acc += code_bits<BITS>(half_at<DT>(w[c >> 1], c & 1), q, tie) << (e * BITS);
+                    acc += code_bits<BITS>(half_at<DT>(w[c >> 1], c & 1), q, mark) << (e * BITS);
                 }
                 code_w[k][ww] = acc;
             }
-            tie_groups |= static_cast<uint32_t>(tie) << k;
+            tie_groups |= static_cast<uint32_t>(mark != 0u) << k;
         }
         // code row: NKG * WPG words (8 bytes per 32 channels at 2 bits, 16 at 4 bits)
         uint32_t* cw = reinterpret_cast<uint32_t*>(codes);
@@ -443,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, CtasPerSm<DS, G>::kValue) quant_keys
 
 // One warp per (stream, run of 32 tokens, channel slice); lane t takes token t.
 template <int BITS, int DT, int DS, int G>
-__global__ void __launch_bounds__(kThreads, CtasPerSm<DS, 32>::kValue) quant_values_kernel(CodecArgs a) {
+__global__ void __launch_bounds__(kThreads, CtasPerSm<DS, 32, BITS, DT>::kValue) quant_values_kernel(CodecArgs a) {
     const int D = a.D, nsl = D / DS, runs = (a.n_tokens + kTile - 1) / kTile;
     const int64_t unit = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
     if (unit >= static_cast<int64_t>(a.n_streams) * runs * nsl) return;
@@ -488,7 +495,8 @@ __device__ __forceinline__ SeqState seq_state(const AppendArgs& a, int b, int ca
 constexpr int kUnitsPerWarp = 32;
 
 template <int BITS, int DT, int DS, int G, int SIDE>
-__global__ void __launch_bounds__(kThreads, CtasPerSm<DS, SIDE == 0 ? G : 32>::kValue) append_pack_kernel(AppendArgs a) {
+__global__ void __launch_bounds__(kThreads, CtasPerSm<DS, SIDE == 0 ? G : 32, SIDE == 0 ? 2 : BITS, DT>::kValue)
+    append_pack_kernel(AppendArgs a) {
     constexpr int TOK = SIDE == 0 ? G : kTile;   // tokens of one unit
     const int h = blockIdx.y, b = blockIdx.z, D = a.D, nsl = D / DS;
     const kivi_seq& sq = a.seqs[b];
