@@ -159,7 +159,6 @@ __global__ void __launch_bounds__(32 * W, W >= 4 ? 12 / W : (W == 2 ? 5 : 8)) de
     constexpr int TPG = G / kTile;             // tiles per key group
     constexpr int NVG = kD / G;                // value channel groups per token
     constexpr int VMETA = kTile * NVG * 2;     // bytes of value scales (or zeros) of one tile
-    constexpr int SHIFTK = CodeShift<KB>::kValue, SHIFTV = CodeShift<VB>::kValue;
     extern __shared__ __align__(16) unsigned char smem[];
     unsigned char* stages = smem;
     constexpr int S = Lay::kStages;
