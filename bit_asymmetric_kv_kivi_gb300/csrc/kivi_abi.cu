@@ -111,7 +111,7 @@ kivi_status kivi_decode_attn(const kivi_cfg* cfg, int32_t nseq, const kivi_seq* 
     if (!cfg_ok(cfg)) return KIVI_ERR_ARG;
     if (nseq < 0 || nseq > 65535 || max_kv_len < 0 || !isfinite(softmax_scale)) return KIVI_ERR_ARG;
     const int g = cfg->num_q_heads / cfg->num_kv_heads;
-    if (cfg->head_dim != 128 || (g != 1 && g != 2 && g != 4 && g != 8)) return KIVI_ERR_UNSUPPORTED;
+    if (cfg->head_dim != 128 || g > 32) return KIVI_ERR_UNSUPPORTED;
     if (nseq == 0) return KIVI_OK;
     if (seqs_dev == nullptr || kv_len_dev == nullptr || q_dev == nullptr || out_dev == nullptr)
         return KIVI_ERR_ARG;

@@ -16,13 +16,14 @@ void decode_plan(int nseq, int H, int Hq, int D, int max_kv_len, int* chunk, int
         *partial_bytes = (2 * static_cast<size_t>(nseq) * H + kDecodeMaxCtas) * gq * (D + 4) * sizeof(float);
         return;
     }
-    // query group 8: decode_multi_kernel with one query per sequence
+    // other query groups (up to 32): decode_multi_kernel with one query per sequence
     multi_plan(nseq, H, Hq, D, 1, max_kv_len, chunk, max_splits, counter_bytes, partial_bytes);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     if (a.nseq == 0) return cudaSuccess;
-    if (a.Hq == 8 * a.H) {
+    const int gq = a.Hq / a.H;
+    if (gq != 1 && gq != 2 && gq != 4) {
         DecodeArgs m = a;
         m.n_query = 0;     // decode: one query per sequence, empty sequences give zeros
         return launch_multi(m, stream);

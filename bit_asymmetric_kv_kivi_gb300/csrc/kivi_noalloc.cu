@@ -64,7 +64,7 @@ extern "C" kivi_status kivi_decode_attn_static(const kivi_cfg* cfg, int32_t nseq
         !isfinite(softmax_scale) || nseq > 65535)
         return KIVI_ERR_ARG;
     const int g = cfg->num_q_heads / cfg->num_kv_heads;
-    if (cfg->head_dim != 128 || (g != 1 && g != 2 && g != 4 && g != 8)) return KIVI_ERR_UNSUPPORTED;
+    if (cfg->head_dim != 128 || g > 32) return KIVI_ERR_UNSUPPORTED;
     if (need > KIVI_STATIC_WORKSPACE_BYTES) return KIVI_ERR_WORKSPACE;
     void* ws = nullptr;
     const kivi_status st = static_workspace(&ws);

@@ -215,7 +215,9 @@ kivi_status kivi_append_flush(const kivi_cfg* cfg, int32_t nseq, const kivi_seq*
  * A sequence with kv_len 0 gets zeros. Device error KIVI_ERR_LENGTH: kv_len_b
  * outside [0, max_kv_len] or more tokens than the sequence can hold; that
  * sequence's output rows are set to NaN.
- * Errors: KIVI_ERR_UNSUPPORTED unless D == 128 and Hq/Hkv is 1, 2, 4 or 8.
+ * Query groups 1, 2 and 4 run on a persistent tensor-core kernel; any other
+ * group up to 32 on the multi-query kernel with one query.
+ * Errors: KIVI_ERR_UNSUPPORTED unless D == 128 and Hq/Hkv <= 32.
  */
 kivi_status kivi_decode_attn(const kivi_cfg* cfg, int32_t nseq, const kivi_seq* seqs_dev,
                              const int32_t* kv_len_dev, const void* q_dev, float* out_dev,

@@ -92,10 +92,10 @@ def test_bad_arguments_rejected_before_launch(lib):
     assert need > 0
     assert lib.kivi_decode_attn(cfg, 2, one, one, one, one, 0.1, 5000, one, need - 1, one, None) == kivi.ERR_WORKSPACE
     assert lib.kivi_decode_attn(cfg, 2, one, one, one, one, 0.1, 5000, null, need, one, None) == kivi.ERR_WORKSPACE
-    # decode supports head_dim 128 and Hq/Hkv in {1, 2, 4, 8} only
+    # decode supports head_dim 128 and Hq/Hkv up to 32
     assert lib.kivi_decode_attn(kivi.Config(head_dim=64).c(), 1, one, one, one, one, 0.1, 10, one, 1 << 20,
                                 one, None) == kivi.ERR_UNSUPPORTED
-    assert lib.kivi_decode_attn(kivi.Config(num_q_heads=3).c(), 1, one, one, one, one, 0.1, 10, one, 1 << 20,
+    assert lib.kivi_decode_attn(kivi.Config(num_q_heads=33).c(), 1, one, one, one, one, 0.1, 10, one, 1 << 20,
                                 one, None) == kivi.ERR_UNSUPPORTED
     # zero-sized calls are no-ops that touch nothing
     assert lib.kivi_quant_keys(cfg, 0, 32, null, null, null, null, None) == kivi.OK

@@ -183,3 +183,17 @@ def test_many_streams_persistent_schedule(g, shape):
     cache, refs = build(wl, 2, cap)
     out, _ = check_decode(wl, cache, refs)
     assert np.all(out[lengths == 0] == 0)
+
+
+@pytest.mark.parametrize("g", [3, 5, 6, 16, 32])
+@pytest.mark.parametrize("bits", [2, 4])
+def test_decode_any_query_group(g, bits):
+    """Query groups other than 1, 2, 4 (up to 32) run on the multi-query kernel with one
+    query, its virtual heads padded to whole warps of four."""
+    lengths = (0, 1, 33, 160, 161, 700, 3000)
+    H = 2
+    dtype = "bf16" if g % 2 else "f16"
+    wl = synth.Workload("anyg", len(lengths), H * g, H, 128, lengths, dtype, bits=bits, seed=700 + g + bits)
+    cache, refs = build(wl, bits, 3008)
+    out, _ = check_decode(wl, cache, refs)
+    assert np.all(out[0] == 0)
