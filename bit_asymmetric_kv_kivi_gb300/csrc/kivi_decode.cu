@@ -7,10 +7,11 @@ namespace kivi {
 
 void decode_plan(int nseq, int H, int Hq, int D, int max_kv_len, int* chunk, int* max_splits,
                  size_t* counter_bytes, size_t* partial_bytes) {
-    *counter_bytes = ((static_cast<size_t>(nseq) * H * sizeof(int32_t) + 255) / 256) * 256;
     const int gq = H > 0 ? Hq / H : 0;
     if (gq == 1 || gq == 2 || gq == 4) {
-        // decode_mma_kernel: one record per segment, fewer than 2 S + kDecodeMaxCtas of them
+        // decode_mma_kernel: a ticket per stream; one record per segment, fewer than
+        // 2 S + kDecodeMaxCtas of them
+        *counter_bytes = ((static_cast<size_t>(nseq) * H * sizeof(int32_t) + 255) / 256) * 256;
         *chunk = 0;
         *max_splits = 0;
         *partial_bytes = (2 * static_cast<size_t>(nseq) * H + kDecodeMaxCtas) * gq * (D + 4) * sizeof(float);

@@ -138,3 +138,26 @@ def test_multi_query_bad_lengths():
     assert np.max(np.abs(out[1] - want)) <= ATTN_TOL
     with pytest.raises(kivi.KiviError):
         cache.decode_multi(dev_tensor(np.zeros((2, 9, 4, 128), np.uint16), "f16"))
+
+
+def test_decode_and_multi_query_share_one_workspace():
+    """kivi_decode_attn and kivi_decode_multi_attn alternate on one cache and one workspace
+    (the binding keeps one per cache). With 64 (sequence, kv head) streams the tickets
+    fill the first 256 bytes exactly: neither call may leave the other's counters
+    disturbed, and decode repeats bit for bit."""
+    H, g, nq = 8, 4, 2
+    lengths = (700, 1000, 150, 3000, 64, 2000, 999, 128)
+    wl = synth.Workload("shared-ws", len(lengths), g * H, H, 128, lengths, "f16", seed=440)
+    kcfg, ocfg = configs(2, "f16", g * H, H)
+    cache, refs = build(wl, kcfg, ocfg, 3008)
+    q1 = dev_tensor(wl.query(5), "f16")
+    first = cache.decode(q1, softmax_scale=wl.softmax_scale).cpu().numpy()
+    for step in range(3):
+        check(wl, cache, refs, nq, step=step)
+        again = cache.decode(q1, softmax_scale=wl.softmax_scale).cpu().numpy()
+        assert int(cache.status.item()) == 0
+        assert np.array_equal(first, again), step
+    for b, r in enumerate(refs):
+        err = float(np.max(np.abs(first[b] - r.decode(wl.query(5)[b], wl.softmax_scale))))
+        record_error(err)
+        assert err <= ATTN_TOL, err
