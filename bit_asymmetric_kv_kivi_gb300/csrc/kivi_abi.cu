@@ -219,7 +219,7 @@ const char* kivi_status_string(int32_t status) {
     switch (status) {
         case KIVI_OK: return "ok";
         case KIVI_ERR_ARG: return "invalid argument or configuration";
-        case KIVI_ERR_UNSUPPORTED: return "configuration not supported by this build";
+        case KIVI_ERR_UNSUPPORTED: return "configuration not supported by this library";
         case KIVI_ERR_CAPACITY: return "append exceeds the packed capacity of a sequence";
         case KIVI_ERR_WORKSPACE: return "workspace missing or too small";
         case KIVI_ERR_CUDA: return "CUDA launch or runtime error";

@@ -74,7 +74,7 @@ extern "C" {
 typedef enum kivi_status {
     KIVI_OK = 0,
     KIVI_ERR_ARG = 1,          /* invalid argument or configuration; nothing launched */
-    KIVI_ERR_UNSUPPORTED = 2,  /* valid configuration this build does not implement */
+    KIVI_ERR_UNSUPPORTED = 2,  /* valid configuration this library does not implement */
     KIVI_ERR_CAPACITY = 3,     /* device: an append would need more than cap_tokens packed tokens */
     KIVI_ERR_WORKSPACE = 4,    /* workspace pointer NULL or smaller than required */
     KIVI_ERR_CUDA = 5,         /* a CUDA launch or runtime call failed */
