@@ -17,7 +17,7 @@ import torch
 import bit_asymmetric_kv_kivi_gb300 as kivi
 import oracle
 import synth
-from gpu_util import ATTN_TOL, assert_state_equal, configs, host_bits, record_error
+from gpu_util import ATTN_TOL, assert_state_equal, configs, dev_tensor, host_bits, record_error
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -142,3 +142,48 @@ def test_streaming_append_full_size(bits):
     for b in sample:
         assert refs[b].L == L0 + steps
         assert oracle.n_packed(ocfg, refs[b].L) == 16256 + 32 * (steps // 32)
+
+
+def test_maximum_sequence_count():
+    """The largest batch the ABI takes (65535 sequences): mostly residual-only sequences
+    of 0..47 tokens and 1 % of 150..199 (a packed group or two), one kv head, query group
+    4. Prefill, one decode step (append + flush + attention); a seeded sample of sequences
+    is checked against the oracle, every output is finite."""
+    n, H, g, D = 65535, 1, 4, 128
+    rng = np.random.default_rng(2024)
+    lengths = rng.integers(0, 48, size=n)
+    long = rng.random(n) < 0.01
+    lengths[long] = rng.integers(150, 200, size=int(long.sum()))
+    lengths[:4] = (0, 1, 159, 160)
+    lengths[-1] = 199
+    kcfg, ocfg = configs(2, "f16", g * H, H)
+    cache = kivi.KVCache(kcfg, n, 96)
+    tot = int(lengths.sum())
+    K = synth.to_dtype_bits(rng.standard_normal((H, tot, D)) * np.where(np.arange(D) < 3, 20.0, 1.0), "f16")
+    V = synth.to_dtype_bits(rng.standard_normal((H, tot, D)), "f16")
+    Kd, Vd = dev_tensor(K, "f16"), dev_tensor(V, "f16")
+    offs = np.concatenate([[0], np.cumsum(lengths)])
+    # one [H][L_b][D] view per sequence, contiguous because H == 1
+    cache.append([Kd[:, offs[b]:offs[b + 1]] for b in range(n)], [Vd[:, offs[b]:offs[b + 1]] for b in range(n)])
+    step_k = synth.to_dtype_bits(rng.standard_normal((H, 1, D)), "f16")
+    step_v = synth.to_dtype_bits(rng.standard_normal((H, 1, D)), "f16")
+    kn, vn = dev_tensor(step_k, "f16"), dev_tensor(step_v, "f16")
+    cache.append([kn] * n, [vn] * n)
+    q = synth.to_dtype_bits(rng.standard_normal((n, g * H, D)), "f16")
+    scale = 1.0 / np.sqrt(D)
+    out = cache.decode(dev_tensor(q, "f16"), softmax_scale=scale).cpu().numpy()
+    torch.cuda.synchronize()
+    assert int(cache.status.item()) == 0
+    assert np.all(np.isfinite(out))
+    sample = sorted(set([0, 1, 2, 3, n - 1] + [int(x) for x in rng.choice(n, 60, replace=False)] +
+                        [int(x) for x in np.flatnonzero(long)[:10]]))
+    worst = 0.0
+    for b in sample:
+        r = oracle.SeqCache(ocfg, 96)
+        assert r.append(np.ascontiguousarray(K[:, offs[b]:offs[b + 1]]),
+                        np.ascontiguousarray(V[:, offs[b]:offs[b + 1]])) == oracle.OK
+        assert r.append(step_k, step_v) == oracle.OK
+        assert_state_equal(cache, b, r)
+        worst = max(worst, float(np.max(np.abs(out[b] - r.decode(q[b], scale)))))
+    record_error(worst)
+    assert worst <= ATTN_TOL, worst

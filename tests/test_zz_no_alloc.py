@@ -63,3 +63,23 @@ def test_static_workspace_rejects_sizes_beyond_its_maximum():
     one = ctypes.c_void_p(16)
     rc = L.kivi_decode_attn_static(kcfg.c(), nseq, one, one, one, one, 0.1, max_len, one, None)
     assert rc == kivi.ERR_WORKSPACE
+
+
+def test_static_workspace_query_group_8():
+    """Query group 8 runs on the multi-query kernel; the fixed workspace serves it too."""
+    wl = synth.Workload("noalloc8", 2, 16, 2, 128, (5000, 700), "bf16", seed=78)
+    kcfg, _ = configs(2, "bf16", 16, 2)
+    cache = kivi.KVCache(kcfg, 2, 5024)
+    cache.append([dev_tensor(wl.kv_seq(b, 0, wl.lengths[b])[0], "bf16") for b in range(2)],
+                 [dev_tensor(wl.kv_seq(b, 0, wl.lengths[b])[1], "bf16") for b in range(2)])
+    q = dev_tensor(wl.query(0), "bf16")
+    want = cache.decode(q, softmax_scale=wl.softmax_scale)
+    out = torch.full_like(want, float("nan"))
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = _lib().kivi_decode_attn_static(kcfg.c(), 2, cache.seqs.data_ptr(), cache.kv_len.data_ptr(), q.data_ptr(),
+                                        out.data_ptr(), wl.softmax_scale, cache.max_len, cache.status.data_ptr(),
+                                        stream)
+    assert rc == kivi.OK, kivi.status_string(rc)
+    torch.cuda.synchronize()
+    assert int(cache.status.item()) == 0
+    assert float((out - want).abs().max().item()) <= ATTN_TOL
