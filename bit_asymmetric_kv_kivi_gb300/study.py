@@ -68,12 +68,14 @@ def attention_errors(q, K, V, Kq, Vq, scale):
     return float(e_s), float(e_p), float(e_o)
 
 
-def run(workload: int = 1, seqs: int = 2, tokens: int | None = None, bits_list=(2, 4), device="cuda"):
+def run(workload: int = 1, seqs: int = 2, tokens: int | None = None, bits_list=(2, 4), device="cuda",
+        group: int = GROUP):
     """One row per (scheme, bits): the three mean errors over `seqs` sequences x every kv
-    head (one decode query per head: the first query head of its group)."""
+    head (one decode query per head: the first query head of its group), with groups of
+    `group` tokens (keys) or channels (values)."""
     import synth   # the seeded generators shared with the tests and the bench
     wl = synth.workload(workload)
-    T = (min(tokens or wl.lengths[0], wl.lengths[0]) // GROUP) * GROUP
+    T = (min(tokens or wl.lengths[0], wl.lengths[0]) // group) * group
     H, D = wl.num_kv_heads, wl.head_dim
     tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
     K = torch.stack([synth.torch_kv_head_major(wl, b, h, 0, T, "k", device) for b in range(seqs) for h in range(H)])
@@ -84,13 +86,14 @@ def run(workload: int = 1, seqs: int = 2, tokens: int | None = None, bits_list=(
     K64, V64 = K.to(torch.float64), V.to(torch.float64)
     rows = []
     for bits in bits_list:
-        cfg = Config(bits=bits, head_dim=D, num_q_heads=1, num_kv_heads=1, dtype=BF16 if wl.dtype == "bf16" else F16)
+        cfg = Config(bits=bits, head_dim=D, num_q_heads=1, num_kv_heads=1, dtype=BF16 if wl.dtype == "bf16" else F16,
+                     group=group)
         deq = {("k", a): dequant(cfg, K, a) for a in ("token", "channel")}
         deq.update({("v", a): dequant(cfg, V, a) for a in ("token", "channel")})
         for name, (ka, va) in SCHEMES.items():
             e = attention_errors(q, K64, V64, deq[("k", ka)], deq[("v", va)], wl.softmax_scale)
             rows.append({"scheme": name, "bits": bits, "score_rel_l2": e[0], "prob_tv": e[1], "out_rel_l2": e[2]})
-    return {"workload": wl.name, "sequences": seqs, "tokens": T, "kv_heads": H, "rows": rows}
+    return {"workload": wl.name, "sequences": seqs, "tokens": T, "kv_heads": H, "group": group, "rows": rows}
 
 
 def main():
@@ -98,9 +101,11 @@ def main():
     ap.add_argument("--workload", type=int, default=1)
     ap.add_argument("--seqs", type=int, default=2)
     ap.add_argument("--tokens", type=int, default=0)
+    ap.add_argument("--group", type=int, default=GROUP, help="G: 32 or 64")
     args = ap.parse_args()
-    res = run(args.workload, args.seqs, args.tokens or None)
-    print(f"{res['workload']}: {res['sequences']} sequences x {res['kv_heads']} kv heads x {res['tokens']} tokens")
+    res = run(args.workload, args.seqs, args.tokens or None, group=args.group)
+    print(f"{res['workload']}: {res['sequences']} sequences x {res['kv_heads']} kv heads x {res['tokens']} tokens, "
+          f"G = {res['group']}")
     print(f"{'scheme':34s} bits  score rel.L2  prob. TV  output rel.L2")
     for r in res["rows"]:
         print(f"{r['scheme']:34s} {r['bits']:4d}  {r['score_rel_l2']:12.4f}  {r['prob_tv']:8.4f}  {r['out_rel_l2']:13.4f}")

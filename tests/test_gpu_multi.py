@@ -94,14 +94,15 @@ def test_multi_query_one_query_matches_decode():
     assert np.max(np.abs(out[:, 0] - dec)) <= 1e-4
 
 
-def test_multi_query_after_streaming_appends_and_paged_layout():
+@pytest.mark.parametrize("kb,vb,G,R", [(2, 2, 32, 128), (4, 2, 64, 64)])
+def test_multi_query_after_streaming_appends_and_paged_layout(kb, vb, G, R):
     """Verification steps as a speculative decoder runs them: append n_query draft tokens,
     verify them, repeat (with flushes in between); the paged cache gives the same output
     bit for bit."""
     H, g, nq = 2, 4, 4
     lengths = (130, 300, 1000)
-    wl = synth.Workload("multi-stream", len(lengths), g * H, H, 128, lengths, "bf16", seed=420)
-    kcfg, ocfg = configs(2, "bf16", g * H, H)
+    wl = synth.Workload("multi-stream", len(lengths), g * H, H, 128, lengths, "bf16", seed=420 + G)
+    kcfg, ocfg = configs(2, "bf16", g * H, H, G=G, R=R, kb=kb, vb=vb)
     cap = 1536
     cont, refs = build(wl, kcfg, ocfg, cap)
     paged, _ = build(wl, kcfg, ocfg, cap, paged=True)

@@ -9,10 +9,10 @@ from test_oracle_study import study as oracle_study
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("workload", [1, 2])
-def test_gpu_study_equals_oracle_study(workload):
-    res = study.run(workload=workload, seqs=1, tokens=512)
-    ref = oracle_study(workload, seqs=1, T=512)
+@pytest.mark.parametrize("workload,group", [(1, 32), (2, 32), (2, 64)])
+def test_gpu_study_equals_oracle_study(workload, group):
+    res = study.run(workload=workload, seqs=1, tokens=512, group=group)
+    ref = oracle_study(workload, seqs=1, T=512, group=group)
     assert res["tokens"] == 512
     for r in res["rows"]:
         want = ref[(r["scheme"], r["bits"])]

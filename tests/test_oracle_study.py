@@ -25,12 +25,13 @@ def f16(b):
 
 
 def dequant(cfg, xb, axis):
+    G = cfg.group
     if axis == "channel":
         codes, s, z = oracle.quant_keys(cfg, xb)
-        s, z = np.repeat(f16(s), 32, axis=1), np.repeat(f16(z), 32, axis=1)
+        s, z = np.repeat(f16(s), G, axis=1), np.repeat(f16(z), G, axis=1)
     else:
         codes, s, z = oracle.quant_values(cfg, xb)
-        s, z = np.repeat(f16(s), 32, axis=2), np.repeat(f16(z), 32, axis=2)
+        s, z = np.repeat(f16(s), G, axis=2), np.repeat(f16(z), G, axis=2)
     return unpack(codes, cfg.bits, cfg.head_dim) * s + z
 
 
@@ -39,7 +40,7 @@ def softmax(x):
     return e / e.sum(axis=-1, keepdims=True)
 
 
-def study(workload=1, seqs=1, T=512, bits_list=(2, 4)):
+def study(workload=1, seqs=1, T=512, bits_list=(2, 4), group=32):
     wl = synth.workload(workload)
     H, D = wl.num_kv_heads, wl.head_dim
     Kb = np.stack([wl.keys(b, h, 0, T) for b in range(seqs) for h in range(H)])
@@ -53,7 +54,7 @@ def study(workload=1, seqs=1, T=512, bits_list=(2, 4)):
     o = np.einsum("st,std->sd", p, V)
     rows = {}
     for bits in bits_list:
-        cfg = oracle.Cfg(bits=bits, head_dim=D, dtype=oracle.BF16 if wl.dtype == "bf16" else oracle.F16)
+        cfg = oracle.Cfg(bits=bits, head_dim=D, dtype=oracle.BF16 if wl.dtype == "bf16" else oracle.F16, group=group)
         deq = {("k", a): dequant(cfg, Kb, a) for a in ("token", "channel")}
         deq.update({("v", a): dequant(cfg, Vb, a) for a in ("token", "channel")})
         for name, (ka, va) in SCHEMES.items():
