@@ -436,7 +436,7 @@ __device__ __forceinline__ void residual_segment(const DecodeArgs& a, const MmaS
 }
 
 // Packed tiles [ga, gb) of stream (b, h) on the tensor cores; leaves the merged warp states
-// in red_* (synchronized). qs holds the stream's q.
+// in red_* (synchronized). Issues its first stages, then loads the stream's q into qs.
 template <int KB, int VB, int DT, int GQ, int G>
 __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem& sm, int b, int h, int64_t ga,
                                               int64_t gb) {
@@ -461,45 +461,6 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
     const int gid = lane >> 2, t = lane & 3;
     const int hh = gid >> 1, part = gid & 1;     // B column gid = (head hh, hi/lo part)
     const bool hv = GQ >= 4 || hh < GQ;   // this thread's B column belongs to a real head
-
-    // q prescale: a power of two putting max |q| in (1/2, 1]
-    float qmax_abs = 0.0f;
-    for (int i = tid; i < GQ * kD; i += kThreads) qmax_abs = fmaxf(qmax_abs, fabsf(qs[i]));
-    qmax_abs = warp_max(qmax_abs);
-    if (lane == 0) reinterpret_cast<float*>(s_misc)[1 + warp] = qmax_abs;
-    __syncthreads();
-    qmax_abs = fmaxf(fmaxf(reinterpret_cast<float*>(s_misc)[1], reinterpret_cast<float*>(s_misc)[2]),
-                     fmaxf(reinterpret_cast<float*>(s_misc)[3], reinterpret_cast<float*>(s_misc)[4]));
-    int qexp = 0;
-    if (qmax_abs > 0.0f) frexpf(qmax_abs, &qexp);
-    const float qpre = ldexpf(1.0f, -qexp), qpost = ldexpf(1.0f, qexp);
-
-    // per-thread constants of the key-side B operand (column gid, thread t's span)
-    uint32_t cY[16], cX[16], cZ[16], cB[16];
-#pragma unroll
-    for (int s = 0; s < 16; ++s) {
-        const int c0 = 32 * t + (s / NSLOT) * 2 * NSLOT + (s % NSLOT), c1 = c0 + NSLOT;
-        const float v0 = hv ? qs[(hv ? hh : 0) * kD + c0] * qpre : 0.0f;
-        const float v1 = hv ? qs[(hv ? hh : 0) * kD + c1] * qpre : 0.0f;
-        const uint32_t qh = pack_h2(v0, v1);
-        const uint32_t ql = pack_h2(v0 - h2_lo(qh), v1 - h2_hi(qh));
-        cY[s] = qh;
-        cX[s] = part ? ql : 0u;
-        cZ[s] = part ? (qh ^ 0x80008000u) : 0u;
-        cB[s] = part ? ql : qh;
-    }
-    // value side: byte / half-word selectors of this thread's four channels per channel group
-    const uint32_t g3 = static_cast<uint32_t>(gid & 3);
-    const uint32_t sel_v = VB == 2 ? (g3 | (g3 << 4) | ((4 + g3) << 8) | ((4 + g3) << 12))
-                                   : ((gid & 1) ? 0x7632u : 0x5410u);
-    const int vbyte = VB == 2 ? 4 * (gid >> 2) : 4 * (gid >> 1);   // byte offset of the word in a 32-channel block
-    const uint32_t sel_z = (gid & 1) ? 0x7632u : 0x5410u;
-
-    float m_run = -CUDART_INF_F, l_run = 0.0f;
-    float cv[8][4], cz[4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) cv[i][0] = cv[i][1] = cv[i][2] = cv[i][3] = 0.0f;
-    cz[0] = cz[1] = cz[2] = cz[3] = 0.0f;
 
     const int64_t g0 = ga, g1 = gb;
     const int64_t gfirst = g0 + warp;
@@ -566,6 +527,51 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
         cp_async_commit();
     }
     int32_t pg_ahead = kStages - 1 < n_my ? page_of(kStages - 1) : 0;
+
+    // q of the stream, loaded while the first stages are in flight (the caller's barrier
+    // has ended the previous segment's use of qs and of the stages)
+    load_q<DT, GQ>(a, qs, b, h);
+    __syncthreads();
+
+    // q prescale: a power of two putting max |q| in (1/2, 1]
+    float qmax_abs = 0.0f;
+    for (int i = tid; i < GQ * kD; i += kThreads) qmax_abs = fmaxf(qmax_abs, fabsf(qs[i]));
+    qmax_abs = warp_max(qmax_abs);
+    if (lane == 0) reinterpret_cast<float*>(s_misc)[1 + warp] = qmax_abs;
+    __syncthreads();
+    qmax_abs = fmaxf(fmaxf(reinterpret_cast<float*>(s_misc)[1], reinterpret_cast<float*>(s_misc)[2]),
+                     fmaxf(reinterpret_cast<float*>(s_misc)[3], reinterpret_cast<float*>(s_misc)[4]));
+    int qexp = 0;
+    if (qmax_abs > 0.0f) frexpf(qmax_abs, &qexp);
+    const float qpre = ldexpf(1.0f, -qexp), qpost = ldexpf(1.0f, qexp);
+
+    // per-thread constants of the key-side B operand (column gid, thread t's span)
+    uint32_t cY[16], cX[16], cZ[16], cB[16];
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+        const int c0 = 32 * t + (s / NSLOT) * 2 * NSLOT + (s % NSLOT), c1 = c0 + NSLOT;
+        const float v0 = hv ? qs[(hv ? hh : 0) * kD + c0] * qpre : 0.0f;
+        const float v1 = hv ? qs[(hv ? hh : 0) * kD + c1] * qpre : 0.0f;
+        const uint32_t qh = pack_h2(v0, v1);
+        const uint32_t ql = pack_h2(v0 - h2_lo(qh), v1 - h2_hi(qh));
+        cY[s] = qh;
+        cX[s] = part ? ql : 0u;
+        cZ[s] = part ? (qh ^ 0x80008000u) : 0u;
+        cB[s] = part ? ql : qh;
+    }
+    // value side: byte / half-word selectors of this thread's four channels per channel group
+    const uint32_t g3 = static_cast<uint32_t>(gid & 3);
+    const uint32_t sel_v = VB == 2 ? (g3 | (g3 << 4) | ((4 + g3) << 8) | ((4 + g3) << 12))
+                                   : ((gid & 1) ? 0x7632u : 0x5410u);
+    const int vbyte = VB == 2 ? 4 * (gid >> 2) : 4 * (gid >> 1);   // byte offset of the word in a 32-channel block
+    const uint32_t sel_z = (gid & 1) ? 0x7632u : 0x5410u;
+
+    float m_run = -CUDART_INF_F, l_run = 0.0f;
+    float cv[8][4], cz[4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cv[i][0] = cv[i][1] = cv[i][2] = cv[i][3] = 0.0f;
+    cz[0] = cz[1] = cz[2] = cz[3] = 0.0f;
+
 
     for (int it = 0; it < n_my; ++it) {
         {
@@ -893,8 +899,6 @@ __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_ker
         if (k.w.u != 0 && k.x1 > k.x0) {
             if (k.x0 < k.w.ng) {
                 __syncthreads();   // the previous segment is done with qs and the shared arrays
-                load_q<DT, GQ>(a, sm.qs, k.b, k.h);
-                __syncthreads();
                 group_segment<KB, VB, DT, GQ, G>(a, sm, k.b, k.h, k.x0, k.x1 < k.w.ng ? k.x1 : k.w.ng);
                 finish(0);
                 k = current();
