@@ -9,6 +9,9 @@ every query head of those sequences within 2e-3.
   * streaming append: 16 sequences, 16384-token prefill then 512 decode steps of
     append + attention, 2-bit and 4-bit; the cache is checked bit-exact after every
     flush and attention every 16 steps.
+  * the Llama-3-8B GQA batch with the other settings the benchmark takes: G = 64 with
+    R = 64, and 4-bit keys with 2-bit values; and its verification step with four draft
+    tokens (multi-query attention over the whole batch).
 """
 import numpy as np
 import pytest
@@ -97,6 +100,49 @@ def test_long_varlen_full_size():
         assert_state_equal(cache, b, ref)
         check_heads(out[b], ref, q[b], wl.softmax_scale)
 
+
+
+@pytest.mark.parametrize("kb,vb,G,R", [(2, 2, 64, 64), (4, 2, 32, 128)])
+def test_llama3_8b_gqa_full_size_variants(kb, vb, G, R):
+    wl = synth.workload(2)
+    L = wl.lengths[0]
+    kcfg, ocfg = configs(2, "bf16", 32, 8, G=G, R=R, kb=kb, vb=vb)
+    cache = kivi.KVCache(kcfg, wl.batch, L)
+    sample = (0, 63)
+    kept = prefill(cache, wl, wl.lengths, keep=sample)
+    q = wl.query(0)
+    qd = torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).to(DEV)
+    out = cache.decode(qd, softmax_scale=wl.softmax_scale).cpu().numpy()
+    assert int(cache.status.item()) == 0 and np.isfinite(out).all()
+    for b in sample:
+        ref = oracle_seq(ocfg, L, *kept[b])
+        assert_state_equal(cache, b, ref)
+        check_heads(out[b], ref, q[b], wl.softmax_scale)
+
+
+def test_verification_step_full_size():
+    """Four draft tokens appended to every sequence in one call, then their queries attend
+    causally (kivi_decode_multi_attn over the whole batch)."""
+    wl = synth.workload(2)
+    L, nq, B = wl.lengths[0], 4, wl.batch
+    cap = L + 32
+    kcfg, ocfg = configs(2, "bf16", 32, 8)
+    cache = kivi.KVCache(kcfg, B, cap)
+    sample = (0, 41, 63)
+    kept = prefill(cache, wl, wl.lengths, keep=sample)
+    kn, vn = zip(*(draw_seq(wl, b, L, nq) for b in range(B)))
+    cache.append(list(kn), list(vn))
+    qb = np.stack([np.stack([wl.query(i, b) for i in range(nq)]) for b in range(B)])   # [B][nq][Hq][D]
+    out = cache.decode_multi(dev_tensor(qb, "bf16"), softmax_scale=wl.softmax_scale).cpu().numpy()
+    assert int(cache.status.item()) == 0 and np.isfinite(out).all()
+    for b in sample:
+        K = np.concatenate([kept[b][0], host_bits(kn[b])], axis=1)
+        V = np.concatenate([kept[b][1], host_bits(vn[b])], axis=1)
+        ref = oracle_seq(ocfg, cap, K, V)
+        assert_state_equal(cache, b, ref)
+        err = float(np.max(np.abs(out[b] - ref.decode_multi(qb[b], wl.softmax_scale))))
+        record_error(err)
+        assert err <= ATTN_TOL, err
 
 @pytest.mark.parametrize("bits", [2, 4])
 def test_streaming_append_full_size(bits):
