@@ -142,12 +142,28 @@ kivi_status kivi_decode_attn(const kivi_cfg* cfg, int32_t nseq, const kivi_seq* 
     return from_cuda(kivi::launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
+// One query per sequence with a query group of 1, 2 or 4 is decode attention: it runs on
+// the persistent decode kernel (kv_len 0 stays a length error there).
+static bool multi_is_decode(const kivi_cfg* cfg, int32_t n_query) {
+    const int g = cfg->num_q_heads / cfg->num_kv_heads;
+    return n_query == 1 && (g == 1 || g == 2 || g == 4);
+}
+
+static void multi_or_decode_plan(const kivi_cfg* cfg, int32_t nseq, int32_t n_query, int32_t max_kv_len, int* chunk,
+                                 int* max_splits, size_t* cb, size_t* pb) {
+    if (multi_is_decode(cfg, n_query))
+        kivi::decode_plan(nseq, cfg->num_kv_heads, cfg->num_q_heads, cfg->head_dim, max_kv_len, chunk, max_splits, cb,
+                          pb);
+    else
+        kivi::multi_plan(nseq, cfg->num_kv_heads, cfg->num_q_heads, cfg->head_dim, n_query, max_kv_len, chunk,
+                         max_splits, cb, pb);
+}
+
 size_t kivi_decode_multi_workspace_bytes(const kivi_cfg* cfg, int32_t nseq, int32_t n_query, int32_t max_kv_len) {
     if (!cfg_ok(cfg) || nseq < 0 || max_kv_len < 0 || n_query < 1) return 0;
     int chunk, max_splits;
     size_t cb, pb;
-    kivi::multi_plan(nseq, cfg->num_kv_heads, cfg->num_q_heads, cfg->head_dim, n_query, max_kv_len, &chunk,
-                     &max_splits, &cb, &pb);
+    multi_or_decode_plan(cfg, nseq, n_query, max_kv_len, &chunk, &max_splits, &cb, &pb);
     return cb + pb;
 }
 
@@ -164,8 +180,7 @@ kivi_status kivi_decode_multi_attn(const kivi_cfg* cfg, int32_t nseq, const kivi
         return KIVI_ERR_ARG;
     kivi::DecodeArgs a;
     size_t cb, pb;
-    kivi::multi_plan(nseq, cfg->num_kv_heads, cfg->num_q_heads, cfg->head_dim, n_query, max_kv_len, &a.chunk,
-                     &a.max_splits, &cb, &pb);
+    multi_or_decode_plan(cfg, nseq, n_query, max_kv_len, &a.chunk, &a.max_splits, &cb, &pb);
     if (workspace_dev == nullptr || workspace_bytes < cb + pb) return KIVI_ERR_WORKSPACE;
     a.kb = cfg->k_bits;
     a.vb = cfg->v_bits;
@@ -186,7 +201,8 @@ kivi_status kivi_decode_multi_attn(const kivi_cfg* cfg, int32_t nseq, const kivi
     a.counters = static_cast<int32_t*>(workspace_dev);
     a.partials = reinterpret_cast<float*>(static_cast<char*>(workspace_dev) + cb);
     a.status = status_dev;
-    return from_cuda(kivi::launch_multi(a, static_cast<cudaStream_t>(stream)));
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return from_cuda(multi_is_decode(cfg, n_query) ? kivi::launch_decode(a, st) : kivi::launch_multi(a, st));
 }
 
 kivi_status kivi_seq_buffer_bytes(const kivi_cfg* cfg, int32_t cap_tokens, size_t bytes_out[8]) {

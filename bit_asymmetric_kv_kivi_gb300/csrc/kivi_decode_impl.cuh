@@ -262,7 +262,9 @@ template <int G>
 __device__ __forceinline__ SeqWork seq_work(const DecodeArgs& a, int b) {
     SeqWork w;
     w.L = a.kv_len[b];
-    w.bad = w.L < 0 || w.L > a.max_kv_len || n_packed(w.L, a.R, G) > a.seqs[b].cap_tokens;
+    // a.n_query is 0 for decode (an empty sequence gives zeros) and 1 for multi-query
+    // attention with one query (kv_len below n_query is a length error)
+    w.bad = w.L < a.n_query || w.L > a.max_kv_len || n_packed(w.L, a.R, G) > a.seqs[b].cap_tokens;
     w.np = w.ng = w.rt = w.u = 0;
     if (w.bad || w.L == 0) return w;
     w.np = n_packed(w.L, a.R, G);

@@ -249,6 +249,8 @@ size_t kivi_decode_workspace_bytes(const kivi_cfg* cfg, int32_t nseq, int32_t ma
  * more tokens than the sequence can hold; that sequence's output rows are NaN.
  * Errors: KIVI_ERR_ARG for n_query < 1; KIVI_ERR_UNSUPPORTED unless D == 128
  * and n_query * Hq / Hkv <= 32.
+ * n_query == 1 with Hq / Hkv of 1, 2 or 4 runs the kernel of kivi_decode_attn
+ * (one query attends to every token), with the length errors above.
  */
 kivi_status kivi_decode_multi_attn(const kivi_cfg* cfg, int32_t nseq, const kivi_seq* seqs_dev,
                                    const int32_t* kv_len_dev, int32_t n_query, const void* q_dev,

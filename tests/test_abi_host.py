@@ -108,7 +108,9 @@ def test_multi_query_arguments_rejected_before_launch(lib):
     P = ctypes.c_void_p
     one = P(16)
     need = lib.kivi_decode_multi_workspace_bytes(cfg, 2, 4, 5000)
-    assert need > lib.kivi_decode_multi_workspace_bytes(cfg, 2, 1, 5000) > 0
+    assert need > lib.kivi_decode_multi_workspace_bytes(cfg, 2, 2, 5000) > 0
+    # one query with a query group of 4 runs the decode kernel, with its workspace
+    assert lib.kivi_decode_multi_workspace_bytes(cfg, 2, 1, 5000) == lib.kivi_decode_workspace_bytes(cfg, 2, 5000)
     assert lib.kivi_decode_multi_workspace_bytes(cfg, 2, 0, 5000) == 0
     call = lambda nq, ws=need: lib.kivi_decode_multi_attn(cfg, 2, one, one, nq, one, one, 0.1, 5000, one, ws, one, None)
     assert call(0) == kivi.ERR_ARG

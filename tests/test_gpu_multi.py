@@ -81,17 +81,44 @@ def test_multi_query_long_sequences_many_splits(g, nq):
     check(wl, cache, refs, nq)
 
 
-def test_multi_query_one_query_matches_decode():
-    """n_query = 1 is decode attention: both entry points agree with the oracle and
-    with each other."""
-    H, g = 2, 4
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+def test_multi_query_one_query_matches_decode(g):
+    """n_query = 1 is decode attention: both entry points agree with the oracle and with
+    each other, bit for bit for query groups 1, 2 and 4 (which run the decode kernel)."""
+    H = 2
     lengths = (1, 150, 1000, 5000)
-    wl = synth.Workload("multi-one", len(lengths), g * H, H, 128, lengths, "f16", seed=410)
+    wl = synth.Workload("multi-one", len(lengths), g * H, H, 128, lengths, "f16", seed=410 + g)
     kcfg, ocfg = configs(2, "f16", g * H, H)
     cache, refs = build(wl, kcfg, ocfg, 5120)
     out = check(wl, cache, refs, 1)
     dec = cache.decode(dev_tensor(queries(wl, 1)[:, 0], "f16"), softmax_scale=wl.softmax_scale).cpu().numpy()
-    assert np.max(np.abs(out[:, 0] - dec)) <= 1e-4
+    if g <= 4:
+        assert np.array_equal(out[:, 0], dec)
+    else:
+        assert np.max(np.abs(out[:, 0] - dec)) <= 1e-4
+
+
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+def test_one_query_empty_sequence_is_a_length_error(g):
+    """With n_query = 1 an empty sequence is a length error (NaN rows, KIVI_ERR_LENGTH),
+    where decode gives zeros; the other sequences of the batch are unaffected."""
+    H = 2
+    lengths = (0, 7, 300)
+    wl = synth.Workload("one-empty", len(lengths), g * H, H, 128, lengths, "bf16", seed=450 + g)
+    kcfg, ocfg = configs(2, "bf16", g * H, H)
+    cache, refs = build(wl, kcfg, ocfg, 320)
+    qb = queries(wl, 1)
+    out = cache.decode_multi(dev_tensor(qb, "bf16"), softmax_scale=wl.softmax_scale).cpu().numpy()
+    assert int(cache.status.item()) == kivi.ERR_LENGTH
+    assert np.all(np.isnan(out[0]))
+    for b in (1, 2):
+        err = float(np.max(np.abs(out[b] - refs[b].decode_multi(qb[b], wl.softmax_scale))))
+        record_error(err)
+        assert err <= ATTN_TOL, err
+    cache.status.zero_()
+    dec = cache.decode(dev_tensor(qb[:, 0], "bf16"), softmax_scale=wl.softmax_scale).cpu().numpy()
+    assert int(cache.status.item()) == 0
+    assert np.array_equal(dec[0], np.zeros_like(dec[0]))
 
 
 @pytest.mark.parametrize("kb,vb,G,R", [(2, 2, 32, 128), (4, 2, 64, 64)])
