@@ -416,7 +416,7 @@ def run_gpu_multi(args, rank, world, local_rank):
                                f"G={G}, R={wl.residual}, {wl.dtype}", "n_query": N,
                    "l2": "flushed before every step" if flush else "no flush: the cache is larger than L2",
                    "layout": "paged" if args.paged else "contiguous"},
-        "roofline": {"bound": "hbm", "kernel": "decode_mma_kernel" if N == 1 and Hq // H in (1, 2, 4)
+        "roofline": {"bound": "hbm", "kernel": "decode_mma_kernel" if N == 1 and Hq // H in (1, 2, 4, 8)
                      else "decode_multi_kernel", "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "avg_launch_ms": avg_ms,
                      "algorithmic_bytes_per_launch": sum(nbytes) / len(nbytes), "traffic": None},
@@ -583,7 +583,7 @@ def main():
     # the decode kernel the library picks: persistent tensor-core kernel for query groups of 1, 2
     # or 4, the multi-query kernel (one query) for 8
     group = config["q_heads"] // config["kv_heads"]
-    kernel = "decode_mma_kernel" if group in (1, 2, 4) else "decode_multi_kernel"
+    kernel = "decode_mma_kernel" if group in (1, 2, 4, 8) else "decode_multi_kernel"
     per_unit = None if args.paged else NCU_TRAFFIC_BYTES_PER_UNIT.get(
         (kernel, kb, vb, wl.group, wl.residual, group, config["input_dtype"]))
     traffic = per_unit * sum(res["attn_units"]) / len(res["attn_units"]) if per_unit else None

@@ -142,11 +142,11 @@ kivi_status kivi_decode_attn(const kivi_cfg* cfg, int32_t nseq, const kivi_seq* 
     return from_cuda(kivi::launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
-// One query per sequence with a query group of 1, 2 or 4 is decode attention: it runs on
-// the persistent decode kernel (kv_len 0 stays a length error there).
+// One query per sequence with a query group of 1, 2, 4 or 8 is decode attention: it runs
+// on the persistent decode kernel (kv_len 0 stays a length error there).
 static bool multi_is_decode(const kivi_cfg* cfg, int32_t n_query) {
     const int g = cfg->num_q_heads / cfg->num_kv_heads;
-    return n_query == 1 && (g == 1 || g == 2 || g == 4);
+    return n_query == 1 && (g == 1 || g == 2 || g == 4 || g == 8);
 }
 
 static void multi_or_decode_plan(const kivi_cfg* cfg, int32_t nseq, int32_t n_query, int32_t max_kv_len, int* chunk,

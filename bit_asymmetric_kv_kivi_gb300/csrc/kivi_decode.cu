@@ -8,13 +8,16 @@ namespace kivi {
 void decode_plan(int nseq, int H, int Hq, int D, int max_kv_len, int* chunk, int* max_splits,
                  size_t* counter_bytes, size_t* partial_bytes) {
     const int gq = H > 0 ? Hq / H : 0;
-    if (gq == 1 || gq == 2 || gq == 4) {
-        // decode_mma_kernel: a ticket per stream; one record per segment, fewer than
+    if (gq == 1 || gq == 2 || gq == 4 || gq == 8) {
+        // decode_mma_kernel over S = nseq * H * (gq / 4 for gq 8, else 1) streams of up to four
+        // query heads: a ticket per stream; one record per segment, fewer than
         // 2 S + kDecodeMaxCtas of them
-        *counter_bytes = ((static_cast<size_t>(nseq) * H * sizeof(int32_t) + 255) / 256) * 256;
+        const int per = gq < 4 ? gq : 4;
+        const size_t S = static_cast<size_t>(nseq) * H * (gq / per);
+        *counter_bytes = ((S * sizeof(int32_t) + 255) / 256) * 256;
         *chunk = 0;
         *max_splits = 0;
-        *partial_bytes = (2 * static_cast<size_t>(nseq) * H + kDecodeMaxCtas) * gq * (D + 4) * sizeof(float);
+        *partial_bytes = (2 * S + kDecodeMaxCtas) * per * (D + 4) * sizeof(float);
         return;
     }
     // other query groups (up to 32): decode_multi_kernel with one query per sequence
@@ -24,7 +27,7 @@ void decode_plan(int nseq, int H, int Hq, int D, int max_kv_len, int* chunk, int
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     if (a.nseq == 0) return cudaSuccess;
     const int gq = a.Hq / a.H;
-    if (gq != 1 && gq != 2 && gq != 4) {
+    if (gq != 1 && gq != 2 && gq != 4 && gq != 8) {
         DecodeArgs m = a;
         m.n_query = 0;     // decode: one query per sequence, empty sequences give zeros
         return launch_multi(m, stream);

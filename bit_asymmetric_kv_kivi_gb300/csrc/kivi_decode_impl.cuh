@@ -9,7 +9,7 @@
 // in SRAM); "KIVI: A Tuning-Free Asymmetric 2bit Quantization for KV Cache",
 // abstract (decode is bound by loading the cache).
 //
-//  * decode_mma_kernel (Hq/Hkv = 1, 2, 4): the dot products run on the tensor
+//  * decode_mma_kernel (Hq/Hkv = 1, 2, 4, 8): the dot products run on the tensor
 //    cores (mma.sync m16n8k16, f16 operands, fp32 accumulation). A CTA owns a
 //    range of 32-token tiles of the packed tokens of one (sequence, kv head)
 //    (a key group of G = 64 is two tiles), or residual tokens of it. Each of its four warps
@@ -26,8 +26,10 @@
 //        sum_t p z_v term is a small MMA of its own.
 //    q is rescaled by a power of two so that max|q| lies in (1/2, 1]; with
 //    |x| <= 65504 no f16 operand can overflow.
-//  * Hq/Hkv = 8 runs on decode_multi_kernel (kivi_multi_impl.cuh) with one
-//    query: its CTAs share each unpacked tile between two warps of four heads.
+//    Hq/Hkv = 8 runs as two streams of four query heads per kv head, each
+//    reading the kv head's tiles (the second read mostly from L2).
+//  * other query groups (up to 32) run on decode_multi_kernel (kivi_multi_impl.cuh)
+//    with one query: its CTAs share each unpacked tile between warps of four heads.
 //
 // Every segment writes (m, l, acc[128]) for its query heads to the workspace;
 // the last CTA of a (sequence, kv head) to finish (an atomic ticket, no
@@ -412,10 +414,10 @@ __device__ __forceinline__ void load_q(const DecodeArgs& a, float* qs, int b, in
     for (int i = threadIdx.x; i < GQ * kD; i += kThreads) qs[i] = widen<DT>(q[i]) * a.scale_log2;
 }
 
-// Residual tiles [t0, t1) of stream (b, h) (tile i = tokens np + 32 i ..), lane-layout
+// Residual tiles [t0, t1) of sequence b, kv head hk (tile i = tokens np + 32 i ..), lane-layout
 // CUDA-core path; leaves the merged warp states in red_* (synchronized).
 template <int DT, int GQ, int G>
-__device__ __forceinline__ void residual_segment(const DecodeArgs& a, const MmaSmem& sm, int b, int h,
+__device__ __forceinline__ void residual_segment(const DecodeArgs& a, const MmaSmem& sm, int b, int hk,
                                                  const SeqWork& w, int64_t t0, int64_t t1) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, ring = a.R + G;
     const kivi_seq& sq = a.seqs[b];
@@ -427,8 +429,8 @@ __device__ __forceinline__ void residual_segment(const DecodeArgs& a, const MmaS
 #pragma unroll
         for (int c = 0; c < kCpl; ++c) acc[hh][c] = 0.0f;
     }
-    const uint16_t* kres = static_cast<const uint16_t*>(sq.k_res) + static_cast<int64_t>(h) * ring * kD;
-    const uint16_t* vres = static_cast<const uint16_t*>(sq.v_res) + static_cast<int64_t>(h) * ring * kD;
+    const uint16_t* kres = static_cast<const uint16_t*>(sq.k_res) + static_cast<int64_t>(hk) * ring * kD;
+    const uint16_t* vres = static_cast<const uint16_t*>(sq.v_res) + static_cast<int64_t>(hk) * ring * kD;
     for (int64_t i = t0 + warp; i < t1; i += kWarps) {
         residual_tile<DT, GQ>(kres, vres, ring, w.np + kTile * i, w.L, sm.qs, lane, m, l, acc);
         __syncwarp();
@@ -437,10 +439,11 @@ __device__ __forceinline__ void residual_segment(const DecodeArgs& a, const MmaS
     __syncthreads();
 }
 
-// Packed tiles [ga, gb) of stream (b, h) on the tensor cores; leaves the merged warp states
+// Packed tiles [ga, gb) of stream (b, h) (query heads h GQ .. h GQ + GQ - 1, kv head hk) on the
+// tensor cores; leaves the merged warp states
 // in red_* (synchronized). Issues its first stages, then loads the stream's q into qs.
 template <int KB, int VB, int DT, int GQ, int G>
-__device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem& sm, int b, int h, int64_t ga,
+__device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem& sm, int b, int h, int hk, int64_t ga,
                                               int64_t gb) {
     using Lay = MmaLayout<KB, VB>;
     constexpr int RBK = Lay::kKRowBytes, RBV = Lay::kVRowBytes;
@@ -473,10 +476,10 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
     // Tile j's code rows and value metadata sit at row-tile index rt of (32 code rows,
     // VMETA bytes of each kind of value metadata), its key scales and zeros at group index
     // kg of (256 bytes of each) from these bases: rt = j, kg = j / TPG in a contiguous
-    // sequence (bases at head h); rt = (page * H + h) * TPG + j mod TPG, kg = page * H + h
+    // sequence (bases at head hk); rt = (page * H + hk) * TPG + j mod TPG, kg = page * H + hk
     // in a paged one (bases at the pools; see group_addr), page = block_table[j / TPG].
     const bool paged = seq_paged(sq);
-    const int64_t hc = paged ? 0 : static_cast<int64_t>(h) * cap;   // head offset in tokens
+    const int64_t hc = paged ? 0 : static_cast<int64_t>(hk) * cap;   // head offset in tokens
     const unsigned char* kc_base = sq.k_codes + hc * RBK;
     const unsigned char* vc_base = sq.v_codes + hc * RBV;
     const unsigned char* ks_base = reinterpret_cast<const unsigned char*>(sq.k_scale + hc / G * kD);
@@ -502,7 +505,7 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
         unsigned char* dst = my_st + slot * STAGE;
         int64_t rt, kg;
         if (paged) {
-            kg = static_cast<int64_t>(page) * a.H + h;
+            kg = static_cast<int64_t>(page) * a.H + hk;
             rt = kg * TPG + (TPG > 1 ? j % TPG : 0);
         } else {
             rt = j;
@@ -789,14 +792,17 @@ a0 = code_slot<KB>(cw[0][w0], cws[0][w0], s0);
     __syncthreads();
 }
 
-template <int KB, int VB, int DT, int GQ, int G>
+template <int KB, int VB, int DT, int GQ, int G, int QS>
 __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_kernel(DecodeArgs a) {
     static_assert(GQ == 1 || GQ == 2 || GQ == 4, "one n8 tile holds hi and lo of up to four heads");
+    static_assert(QS == 1 || (GQ == 4 && QS == 2), "streams per kv head");
     extern __shared__ __align__(16) unsigned char smem[];
     const MmaSmem sm(smem, MmaLayout<KB, VB>::kStageBytes, GQ);
     int64_t* sched = reinterpret_cast<int64_t*>(smem);   // scan scratch: the stages are idle until the walk
     const int tid = threadIdx.x;
-    const int C = gridDim.x, c = blockIdx.x, H = a.H;
+    // streams: (sequence, h) with query heads h GQ .. h GQ + GQ - 1 and kv head h / QS; a query
+    // group of 8 is two streams of four heads per kv head (QS = 2), each reading the kv head
+    const int C = gridDim.x, c = blockIdx.x, H = a.H * QS;
 
     // sequences without work: zeros for an empty one, NaN and a status for a bad length
     for (int b = c; b < a.nseq; b += C) {
@@ -901,7 +907,7 @@ __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_ker
         if (k.w.u != 0 && k.x1 > k.x0) {
             if (k.x0 < k.w.ng) {
                 __syncthreads();   // the previous segment is done with qs and the shared arrays
-                group_segment<KB, VB, DT, GQ, G>(a, sm, k.b, k.h, k.x0, k.x1 < k.w.ng ? k.x1 : k.w.ng);
+                group_segment<KB, VB, DT, GQ, G>(a, sm, k.b, k.h, k.h / QS, k.x0, k.x1 < k.w.ng ? k.x1 : k.w.ng);
                 finish(0);
                 k = current();
             }
@@ -910,7 +916,7 @@ __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_ker
                 __syncthreads();
                 load_q<DT, GQ>(a, sm.qs, k.b, k.h);
                 __syncthreads();
-                residual_segment<DT, GQ, G>(a, sm, k.b, k.h, k.w, (u0 + kResidualWeight - 1) / kResidualWeight,
+                residual_segment<DT, GQ, G>(a, sm, k.b, k.h / QS, k.w, (u0 + kResidualWeight - 1) / kResidualWeight,
                                          (u1 + kResidualWeight - 1) / kResidualWeight);
                 finish(1);
             }
@@ -946,16 +952,16 @@ int resident_ctas(K kernel, int smem, int* cache) {
     return n;
 }
 
-template <int KB, int VB, int DT, int GQ, int G>
+template <int KB, int VB, int DT, int GQ, int G, int QS = 1>
 cudaError_t launch_mma(const DecodeArgs& a, cudaStream_t stream) {
     constexpr int smem = MmaLayout<KB, VB>::kSmemBytes(GQ);
     static int ctas[64] = {};
-    const cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<KB, VB, DT, GQ, G>,
+    const cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<KB, VB, DT, GQ, G, QS>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const int n = resident_ctas(decode_mma_kernel<KB, VB, DT, GQ, G>, smem, ctas);
+    const int n = resident_ctas(decode_mma_kernel<KB, VB, DT, GQ, G, QS>, smem, ctas);
     if (n <= 0) return cudaErrorInvalidValue;
-    decode_mma_kernel<KB, VB, DT, GQ, G><<<n, kThreads, smem, stream>>>(a);
+    decode_mma_kernel<KB, VB, DT, GQ, G, QS><<<n, kThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -965,6 +971,7 @@ cudaError_t launch_gq(const DecodeArgs& a, cudaStream_t stream) {
         case 1: return launch_mma<KB, VB, DT, 1, G>(a, stream);
         case 2: return launch_mma<KB, VB, DT, 2, G>(a, stream);
         case 4: return launch_mma<KB, VB, DT, 4, G>(a, stream);
+        case 8: return launch_mma<KB, VB, DT, 4, G, 2>(a, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -215,7 +215,8 @@ kivi_status kivi_append_flush(const kivi_cfg* cfg, int32_t nseq, const kivi_seq*
  * A sequence with kv_len 0 gets zeros. Device error KIVI_ERR_LENGTH: kv_len_b
  * outside [0, max_kv_len] or more tokens than the sequence can hold; that
  * sequence's output rows are set to NaN.
- * Query groups 1, 2 and 4 run on a persistent tensor-core kernel; any other
+ * Query groups 1, 2, 4 and 8 run on a persistent tensor-core kernel (a group of
+ * 8 as two streams of four heads, each reading the kv head); any other
  * group up to 32 on the multi-query kernel with one query.
  * Errors: KIVI_ERR_UNSUPPORTED unless D == 128 and Hq/Hkv <= 32.
  */
@@ -249,7 +250,7 @@ size_t kivi_decode_workspace_bytes(const kivi_cfg* cfg, int32_t nseq, int32_t ma
  * more tokens than the sequence can hold; that sequence's output rows are NaN.
  * Errors: KIVI_ERR_ARG for n_query < 1; KIVI_ERR_UNSUPPORTED unless D == 128
  * and n_query * Hq / Hkv <= 32.
- * n_query == 1 with Hq / Hkv of 1, 2 or 4 runs the kernel of kivi_decode_attn
+ * n_query == 1 with Hq / Hkv of 1, 2, 4 or 8 runs the kernel of kivi_decode_attn
  * (one query attends to every token), with the length errors above.
  */
 kivi_status kivi_decode_multi_attn(const kivi_cfg* cfg, int32_t nseq, const kivi_seq* seqs_dev,

@@ -162,12 +162,13 @@ def test_workload_llama2_7b_mha():
     check_decode(wl, cache, refs)
 
 
-@pytest.mark.parametrize("g", [1, 4])
+@pytest.mark.parametrize("g", [1, 4, 8])
 @pytest.mark.parametrize("shape", ["short", "one_long"])
 def test_many_streams_persistent_schedule(g, shape):
     """Hundreds of sequences (more than one per scan thread) of mixed lengths: empty ones,
     residual-only ones, a few groups; in "one_long" also one 20000-token sequence, so
-    that one stream spans many CTAs while single CTAs hold many short streams."""
+    that one stream spans many CTAs while single CTAs hold many short streams (with a
+    query group of 8, two streams of four heads per kv head)."""
     rng = np.random.default_rng(900 + g)
     n = 300
     lengths = rng.integers(0, 700, size=n)

@@ -81,10 +81,10 @@ def test_multi_query_long_sequences_many_splits(g, nq):
     check(wl, cache, refs, nq)
 
 
-@pytest.mark.parametrize("g", [1, 2, 4, 8])
+@pytest.mark.parametrize("g", [1, 2, 4, 8, 16])
 def test_multi_query_one_query_matches_decode(g):
     """n_query = 1 is decode attention: both entry points agree with the oracle and with
-    each other, bit for bit for query groups 1, 2 and 4 (which run the decode kernel)."""
+    each other, bit for bit for query groups 1, 2, 4 and 8 (which run the decode kernel)."""
     H = 2
     lengths = (1, 150, 1000, 5000)
     wl = synth.Workload("multi-one", len(lengths), g * H, H, 128, lengths, "f16", seed=410 + g)
@@ -92,7 +92,7 @@ def test_multi_query_one_query_matches_decode(g):
     cache, refs = build(wl, kcfg, ocfg, 5120)
     out = check(wl, cache, refs, 1)
     dec = cache.decode(dev_tensor(queries(wl, 1)[:, 0], "f16"), softmax_scale=wl.softmax_scale).cpu().numpy()
-    if g <= 4:
+    if g <= 8:
         assert np.array_equal(out[:, 0], dec)
     else:
         assert np.max(np.abs(out[:, 0] - dec)) <= 1e-4
