@@ -92,11 +92,11 @@ def attn_bytes(wl, lengths, kb, vb):
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per (token, kv head) of one
 # decode launch, from an ncu capture of the kernel in its current version on the 8-sequence
-# case of the Llama-3-8B GQA workload (2-bit, bf16): 209.71 MB for 8 x 8 x 32772 units.
+# case of the Llama-3-8B GQA workload (2-bit, bf16): 210.05 MB for 8 x 8 x 32772 units.
 # Keyed by (kernel, k_bits, v_bits, G, R, query group, input dtype); a configuration without
 # an entry reports traffic as null. Profile summary:
 # profiles/decode_kernels_llama3-8b-gqa_b8_ctx32768.md.
-NCU_TRAFFIC_BYTES_PER_UNIT = {("decode_mma_kernel", 2, 2, 32, 128, 4, "bf16"): 209_712_640 / (8 * 8 * 32772)}
+NCU_TRAFFIC_BYTES_PER_UNIT = {("decode_mma_kernel", 2, 2, 32, 128, 4, "bf16"): 210_048_256 / (8 * 8 * 32772)}
 
 
 def reduce_max(x: float, device=None) -> float:
