@@ -68,6 +68,10 @@ def workload_spec(args):
         wl = wl.replace(group=args.group)
     if args.residual:
         wl = wl.replace(residual=args.residual)
+    if getattr(args, "q_heads", 0):
+        if args.q_heads % wl.num_kv_heads:
+            raise SystemExit(f"--q-heads must be a multiple of the {wl.num_kv_heads} kv heads")
+        wl = wl.replace(num_q_heads=args.q_heads)
     return wl
 
 
@@ -509,6 +513,8 @@ def main():
     ap.add_argument("--v-bits", type=int, default=0, help="value code width (overrides --bits)")
     ap.add_argument("--group", type=int, default=0, help="G: 32 (default) or 64")
     ap.add_argument("--residual", type=int, default=0, help="R: a multiple of G (default 128)")
+    ap.add_argument("--q-heads", type=int, default=0,
+                    help="query heads per sequence, a multiple of the workload's kv heads (64 over 8: query group 8)")
     ap.add_argument("--workload", type=int, default=2, choices=[0, 1, 2, 3, 4],
                     help="0 tiny, 1 Llama-2-7B MHA, 2 Llama-3-8B GQA (default), 3 streaming, 4 long varlen")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -27,7 +27,8 @@
 //    q is rescaled by a power of two so that max|q| lies in (1/2, 1]; with
 //    |x| <= 65504 no f16 operand can overflow.
 //    Hq/Hkv = 8 runs as two streams of four query heads per kv head, each
-//    reading the kv head's tiles (the second read mostly from L2).
+//    reading the kv head's tiles from DRAM (the kernel is issue-bound, so
+//    the second read costs little time).
 //  * other query groups (up to 32) run on decode_multi_kernel (kivi_multi_impl.cuh)
 //    with one query: its CTAs share each unpacked tile between warps of four heads.
 //
