@@ -420,8 +420,8 @@ def run_gpu_multi(args, rank, world, local_rank):
                                f"G={G}, R={wl.residual}, {wl.dtype}", "n_query": N,
                    "l2": "flushed before every step" if flush else "no flush: the cache is larger than L2",
                    "layout": "paged" if args.paged else "contiguous"},
-        "roofline": {"bound": "hbm", "kernel": "decode_mma_kernel" if N == 1 and Hq // H in (1, 2, 4, 8)
-                     else "decode_multi_kernel", "achieved": achieved, "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": "decode_mma_kernel" if (N == 1 and Hq // H in (1, 2, 4, 8)) or
+                     (N == 2 and Hq // H == 4) else "decode_multi_kernel", "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "avg_launch_ms": avg_ms,
                      "algorithmic_bytes_per_launch": sum(nbytes) / len(nbytes), "traffic": None},
         "attn_pairs_per_s": sum(pairs) / (sum(attn_ms) / 1e3),

@@ -27,6 +27,8 @@ void decode_plan(int nseq, int H, int Hq, int D, int max_kv_len, int* chunk, int
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     if (a.nseq == 0) return cudaSuccess;
     const int gq = a.Hq / a.H;
+    // multi-query calls reach here only with streams whose heads share one query
+    if (a.n_query > 1 && (gq % 4 != 0 || gq * a.n_query != 8)) return cudaErrorInvalidValue;
     if (gq != 1 && gq != 2 && gq != 4 && gq != 8) {
         DecodeArgs m = a;
         m.n_query = 0;     // decode: one query per sequence, empty sequences give zeros

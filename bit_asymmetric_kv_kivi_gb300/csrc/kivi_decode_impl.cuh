@@ -407,19 +407,38 @@ struct MmaSmem {
     }
 };
 
-// q of stream (b, h) into shared memory, scaled by softmax_scale * log2(e); the caller's
-// earlier use of qs must be over (a CTA barrier) before this runs.
+// Streams of sequence b: h = 0 .. QS Hkv - 1, kv head h / QS. The kv head's V = nq g
+// (query, head) pairs, nq = max(n_query, 1) and g = Hq / Hkv, are numbered query-major
+// (v = i g + j), and stream h takes v0 = (h % QS) GQ .. v0 + GQ - 1, all of one query
+// i = v0 / g (GQ divides g whenever QS > 1). stream_row is the row of its first query head
+// in q and out ([nseq][nq][Hq][D]); stream_query is i.
+// (QS = 1 serves only one query per sequence and g = GQ: row b Hq + h GQ, query 0.)
+template <int GQ, int QS>
+__device__ __forceinline__ int64_t stream_row(const DecodeArgs& a, int b, int h) {
+    if constexpr (QS == 1) return static_cast<int64_t>(b) * a.Hq + h * GQ;
+    const int g = a.Hq / a.H, nq = a.n_query > 1 ? a.n_query : 1, v0 = (h % QS) * GQ;
+    return (static_cast<int64_t>(b) * nq + v0 / g) * a.Hq + (h / QS) * g + v0 % g;
+}
+template <int GQ, int QS>
+__device__ __forceinline__ int stream_query(const DecodeArgs& a, int h) {
+    if constexpr (QS == 1) return 0;
+    return (h % QS) * GQ / (a.Hq / a.H);
+}
+
+// q rows [row, row + GQ) into shared memory, scaled by softmax_scale * log2(e); the
+// caller's earlier use of qs must be over (a CTA barrier) before this runs.
 template <int DT, int GQ>
-__device__ __forceinline__ void load_q(const DecodeArgs& a, float* qs, int b, int h) {
-    const uint16_t* q = static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(b) * a.Hq + h * GQ) * kD;
+__device__ __forceinline__ void load_q(const DecodeArgs& a, float* qs, int64_t row) {
+    const uint16_t* q = static_cast<const uint16_t*>(a.q) + row * kD;
     for (int i = threadIdx.x; i < GQ * kD; i += kThreads) qs[i] = widen<DT>(q[i]) * a.scale_log2;
 }
 
 // Residual tiles [t0, t1) of sequence b, kv head hk (tile i = tokens np + 32 i ..), lane-layout
-// CUDA-core path; leaves the merged warp states in red_* (synchronized).
+// CUDA-core path, over the tokens below lend (w.L, or the causal end of a stream's query);
+// leaves the merged warp states in red_* (synchronized).
 template <int DT, int GQ, int G>
 __device__ __forceinline__ void residual_segment(const DecodeArgs& a, const MmaSmem& sm, int b, int hk,
-                                                 const SeqWork& w, int64_t t0, int64_t t1) {
+                                                 const SeqWork& w, int64_t lend, int64_t t0, int64_t t1) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, ring = a.R + G;
     const kivi_seq& sq = a.seqs[b];
     float m[GQ], l[GQ], acc[GQ][kCpl];
@@ -432,19 +451,21 @@ __device__ __forceinline__ void residual_segment(const DecodeArgs& a, const MmaS
     }
     const uint16_t* kres = static_cast<const uint16_t*>(sq.k_res) + static_cast<int64_t>(hk) * ring * kD;
     const uint16_t* vres = static_cast<const uint16_t*>(sq.v_res) + static_cast<int64_t>(hk) * ring * kD;
-    for (int64_t i = t0 + warp; i < t1; i += kWarps) {
-        residual_tile<DT, GQ>(kres, vres, ring, w.np + kTile * i, w.L, sm.qs, lane, m, l, acc);
+    const int64_t tv = (lend - w.np + kTile - 1) / kTile;   // tiles holding visible tokens
+    const int64_t te = t1 < tv ? t1 : tv;
+    for (int64_t i = t0 + warp; i < te; i += kWarps) {
+        residual_tile<DT, GQ>(kres, vres, ring, w.np + kTile * i, lend, sm.qs, lane, m, l, acc);
         __syncwarp();
     }
     store_lane_state<GQ>(warp, lane, m, l, acc, sm.red_m, sm.red_l, sm.red_acc);
     __syncthreads();
 }
 
-// Packed tiles [ga, gb) of stream (b, h) (query heads h GQ .. h GQ + GQ - 1, kv head hk) on the
-// tensor cores; leaves the merged warp states
+// Packed tiles [ga, gb) of sequence b, kv head hk, for the GQ query heads at q row qrow, on
+// the tensor cores; leaves the merged warp states
 // in red_* (synchronized). Issues its first stages, then loads the stream's q into qs.
 template <int KB, int VB, int DT, int GQ, int G>
-__device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem& sm, int b, int h, int hk, int64_t ga,
+__device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem& sm, int b, int64_t qrow, int hk, int64_t ga,
                                               int64_t gb) {
     using Lay = MmaLayout<KB, VB>;
     constexpr int RBK = Lay::kKRowBytes, RBV = Lay::kVRowBytes;
@@ -536,7 +557,7 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
 
     // q of the stream, loaded while the first stages are in flight (the caller's barrier
     // has ended the previous segment's use of qs and of the stages)
-    load_q<DT, GQ>(a, qs, b, h);
+    load_q<DT, GQ>(a, qs, qrow);
     __syncthreads();
 
     // q prescale: a power of two putting max |q| in (1/2, 1]
@@ -809,8 +830,9 @@ __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_ker
     for (int b = c; b < a.nseq; b += C) {
         const SeqWork w = seq_work<G>(a, b);
         if (w.u != 0) continue;
-        float* o = a.out + static_cast<int64_t>(b) * a.Hq * kD;
-        for (int i = tid; i < a.Hq * kD; i += kThreads) o[i] = w.bad ? CUDART_NAN_F : 0.0f;
+        const int rows = a.Hq * (QS > 1 && a.n_query > 1 ? a.n_query : 1);
+        float* o = a.out + static_cast<int64_t>(b) * rows * kD;
+        for (int i = tid; i < rows * kD; i += kThreads) o[i] = w.bad ? CUDART_NAN_F : 0.0f;
         if (w.bad && tid == 0) set_status(a.status, KIVI_ERR_LENGTH);
     }
 
@@ -893,7 +915,7 @@ __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_ker
         ss.cr0 = owner(k.Ws + k.w.ng, U_, Ceff_);
         ss.cr1 = k.w.rt > 0 ? owner(k.Ps + k.w.u - 1, U_, Ceff_) : ss.cr0 - 1;
         ss.nseg = static_cast<int>((ss.cg1 - ss.cg0 + 1) + (ss.cr1 - ss.cr0 + 1));
-        float* out_s = a.out + (static_cast<int64_t>(k.b) * a.Hq + static_cast<int64_t>(k.h) * GQ) * kD;
+        float* out_s = a.out + stream_row<GQ, QS>(a, k.b, k.h) * kD;
         finish_segment<GQ>(a, ss, 2 * ss.s + part + c, out_s, sm.red_m, sm.red_l, sm.red_acc, &sm.s_misc[0],
                            reinterpret_cast<float*>(smem) + GQ * (kWarps + 1) * kD + GQ);
     };
@@ -908,16 +930,20 @@ __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_ker
         if (k.w.u != 0 && k.x1 > k.x0) {
             if (k.x0 < k.w.ng) {
                 __syncthreads();   // the previous segment is done with qs and the shared arrays
-                group_segment<KB, VB, DT, GQ, G>(a, sm, k.b, k.h, k.h / QS, k.x0, k.x1 < k.w.ng ? k.x1 : k.w.ng);
+                group_segment<KB, VB, DT, GQ, G>(a, sm, k.b, stream_row<GQ, QS>(a, k.b, k.h), k.h / QS, k.x0,
+                                                 k.x1 < k.w.ng ? k.x1 : k.w.ng);
                 finish(0);
                 k = current();
             }
             if (k.x1 > k.w.ng) {
                 const int64_t u0 = (k.x0 > k.w.ng ? k.x0 : k.w.ng) - k.w.ng, u1 = k.x1 - k.w.ng;
                 __syncthreads();
-                load_q<DT, GQ>(a, sm.qs, k.b, k.h);
+                load_q<DT, GQ>(a, sm.qs, stream_row<GQ, QS>(a, k.b, k.h));
                 __syncthreads();
-                residual_segment<DT, GQ, G>(a, sm, k.b, k.h / QS, k.w, (u0 + kResidualWeight - 1) / kResidualWeight,
+                // the stream's query i sees tokens below L - n_query + 1 + i (L for decode)
+                const int nq = QS > 1 && a.n_query > 1 ? a.n_query : 1;
+                const int64_t lend = k.w.L - (nq - 1 - stream_query<GQ, QS>(a, k.h));
+                residual_segment<DT, GQ, G>(a, sm, k.b, k.h / QS, k.w, lend, (u0 + kResidualWeight - 1) / kResidualWeight,
                                          (u1 + kResidualWeight - 1) / kResidualWeight);
                 finish(1);
             }
@@ -968,7 +994,8 @@ cudaError_t launch_mma(const DecodeArgs& a, cudaStream_t stream) {
 
 template <int KB, int VB, int DT, int G>
 cudaError_t launch_gq(const DecodeArgs& a, cudaStream_t stream) {
-    switch (a.Hq / a.H) {
+    // (query, head) pairs per kv head: the query group, times n_query for multi-query calls
+    switch (a.Hq / a.H * (a.n_query > 1 ? a.n_query : 1)) {
         case 1: return launch_mma<KB, VB, DT, 1, G>(a, stream);
         case 2: return launch_mma<KB, VB, DT, 2, G>(a, stream);
         case 4: return launch_mma<KB, VB, DT, 4, G>(a, stream);

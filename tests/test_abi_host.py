@@ -108,7 +108,7 @@ def test_multi_query_arguments_rejected_before_launch(lib):
     P = ctypes.c_void_p
     one = P(16)
     need = lib.kivi_decode_multi_workspace_bytes(cfg, 2, 4, 5000)
-    assert need > lib.kivi_decode_multi_workspace_bytes(cfg, 2, 2, 5000) > 0
+    assert lib.kivi_decode_multi_workspace_bytes(cfg, 2, 8, 5000) > need >= lib.kivi_decode_multi_workspace_bytes(cfg, 2, 3, 5000) > 0
     # one query with a query group of 4 runs the decode kernel, with its workspace
     assert lib.kivi_decode_multi_workspace_bytes(cfg, 2, 1, 5000) == lib.kivi_decode_workspace_bytes(cfg, 2, 5000)
     assert lib.kivi_decode_multi_workspace_bytes(cfg, 2, 0, 5000) == 0
@@ -127,7 +127,7 @@ def test_decode_workspace_plans_by_query_group(lib):
     hold one ticket per (sequence, kv head) and fewer than 2 S + 1024 records of GQ (D + 4)
     floats, S the number of streams; a group of 8 runs two streams of four heads per kv
     head; other groups take the multi-query plan with one query. One-query multi-query
-    calls of groups 1 to 8 take the decode plan."""
+    calls of groups 1 to 8, and two-query calls of group 4, take the decode plan."""
     nseq, H, D = 3, 8, 128
     def tickets(S):
         return ((S * 4 + 255) // 256) * 256
@@ -137,6 +137,9 @@ def test_decode_workspace_plans_by_query_group(lib):
         want = tickets(S) + (2 * S + 1024) * per * (D + 4) * 4
         assert lib.kivi_decode_workspace_bytes(cfg, nseq, 5000) == want, g
         assert lib.kivi_decode_multi_workspace_bytes(cfg, nseq, 1, 5000) == want, g
+    # two queries at group 4: the decode plan of 8 (query, head) pairs per kv head
+    cfg4, cfg8 = (kivi.Config(num_q_heads=g * H, num_kv_heads=H).c() for g in (4, 8))
+    assert lib.kivi_decode_multi_workspace_bytes(cfg4, nseq, 2, 5000) == lib.kivi_decode_workspace_bytes(cfg8, nseq, 5000)
     cfg16 = kivi.Config(num_q_heads=16 * H, num_kv_heads=H).c()
     assert lib.kivi_decode_workspace_bytes(cfg16, nseq, 5000) == lib.kivi_decode_multi_workspace_bytes(cfg16, nseq, 1, 5000)
 

@@ -120,11 +120,13 @@ def test_llama3_8b_gqa_full_size_variants(kb, vb, G, R):
         check_heads(out[b], ref, q[b], wl.softmax_scale)
 
 
-def test_verification_step_full_size():
-    """Four draft tokens appended to every sequence in one call, then their queries attend
-    causally (kivi_decode_multi_attn over the whole batch)."""
+@pytest.mark.parametrize("nq", [2, 4])
+def test_verification_step_full_size(nq):
+    """Draft tokens (two: the decode kernel, two streams per kv head; four: the multi-query
+    kernel) appended to every sequence in one call, then their queries attend causally
+    (kivi_decode_multi_attn over the whole batch)."""
     wl = synth.workload(2)
-    L, nq, B = wl.lengths[0], 4, wl.batch
+    L, B = wl.lengths[0], wl.batch
     cap = L + 32
     kcfg, ocfg = configs(2, "bf16", 32, 8)
     cache = kivi.KVCache(kcfg, B, cap)

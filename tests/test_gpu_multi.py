@@ -54,6 +54,8 @@ CASES = [  # (k_bits, v_bits, G, R, query group, n_query)
     (2, 2, 32, 128, 8, 1), (2, 2, 32, 128, 8, 4), (4, 4, 32, 128, 4, 4), (4, 4, 32, 128, 8, 2),
     (2, 2, 64, 64, 4, 4), (4, 2, 64, 64, 2, 7), (2, 4, 32, 64, 4, 8), (4, 2, 32, 128, 1, 12),
     (2, 4, 64, 128, 8, 3), (4, 4, 64, 64, 1, 1),
+    # two queries at group 4 run on the decode kernel: two streams per kv head, one per query
+    (4, 2, 64, 64, 4, 2), (2, 4, 32, 64, 4, 2), (4, 4, 64, 128, 4, 2),
 ]
 
 
@@ -121,12 +123,13 @@ def test_one_query_empty_sequence_is_a_length_error(g):
     assert np.array_equal(dec[0], np.zeros_like(dec[0]))
 
 
-@pytest.mark.parametrize("kb,vb,G,R", [(2, 2, 32, 128), (4, 2, 64, 64)])
-def test_multi_query_after_streaming_appends_and_paged_layout(kb, vb, G, R):
+@pytest.mark.parametrize("kb,vb,G,R,nq", [(2, 2, 32, 128, 4), (4, 2, 64, 64, 4), (2, 2, 32, 128, 2),
+                                          (4, 2, 64, 64, 2)])
+def test_multi_query_after_streaming_appends_and_paged_layout(kb, vb, G, R, nq):
     """Verification steps as a speculative decoder runs them: append n_query draft tokens,
     verify them, repeat (with flushes in between); the paged cache gives the same output
     bit for bit."""
-    H, g, nq = 2, 4, 4
+    H, g = 2, 4
     lengths = (130, 300, 1000)
     wl = synth.Workload("multi-stream", len(lengths), g * H, H, 128, lengths, "bf16", seed=420 + G)
     kcfg, ocfg = configs(2, "bf16", g * H, H, G=G, R=R, kb=kb, vb=vb)
@@ -150,11 +153,13 @@ def test_multi_query_after_streaming_appends_and_paged_layout(kb, vb, G, R):
         assert np.array_equal(oc, op), step
 
 
-def test_multi_query_bad_lengths():
-    """kv_len below n_query: NaN rows and KIVI_ERR_LENGTH for that sequence only; n_query
-    * group above 32 is refused before launch."""
-    H, g, nq = 1, 4, 6
-    lengths = (5, 200)
+@pytest.mark.parametrize("nq", [6, 2])
+def test_multi_query_bad_lengths(nq):
+    """kv_len below n_query: NaN rows and KIVI_ERR_LENGTH for that sequence only (six
+    queries on the multi-query kernel, two on the decode kernel); n_query * group above 32
+    is refused before launch."""
+    H, g = 1, 4
+    lengths = (nq - 1, 200)
     wl = synth.Workload("multi-bad", len(lengths), g * H, H, 128, lengths, "f16", seed=430)
     kcfg, ocfg = configs(2, "f16", g * H, H)
     cache, refs = build(wl, kcfg, ocfg, 256)
@@ -168,12 +173,14 @@ def test_multi_query_bad_lengths():
         cache.decode_multi(dev_tensor(np.zeros((2, 9, 4, 128), np.uint16), "f16"))
 
 
-def test_decode_and_multi_query_share_one_workspace():
+@pytest.mark.parametrize("nq", [2, 3])
+def test_decode_and_multi_query_share_one_workspace(nq):
     """kivi_decode_attn and kivi_decode_multi_attn alternate on one cache and one workspace
-    (the binding keeps one per cache). With 64 (sequence, kv head) streams the tickets
-    fill the first 256 bytes exactly: neither call may leave the other's counters
+    (the binding keeps one per cache). With 64 (sequence, kv head) streams the decode
+    tickets fill the first 256 bytes exactly; two queries run the decode kernel over 128
+    streams, three the multi-query kernel. Neither call may leave the other's counters
     disturbed, and decode repeats bit for bit."""
-    H, g, nq = 8, 4, 2
+    H, g = 8, 4
     lengths = (700, 1000, 150, 3000, 64, 2000, 999, 128)
     wl = synth.Workload("shared-ws", len(lengths), g * H, H, 128, lengths, "f16", seed=440)
     kcfg, ocfg = configs(2, "f16", g * H, H)
