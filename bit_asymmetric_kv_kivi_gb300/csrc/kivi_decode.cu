@@ -5,6 +5,14 @@
 
 namespace kivi {
 
+// Tickets at the start of every workspace: one int32 per stream, with room for two streams
+// per kv head in every plan. Decode and multi-query calls may then share one workspace:
+// every plan's records start past the tickets of any plan, and every kernel leaves its
+// tickets at zero (the last CTA of a stream resets its ticket).
+static size_t ticket_bytes(int nseq, int H) {
+    return ((2 * static_cast<size_t>(nseq) * H * sizeof(int32_t) + 255) / 256) * 256;
+}
+
 void decode_plan(int nseq, int H, int Hq, int D, int max_kv_len, int* chunk, int* max_splits,
                  size_t* counter_bytes, size_t* partial_bytes) {
     const int gq = H > 0 ? Hq / H : 0;
@@ -14,7 +22,7 @@ void decode_plan(int nseq, int H, int Hq, int D, int max_kv_len, int* chunk, int
         // 2 S + kDecodeMaxCtas of them
         const int per = gq < 4 ? gq : 4;
         const size_t S = static_cast<size_t>(nseq) * H * (gq / per);
-        *counter_bytes = ((S * sizeof(int32_t) + 255) / 256) * 256;
+        *counter_bytes = ticket_bytes(nseq, H);
         *chunk = 0;
         *max_splits = 0;
         *partial_bytes = (2 * S + kDecodeMaxCtas) * per * (D + 4) * sizeof(float);
@@ -44,7 +52,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
 // virtual heads padded to whole warps of four.
 void multi_plan(int nseq, int H, int Hq, int D, int n_query, int max_kv_len, int* chunk, int* max_splits,
                 size_t* counter_bytes, size_t* partial_bytes) {
-    *counter_bytes = ((static_cast<size_t>(nseq) * H * sizeof(int32_t) + 255) / 256) * 256;
+    *counter_bytes = ticket_bytes(nseq, H);
     const int V = H > 0 ? n_query * (Hq / H) : 0;
     const int w = V <= 4 ? 1 : V <= 8 ? 2 : V <= 16 ? 4 : 8;
     const int64_t eighth = (static_cast<int64_t>(max_kv_len) + 7) / 8;

@@ -123,18 +123,18 @@ def test_multi_query_arguments_rejected_before_launch(lib):
 
 
 def test_decode_workspace_plans_by_query_group(lib):
-    """The workspace each query group needs, from the documented plans: groups 1, 2 and 4
-    hold one ticket per (sequence, kv head) and fewer than 2 S + 1024 records of GQ (D + 4)
-    floats, S the number of streams; a group of 8 runs two streams of four heads per kv
-    head; other groups take the multi-query plan with one query. One-query multi-query
-    calls of groups 1 to 8, and two-query calls of group 4, take the decode plan."""
+    """The workspace each query group needs, from the documented plans: tickets for two
+    streams per (sequence, kv head) in every plan, then fewer than 2 S + 1024 records of
+    GQ (D + 4) floats, S the number of streams; a group of 8 runs two streams of four heads
+    per kv head; other groups take the multi-query plan with one query. One-query
+    multi-query calls of groups 1 to 8, and two-query calls of group 4, take the decode
+    plan."""
     nseq, H, D = 3, 8, 128
-    def tickets(S):
-        return ((S * 4 + 255) // 256) * 256
+    tickets = ((2 * nseq * H * 4 + 255) // 256) * 256
     for g in (1, 2, 4, 8):
         cfg = kivi.Config(num_q_heads=g * H, num_kv_heads=H).c()
         per, S = min(g, 4), nseq * H * (g // min(g, 4))
-        want = tickets(S) + (2 * S + 1024) * per * (D + 4) * 4
+        want = tickets + (2 * S + 1024) * per * (D + 4) * 4
         assert lib.kivi_decode_workspace_bytes(cfg, nseq, 5000) == want, g
         assert lib.kivi_decode_multi_workspace_bytes(cfg, nseq, 1, 5000) == want, g
     # two queries at group 4: the decode plan of 8 (query, head) pairs per kv head

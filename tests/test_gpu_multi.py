@@ -196,3 +196,32 @@ def test_decode_and_multi_query_share_one_workspace(nq):
         err = float(np.max(np.abs(first[b] - r.decode(wl.query(5)[b], wl.softmax_scale))))
         record_error(err)
         assert err <= ATTN_TOL, err
+
+
+@pytest.mark.parametrize("g,nq", [(4, 2), (8, 2)])
+def test_plans_with_different_stream_counts_share_one_workspace(g, nq):
+    """Calls whose plans count different streams alternate on one workspace: two queries
+    at group 4 run the decode kernel with two streams per kv head next to one-stream
+    decode, and group 8 decodes with two streams next to the multi-query kernel. The
+    sequences are long enough that the first CTA writes a partial record right after the
+    tickets, so a record region overlapping another plan's tickets would corrupt the next
+    call (8000 tokens: about 41 schedule units per CTA, past a stream's 32 units of setup,
+    so the first CTA holds packed tiles of stream 0; the multi-query kernel splits each
+    sequence nine ways). Every output stays within the bound, and decode repeats bit for
+    bit."""
+    H = 8
+    lengths = (8000,) * 6 + (7000, 6500)
+    wl = synth.Workload("plans-ws", len(lengths), g * H, H, 128, lengths, "f16", seed=460 + g)
+    kcfg, ocfg = configs(2, "f16", g * H, H)
+    cache, refs = build(wl, kcfg, ocfg, 8000)
+    q1 = dev_tensor(wl.query(7), "f16")
+    first = cache.decode(q1, softmax_scale=wl.softmax_scale).cpu().numpy()
+    for step in range(3):
+        check(wl, cache, refs, nq, step=step)
+        again = cache.decode(q1, softmax_scale=wl.softmax_scale).cpu().numpy()
+        assert int(cache.status.item()) == 0
+        assert np.array_equal(first, again), step
+    for b in (0, 7):
+        err = float(np.max(np.abs(first[b] - refs[b].decode(wl.query(7)[b], wl.softmax_scale))))
+        record_error(err)
+        assert err <= ATTN_TOL, err
