@@ -46,3 +46,16 @@ def test_single_process_without_group():
     import bench
     assert bench.reduce_max(3.5) == 3.5
     assert bench.job_throughput(100.0, 1, 1000.0) == 100.0
+
+
+def test_workload_options_set_query_heads_and_sizes():
+    """bench.py's workload options: --q-heads changes only the query heads (64 over the
+    8 kv heads of the Llama-3-8B shape is query group 8) and must be a multiple of the kv
+    heads; --batch / --context set the shape."""
+    import argparse
+    import bench
+    args = argparse.Namespace(workload=2, batch=16, context=0, bits=0, group=0, residual=0, q_heads=64)
+    wl = bench.workload_spec(args)
+    assert (wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.lengths) == (16, 64, 8, (32768,) * 16)
+    with pytest.raises(SystemExit):
+        bench.workload_spec(argparse.Namespace(**{**vars(args), "q_heads": 12}))
