@@ -98,8 +98,7 @@ def attn_bytes(wl, lengths, kb, vb):
 # decode launch, from an ncu capture of the kernel in its current version on the 8-sequence
 # case of the Llama-3-8B GQA workload (2-bit, bf16): 210.05 MB for 8 x 8 x 32772 units.
 # Keyed by (kernel, k_bits, v_bits, G, R, query group, input dtype); a configuration without
-# an entry reports traffic as null. Profile summary:
-# profiles/decode_kernels_llama3-8b-gqa_b8_ctx32768.md.
+# an entry reports traffic as null.
 NCU_TRAFFIC_BYTES_PER_UNIT = {("decode_mma_kernel", 2, 2, 32, 128, 4, "bf16"): 210_048_256 / (8 * 8 * 32772)}
 
 
@@ -586,8 +585,8 @@ def main():
     avg_bytes = sum(res["attn_bytes"]) / len(res["attn_bytes"])
     achieved = avg_bytes / (avg_attn_ms / 1e3) / 1e9
     peak, peak_kind = measured_hbm_peak()
-    # the decode kernel the library picks: persistent tensor-core kernel for query groups of 1, 2
-    # or 4, the multi-query kernel (one query) for 8
+    # the decode kernel the library picks: the persistent tensor-core kernel for query groups of
+    # 1, 2, 4 and 8, the multi-query kernel (one query) for any other group
     group = config["q_heads"] // config["kv_heads"]
     kernel = "decode_mma_kernel" if group in (1, 2, 4, 8) else "decode_multi_kernel"
     per_unit = None if args.paged else NCU_TRAFFIC_BYTES_PER_UNIT.get(

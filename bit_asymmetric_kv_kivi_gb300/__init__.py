@@ -81,6 +81,8 @@ def lib() -> ctypes.CDLL:
             L.kivi_seq_bytes.restype = ctypes.c_int64
             L.kivi_n_packed.argtypes = [CFG, ctypes.c_int64]
             L.kivi_n_packed.restype = ctypes.c_int64
+            L.kivi_kv_bytes_plain.argtypes = [I32, I32, I32, I32, ctypes.c_int64, ctypes.c_int64]
+            L.kivi_kv_bytes_plain.restype = ctypes.c_int64
             L.kivi_status_string.argtypes = [I32]
             L.kivi_status_string.restype = ctypes.c_char_p
             L.kivi_abi_version.argtypes = []
@@ -91,6 +93,11 @@ def lib() -> ctypes.CDLL:
 
 def status_string(status: int) -> str:
     return lib().kivi_status_string(int(status)).decode()
+
+
+def kv_bytes_plain(layers: int, num_kv_heads: int, head_dim: int, bits: int, tokens: int, batch: int = 1) -> int:
+    """KV-cache bytes with no quantization metadata (kivi_kv_bytes_plain); -1 on bad input."""
+    return int(lib().kivi_kv_bytes_plain(layers, num_kv_heads, head_dim, bits, tokens, batch))
 
 
 def _check(status: int, where: str) -> None:

@@ -228,6 +228,22 @@ int64_t kivi_seq_bytes(const kivi_cfg* cfg, int32_t cap_tokens) {
     return total;
 }
 
+int64_t kivi_kv_bytes_plain(int32_t layers, int32_t num_kv_heads, int32_t head_dim, int32_t bits, int64_t tokens,
+                            int64_t batch) {
+    if (bits != 2 && bits != 4 && bits != 8 && bits != 16) return -1;
+    if (layers < 0 || num_kv_heads < 0 || head_dim < 0 || tokens < 0 || batch < 0) return -1;
+    // bits of one token of one layer (K and V), then bytes: every factor is checked against
+    // overflow before it is applied
+    const int64_t lim = INT64_MAX;
+    int64_t v = 2 * static_cast<int64_t>(num_kv_heads) * head_dim * bits;   // < 2^49
+    const int64_t f[3] = {layers, tokens, batch};
+    for (int i = 0; i < 3; ++i) {
+        if (f[i] != 0 && v > lim / f[i]) return -1;
+        v *= f[i];
+    }
+    return v / 8;
+}
+
 int64_t kivi_n_packed(const kivi_cfg* cfg, int64_t kv_len) {
     if (!cfg_ok(cfg) || kv_len < 0) return -1;
     return kivi::n_packed(kv_len, cfg->residual, cfg->group);

@@ -44,6 +44,8 @@
 #pragma once
 #include <math_constants.h>
 
+#include <atomic>
+
 #include "kivi_internal.cuh"
 
 namespace kivi {
@@ -255,6 +257,7 @@ constexpr int kResidualWeight = 4;
 constexpr int kStreamOverhead = 32;      // units charged per stream for its setup and merge
 constexpr int kMinUnitsPerCta = 8;
 constexpr int kMaxCtas = kDecodeMaxCtas;
+constexpr int kMaxDevices = 64;     // devices whose launch sizes are cached
 
 struct SeqWork {
     int64_t L, np, ng, rt, u;   // tokens, packed tokens, packed tiles, residual tiles, units
@@ -334,7 +337,7 @@ __device__ __forceinline__ void finish_segment(const DecodeArgs& a, const Stream
     // running max and the weights exp2(m - M) of all records at once (loads in parallel),
     // then every output sums its records with independent loads
     const int ng_cnt = static_cast<int>(ss.cg1 - ss.cg0 + 1);
-    auto rec_at = [&](int k, int hh) {
+    auto rec_at = [&](int k, int hh) -> float* {
         const int64_t idx = k < ng_cnt ? 2 * ss.s + ss.cg0 + k : 2 * ss.s + 1 + ss.cr0 + (k - ng_cnt);
         return a.partials + (idx * GQ + hh) * rec;
     };
@@ -361,6 +364,13 @@ __device__ __forceinline__ void finish_segment(const DecodeArgs& a, const Stream
 #pragma unroll 8
         for (int k = 0; k < ss.nseg; ++k) num = fmaf(scratch[k * GQ + hh], __ldcg(rec_at(k, hh) + d), num);
         out_s[i] = num / scratch[-GQ + hh];
+    }
+    // the stream's records back to zero (each segment's GQ records are contiguous): every call
+    // leaves the workspace as it found it (all zero), whatever plan the next call has
+    __syncthreads();
+    for (int k = 0; k < ss.nseg; ++k) {
+        float4* z = reinterpret_cast<float4*>(rec_at(k, 0));
+        for (int i = tid; i < GQ * static_cast<int>(rec) / 4; i += kThreads) z[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     }
     if (tid == 0) a.counters[ss.s] = 0;
 }
@@ -963,29 +973,31 @@ __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_ker
     }
 }
 
-// Resident CTAs of a kernel on the current device (SM count x blocks per SM), cached per
-// device; at most kMaxCtas.
+// Resident CTAs of a kernel on the current device (SM count x blocks per SM), at most
+// kMaxCtas. The first launch of an instantiation on a device raises its dynamic shared
+// memory limit, asks the occupancy calculator and caches the count in an atomic per-device
+// slot; later launches read the slot. Host threads that race on a first launch compute and
+// store the same value.
 template <typename K>
-int resident_ctas(K kernel, int smem, int* cache) {
+int resident_ctas(K kernel, int smem, std::atomic<int>* cache) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (cache[dev] > 0) return cache[dev];
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    const int have = cache[dev].load(std::memory_order_relaxed);
+    if (have > 0) return have;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
     int sms = 0, per_sm = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem) != cudaSuccess) return 0;
     int n = sms * (per_sm > 0 ? per_sm : 1);
     n = n > kMaxCtas ? kMaxCtas : n;
-    cache[dev] = n;
+    cache[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
 template <int KB, int VB, int DT, int GQ, int G, int QS = 1>
 cudaError_t launch_mma(const DecodeArgs& a, cudaStream_t stream) {
     constexpr int smem = MmaLayout<KB, VB>::kSmemBytes(GQ);
-    static int ctas[64] = {};
-    const cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<KB, VB, DT, GQ, G, QS>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
+    static std::atomic<int> ctas[kMaxDevices];
     const int n = resident_ctas(decode_mma_kernel<KB, VB, DT, GQ, G, QS>, smem, ctas);
     if (n <= 0) return cudaErrorInvalidValue;
     decode_mma_kernel<KB, VB, DT, GQ, G, QS><<<n, kThreads, smem, stream>>>(a);

@@ -580,15 +580,31 @@ __global__ void __launch_bounds__(32 * W, W >= 4 ? 12 / W : (W == 2 ? 5 : 8)) de
         }
         out_row(v)[d] = num / den;
     }
+    // every record of this (sequence, kv head), padding heads included, back to zero: each call
+    // leaves the workspace as it found it (all zero), whatever plan the next call has
+    __syncthreads();
+    {
+        float4* z = reinterpret_cast<float4*>(a.partials + rec_base * (4 * W) * rec_stride);
+        const int64_t n4 = static_cast<int64_t>(nsplit) * (4 * W) * rec_stride / 4;
+        for (int64_t i = tid; i < n4; i += NT) z[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
     if (tid == 0) a.counters[static_cast<int64_t>(b) * a.H + h] = 0;
 }
 
 template <int KB, int VB, int DT, int W, int G>
 cudaError_t launch_multi_w(const DecodeArgs& a, cudaStream_t stream) {
     constexpr int smem = MultiLayout<KB, VB, W>::kBytes;
-    const cudaError_t e = cudaFuncSetAttribute(decode_multi_kernel<KB, VB, DT, W, G>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
+    // the shared memory limit is raised once per device (an atomic flag per device; racing
+    // first launches set the same value)
+    static std::atomic<int> raised[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (raised[dev].load(std::memory_order_relaxed) == 0) {
+        const cudaError_t e = cudaFuncSetAttribute(decode_multi_kernel<KB, VB, DT, W, G>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        raised[dev].store(1, std::memory_order_relaxed);
+    }
     decode_multi_kernel<KB, VB, DT, W, G><<<dim3(a.max_splits, a.H, a.nseq), 32 * W, smem, stream>>>(a);
     return cudaGetLastError();
 }

@@ -34,7 +34,10 @@ std::mutex g_mutex;
 void* g_ws_ptr[kMaxDevices] = {};   // device address of g_static_ws, per device
 
 // Device address of the array on the current device, looked up once per
-// device (with that device current) and cached.
+// device (with that device current) and cached for the life of the process.
+// cudaDeviceReset tears down the context that holds the array, so after it the
+// cached address is stale: a process that resets a device must not call
+// kivi_decode_attn_static on that device again.
 kivi_status static_workspace(void** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KIVI_ERR_CUDA;

@@ -17,9 +17,12 @@
  *    caller, 16-byte aligned. Configuration structs (kivi_cfg) are host memory.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream). All work is enqueued on it; no entry point synchronizes, and
- *    the library allocates no device memory, keeps no global state between
- *    calls and is safe to call from several host threads (the one exception,
- *    kivi_decode_attn_static, is described at its declaration).
+ *    the library allocates no device memory. The only state it keeps between
+ *    calls is per-device launch settings (each attention kernel's shared
+ *    memory limit, raised on its first launch on a device, and its count of
+ *    resident CTAs), held in atomic per-device slots, so it is safe to call
+ *    from several host threads (kivi_decode_attn_static, described at its
+ *    declaration, adds a device array that its calls share).
  *  - Argument errors are found on the host before anything is launched and
  *    returned synchronously (KIVI_ERR_ARG, KIVI_ERR_UNSUPPORTED,
  *    KIVI_ERR_WORKSPACE). A failed launch returns KIVI_ERR_CUDA.
@@ -210,7 +213,10 @@ kivi_status kivi_append_flush(const kivi_cfg* cfg, int32_t nseq, const kivi_seq*
  *   max_kv_len host bound on every kv_len_b (sizes the grid and the workspace)
  *   workspace_dev, workspace_bytes: at least kivi_decode_workspace_bytes()
  *              bytes, zero-filled before its first use; every call leaves it
- *              zero-filled again. Calls that share a workspace must not overlap.
+ *              zero-filled again (the kernels reset their split tickets and
+ *              clear the partial records they merge), so one workspace serves
+ *              any sequence of decode and multi-query calls whose sizes it
+ *              covers. Calls that share a workspace must not overlap.
  *   status_dev one int32 (may be NULL)
  * A sequence with kv_len 0 gets zeros. Device error KIVI_ERR_LENGTH: kv_len_b
  * outside [0, max_kv_len] or more tokens than the sequence can hold; that
@@ -280,7 +286,8 @@ size_t kivi_decode_multi_workspace_bytes(const kivi_cfg* cfg, int32_t nseq, int3
  * max_kv_len) exceeds that size return KIVI_ERR_WORKSPACE and launch nothing.
  * The first call on each device looks up the array's device address (with
  * that device current) and caches it; make that first call before any stream
- * capture. The entry point calls no cudaMalloc, cudaFree or other allocating
+ * capture. The cached address belongs to the device's primary context: after
+ * cudaDeviceReset on a device, do not call this entry point on it again. The entry point calls no cudaMalloc, cudaFree or other allocating
  * routine. All calls on a device share the array: each call clears the part
  * that must start at zero (with an asynchronous memset on `stream`), and calls
  * that overlap on the GPU race and give wrong results.
@@ -302,6 +309,20 @@ kivi_status kivi_seq_buffer_bytes(const kivi_cfg* cfg, int32_t cap_tokens, size_
 
 /* Total bytes of one sequence's buffers (the sum of the above), -1 on error. */
 int64_t kivi_seq_bytes(const kivi_cfg* cfg, int32_t cap_tokens);
+
+/*
+ * KV-cache bytes with no quantization metadata and no residual window: the
+ * closed form the pages use for cache size, 2 (K and V) x layers x kv_heads x
+ * head_dim x bits / 8 x tokens x batch ("KV-Cache Quantization: I Ran the
+ * Experiments So You Don't Have To", section "Component 1", the table under
+ * Figure 3 and the figures beside it: 128 KiB per token for Llama-3-8B at fp16,
+ * about 275 GB for 64 requests of 32K tokens; section "The memory math
+ * (verified)"). bits is 2, 4, 8 or 16. Compare kivi_seq_bytes, which counts the
+ * scales, zeros and ring this library stores. Returns -1 for bits outside that
+ * set, a negative size, or a product beyond int64.
+ */
+int64_t kivi_kv_bytes_plain(int32_t layers, int32_t num_kv_heads, int32_t head_dim, int32_t bits, int64_t tokens,
+                            int64_t batch);
 
 /* n_packed(L) for this config (see above), -1 on a bad config or L < 0. */
 int64_t kivi_n_packed(const kivi_cfg* cfg, int64_t kv_len);

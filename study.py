@@ -1,5 +1,8 @@
 """Attention error of four quantization axes on a synthetic outlier-structured cache.
 
+An analysis script that sits beside bench.py: it drives the library's codec entry
+points with the seeded generators of synth/ and is not part of the library package.
+
 The comparison of "KV-Cache Quantization: I Ran the Experiments So You Don't Have To",
 Component 2 (Figure 4): keys and values each quantized along the tokens of a channel
 ("per-channel": this library's key quantizer, kivi_quant_keys) or along the channels of a
@@ -10,7 +13,7 @@ computed in fp64. The page does not define its error; here three are reported pe
 head and averaged: relative L2 error of the scores, total variation of the softmax
 probabilities, and relative L2 error of the attention output.
 
-    python -m bit_asymmetric_kv_kivi_gb300.study --workload 1 --seqs 2
+    python study.py --workload 1 --seqs 2
 """
 from __future__ import annotations
 
@@ -20,7 +23,8 @@ import json
 import numpy as np
 import torch
 
-from . import BF16, F16, Config, GROUP, quant_keys, quant_values
+import synth
+from bit_asymmetric_kv_kivi_gb300 import BF16, F16, Config, GROUP, quant_keys, quant_values
 
 SCHEMES = {
     "uniform, K and V per-token": ("token", "token"),
@@ -73,7 +77,6 @@ def run(workload: int = 1, seqs: int = 2, tokens: int | None = None, bits_list=(
     """One row per (scheme, bits): the three mean errors over `seqs` sequences x every kv
     head (one decode query per head: the first query head of its group), with groups of
     `group` tokens (keys) or channels (values)."""
-    import synth   # the seeded generators shared with the tests and the bench
     wl = synth.workload(workload)
     T = (min(tokens or wl.lengths[0], wl.lengths[0]) // group) * group
     H, D = wl.num_kv_heads, wl.head_dim

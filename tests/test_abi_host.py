@@ -178,3 +178,54 @@ def test_seq_record_layout_matches_header(tmp_path):
     assert size == kivi.SEQ_STRUCT_BYTES
     assert cap_off == 8 * len(kivi.SEQ_FIELDS) and flags_off == cap_off + 4 and table_off == cap_off + 8
     assert paged == kivi.SEQ_PAGED
+
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "llama3_8b_kv_bytes.txt")
+
+
+def test_kv_bytes_plain_matches_the_pages_llama3_8b_table(lib):
+    """kivi_kv_bytes_plain against the table printed under Figure 3 of "KV-Cache
+    Quantization: I Ran the Experiments So You Don't Have To", "Component 1"
+    (Llama-3-8B: 32 layers, 8 kv heads, head_dim 128; decimal GB, one request)."""
+    rows = [[float(x) for x in line.split()] for line in open(GOLDEN)
+            if line.strip() and not line.startswith("#")]
+    assert len(rows) == 4
+    for ctx, *gb in rows:
+        for bits, want in zip((16, 8, 4, 2), gb):
+            got = kivi.kv_bytes_plain(32, 8, 128, bits, int(ctx)) / 1e9
+            assert round(got, 2) == want, (ctx, bits, got, want)
+
+
+def test_kv_bytes_plain_prose_figures(lib):
+    """The same section's prose: 128 KiB per token at fp16, about 275 GB for 64 requests at
+    32K tokens and about 69 GB at 4-bit; "The memory math (verified)": 17.18 GB (fp16) and
+    4.29 GB (4-bit) at 131072 tokens."""
+    assert kivi.kv_bytes_plain(32, 8, 128, 16, 1) == 128 * 1024
+    assert round(kivi.kv_bytes_plain(32, 8, 128, 16, 32768, 64) / 1e9) == 275
+    assert round(kivi.kv_bytes_plain(32, 8, 128, 4, 32768, 64) / 1e9) == 69
+    assert round(kivi.kv_bytes_plain(32, 8, 128, 16, 131072) / 1e9, 2) == 17.18
+    assert round(kivi.kv_bytes_plain(32, 8, 128, 4, 131072) / 1e9, 2) == 4.29
+
+
+def test_kv_bytes_plain_rejects_bad_input(lib):
+    for bad in [(32, 8, 128, 3, 1, 1), (32, 8, 128, 32, 1, 1), (-1, 8, 128, 2, 1, 1), (32, 8, 128, 2, -5, 1),
+                (32, 8, 128, 16, 1 << 40, 1 << 30)]:
+        assert kivi.kv_bytes_plain(*bad) == -1, bad
+    assert kivi.kv_bytes_plain(32, 8, 128, 2, 0, 7) == 0
+
+
+def test_no_unsynchronised_static_state_in_the_library_sources():
+    """The header says the only state kept between calls is per-device launch settings in
+    atomic slots. Every function-scope or file-scope `static` variable in the CUDA sources
+    must therefore be constant, atomic, or device memory (the fixed workspace of
+    kivi_decode_attn_static, whose host-side address cache is guarded by a mutex)."""
+    csrc = os.path.join(os.path.dirname(_build.__file__), "csrc")
+    pat = re.compile(r"\bstatic\s+(?!constexpr\b|const\b|inline\b|__device__\b|__host__\b|__forceinline__\b)"
+                     r"([A-Za-z_][\w:<>]*)\s+([A-Za-z_]\w*)\s*(\[|=|;)")
+    bad = []
+    for name in sorted(os.listdir(csrc)):
+        text = re.sub(r"//[^\n]*", "", open(os.path.join(csrc, name)).read())
+        for m in pat.finditer(text):
+            if not m.group(1).startswith("std::atomic"):
+                bad.append(f"{name}: {m.group(0)}")
+    assert not bad, bad

@@ -3,7 +3,7 @@ through the oracle's quantizers (the codes are bit-exact, so the dequantized cac
 identical; only fp64 summation order differs)."""
 import pytest
 
-from bit_asymmetric_kv_kivi_gb300 import study
+import study
 from test_oracle_study import study as oracle_study
 
 pytestmark = pytest.mark.gpu
