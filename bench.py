@@ -217,7 +217,9 @@ def step_inputs(wl, L0s, n_steps, device):
     return kn, vn, q
 
 
-def run_gpu(args, rank, world, local_rank):
+def run_gpu(args, rank, world, local_rank, full=True):
+    """The timed decode steps of one workload. full=False (the per-workload lines) skips the
+    end-to-end leg."""
     import torch
     import bit_asymmetric_kv_kivi_gb300 as kivi
 
@@ -320,12 +322,13 @@ def run_gpu(args, rank, world, local_rank):
     units_per_step = [wl.num_kv_heads * sum(ls) for ls in lens_per_step]
 
     # ------------------------------------------------------------ end to end through the public API
-    e2e = run_e2e(args, cache, wl, device, [L + n_steps for L in L0s], max_len_final + args.steps, out)
+    e2e = run_e2e(args, cache, wl, device, [L + n_steps for L in L0s], max_len_final + args.steps, out) if full \
+        else None
 
     res = {
         "total_ms": total_ms, "attn_ms": attn_ms, "kv_tokens": kv_tokens, "attn_bytes": bytes_per_step,
         "attn_units": units_per_step,
-        "clocks": clk.summary(), "e2e": e2e, "launches_per_step": 4, "cap": cap, "flush": flush,
+        "clocks": clk.summary(), "e2e": e2e, "launches_per_step": 2, "cap": cap, "flush": flush,
         "prefill": {"ms": prefill_ms, "algorithmic_bytes": prefill_bytes,
                     "GBps": prefill_bytes / (prefill_ms / 1e3) / 1e9 if prefill_ms > 0 else None},
     }
@@ -424,7 +427,7 @@ def run_gpu_multi(args, rank, world, local_rank):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "avg_launch_ms": avg_ms,
                      "algorithmic_bytes_per_launch": sum(nbytes) / len(nbytes), "traffic": None},
         "attn_pairs_per_s": sum(pairs) / (sum(attn_ms) / 1e3),
-        "gpu_launches": 4 * args.steps, "clocks": clk.summary(),
+        "gpu_launches": (2 if N <= wl.group else 4) * args.steps, "clocks": clk.summary(),
     }
 
 
@@ -465,6 +468,42 @@ def run_e2e(args, cache, wl, device, L_start, max_len, out_dev):
             "d2h_bytes_per_step": d2h, "ms_per_step": ms / n, "kv_tokens": kv_tokens, "steps": n}
 
 
+# ---------------------------------------------------------------- every workload in one line
+# The sub-lines of the default run: each workload's decode steps (append + attention) timed
+# as in the headline, fewer steps, no end-to-end leg. Workload 3 runs its 512 decode steps
+# after the 16384-token prefill, at 2 and 4 bits.
+SUB_WORKLOADS = (("0 tiny decode", 0, 0, 200), ("1 Llama-2-7B MHA", 1, 0, 200),
+                 ("3 streaming 2-bit", 3, 2, 507), ("3 streaming 4-bit", 3, 4, 507),
+                 ("4 long varlen", 4, 0, 100))
+
+
+def run_workloads(args, rank, world, local_rank):
+    import torch
+    lines = {}
+    for name, wi, bits, steps in SUB_WORKLOADS:
+        sub = argparse.Namespace(**vars(args))
+        sub.workload, sub.steps, sub.warmup = wi, steps, 5
+        sub.batch = sub.context = sub.q_heads = sub.group = sub.residual = sub.k_bits = sub.v_bits = 0
+        sub.bits, sub.paged = bits, False
+        res, wl = run_gpu(sub, rank, world, local_rank, full=False)
+        kb, vb = kv_bits(sub, wl)
+        avg_ms = sum(res["attn_ms"]) / len(res["attn_ms"])
+        avg_bytes = sum(res["attn_bytes"]) / len(res["attn_bytes"])
+        peak, peak_kind = measured_hbm_peak()
+        gbps = avg_bytes / (avg_ms / 1e3) / 1e9
+        lines[name] = {
+            "workload": f"{WORKLOAD_NAMES[wi]}: {wl.batch} sequences, {wl.num_q_heads} query / {wl.num_kv_heads} kv "
+                        f"heads, {kb}/{vb}-bit K/V, G={wl.group}, R={wl.residual}, {wl.dtype}",
+            "steps": steps, "kv_tokens_per_s": res["kv_tokens"] / (res["total_ms"] / 1e3),
+            "ms_per_step": res["total_ms"] / steps, "attn_kv_tokens_per_s": (res["kv_tokens"] / steps) / (avg_ms / 1e3),
+            "attn_GBps": gbps, "frac": gbps / peak, "peak": peak, "peak_kind": peak_kind,
+            "avg_launch_ms": avg_ms, "algorithmic_bytes_per_launch": avg_bytes,
+            "l2": "flushed before every step" if res["flush"] else "no flush: the cache is larger than L2"}
+        del res
+        torch.cuda.empty_cache()
+    return lines
+
+
 # ---------------------------------------------------------------- CPU oracle arm
 def oracle_sample(wl, n_steps, kb, vb, budget_s=20.0):
     """The oracle on a bounded sample of the workload: one sequence (all kv and query
@@ -498,6 +537,60 @@ def oracle_sample(wl, n_steps, kb, vb, budget_s=20.0):
     return tokens / dt, threads, desc, dt
 
 
+def oracle_parts(wl, kb, vb, runs=3, quant_tokens=2048):
+    """The oracle timed in its two parts on sequence 0 of the workload, median of `runs`
+    each: quantization (one append of `quant_tokens` tokens, every kv head, to an empty
+    cache: codec, packing and the ring) and fp64 decode attention (every query head over the
+    workload's context, prefilled untimed). Threads as the process runs them (OpenMP)."""
+    import oracle
+    oracle.build()
+    L0 = wl.lengths[0]
+    ocfg = oracle.Cfg(k_bits=kb, v_bits=vb, group=wl.group, residual=wl.residual, num_q_heads=wl.num_q_heads,
+                      num_kv_heads=wl.num_kv_heads, dtype=oracle.BF16 if wl.dtype == "bf16" else oracle.F16)
+    nq = min(quant_tokens, L0)
+    Kq, Vq = wl.kv_seq(0, 0, nq)
+    quant = []
+    for _ in range(runs):
+        seq = oracle.SeqCache(ocfg, ((nq + wl.group - 1) // wl.group) * wl.group)
+        t0 = time.perf_counter()
+        assert seq.append(Kq, Vq) == oracle.OK
+        quant.append(time.perf_counter() - t0)
+    cap = ((L0 + wl.group - 1) // wl.group) * wl.group
+    seq = oracle.SeqCache(ocfg, cap)
+    K, V = wl.kv_seq(0, 0, L0)
+    assert seq.append(K, V) == oracle.OK
+    attn = []
+    for r in range(runs):
+        t0 = time.perf_counter()
+        seq.decode(wl.query(r, 0), wl.softmax_scale)
+        attn.append(time.perf_counter() - t0)
+    return statistics.median(quant), nq, statistics.median(attn), L0
+
+
+def cpu_baseline(args, wl, kb, vb):
+    """The cpu_baseline object of the JSON line (the oracle, as it stands, on this host)."""
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    v, _, desc, _ = oracle_sample(wl, 4, kb, vb, budget_s=20.0)
+    quant_s, nq, attn_s, L0 = oracle_parts(wl, kb, vb)
+    out = {"value": v, "unit": "KV-tokens/s", "cores": threads, "kind": "oracle", "sample": desc,
+           "threads": threads, "runs": 3,
+           "quant_s": quant_s, "quant_tokens": nq, "quant_tokens_per_s": nq / quant_s,
+           "attn_s": attn_s, "attn_context": L0, "attn_kv_tokens_per_s": L0 / attn_s,
+           "parts": "median of 3: quant_s = one append of quant_tokens tokens (all kv heads) to an empty cache; "
+                    "attn_s = one fp64 decode of every query head over attn_context tokens"}
+    if args.workload in (0, 1):
+        # single-threaded leg, in a child process whose OpenMP runtime starts with one thread
+        code = ("import json,sys; sys.path.insert(0, %r); import bench, synth; wl = synth.workload(%d); "
+                "print(json.dumps(bench.oracle_parts(wl, %d, %d)))" % (ROOT, args.workload, kb, vb))
+        env = dict(os.environ, OMP_NUM_THREADS="1")
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
+        if r.returncode == 0:
+            q1, n1, a1, l1 = json.loads(r.stdout.strip().splitlines()[-1])
+            out["single_thread"] = {"threads": 1, "quant_s": q1, "quant_tokens": n1, "attn_s": a1,
+                                    "attn_kv_tokens_per_s": l1 / a1}
+    return out
+
+
 # ---------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -521,7 +614,12 @@ def main():
                     help="time verification steps instead: append N tokens per sequence, then multi-query attention")
     ap.add_argument("--paged", action="store_true",
                     help="packed cache in shared G-token pages behind block tables (random page order)")
+    ap.add_argument("--no-workloads", dest="workloads", action="store_false",
+                    help="skip the per-workload lines (workloads 0, 1, 3 at 2 and 4 bits, 4) of the default run")
     args = ap.parse_args()
+    if any((args.batch, args.context, args.bits, args.k_bits, args.v_bits, args.group, args.residual, args.q_heads,
+            args.paged, args.workload != 2)):
+        args.workloads = False    # the sub-lines belong to the default headline run only
 
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
@@ -608,10 +706,10 @@ def main():
         "prefill": res["prefill"],
         "clocks": res["clocks"],
     }
+    if args.workloads and args.n_query == 0:
+        line["workloads"] = run_workloads(args, rank, world, local_rank)
     if not args.no_cpu_baseline:
-        v, threads, desc, dt = oracle_sample(wl, 4, kb, vb, budget_s=20.0)
-        line["cpu_baseline"] = {"value": v, "unit": "KV-tokens/s", "cores": threads, "kind": "oracle",
-                                "sample": desc}
+        line["cpu_baseline"] = cpu_baseline(args, wl, kb, vb)
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -586,6 +586,94 @@ __global__ void __launch_bounds__(256) append_ring_kernel(AppendArgs a) {
     if (threadIdx.x == 0) a.kv_len[b] = static_cast<int32_t>(st.L1);
 }
 
+// Appends of at most G tokens per sequence (decode steps, a few draft tokens) in ONE launch
+// at head_dim 128: such an append flushes at most one group per (sequence, kv head), so one
+// CTA per sequence does all of it. Its warps take the flush units of every kv head (the key
+// slices of the group, then the value slices of its 32-token runs) with the same warp
+// routines as append_pack_kernel, reading the group from the ring (or from the new tokens);
+// after a CTA barrier, every thread writes the new tokens that stay in the window into their
+// ring slots, and thread 0 advances kv_len. The barrier orders the flush's ring reads before
+// the ring writes of the same sequence.
+template <int KB, int VB, int DT, int G>
+__global__ void __launch_bounds__(kThreads, 1) append_step_kernel(AppendArgs a) {
+    constexpr int D = 128;
+    constexpr int DSK = key_slice_width(D, G), DSV = slice_width(D);
+    constexpr int KU = D / DSK;                    // key units per (kv head, group)
+    constexpr int VU = (G / kTile) * (D / DSV);    // value units per (kv head, group)
+    const int b = blockIdx.x, H = a.H;
+    const kivi_seq& sq = a.seqs[b];
+    const int cap = sq.cap_tokens;
+    const SeqState st = seq_state(a, b, cap);
+    if (!st.ok) {
+        if (threadIdx.x == 0) {
+            const bool len_bad = st.L < 0 || st.L1 < st.L || st.L1 - st.L > a.max_new;
+            set_status(a.status, len_bad ? KIVI_ERR_LENGTH : KIVI_ERR_CAPACITY);
+        }
+        return;
+    }
+    const int ring = a.R + G;
+    const int64_t n = st.L1 - st.L;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (st.np1 > st.np0) {                         // exactly one group leaves the window
+        const int64_t p0g = st.np0, j = p0g / G;
+        const int32_t page = group_page(sq, j);
+        auto row_at = [&](const void* res, const void* nw, int h, int64_t p0, int sl, int ds, int t) -> const uint16_t* {
+            const int64_t p = p0 + t;
+            if (p < st.L) {
+                int slot = static_cast<int>(p0 % ring) + t;
+                slot = slot >= ring ? slot - ring : slot;
+                return static_cast<const uint16_t*>(res) + (static_cast<int64_t>(h) * ring + slot) * D + sl * ds;
+            }
+            return static_cast<const uint16_t*>(nw) + (static_cast<int64_t>(h) * n + (p - st.L)) * D + sl * ds;
+        };
+        for (int u = warp; u < H * (KU + VU); u += kWarps) {
+            if (u < H * KU) {
+                const int h = u / KU, sl = u % KU;
+                auto row = [&](int t) { return row_at(sq.k_res, a.k_new[b], h, p0g, sl, DSK, t); };
+                Tile<DSK, G> tile;
+                keys_load<DSK, G>(row, p0g >= st.L, D, tile);
+                const GroupAddr ga = group_addr(sq, H, h, j, page, D, KB, KB, G);
+                keys_compute<KB, DT, DSK, G>(tile, row, ga.kc + sl * (DSK * KB / 8), D * KB / 8, ga.ks + sl * DSK,
+                                             ga.kz + sl * DSK);
+            } else {
+                const int v = u - H * KU, h = v / VU, rest = v % VU;
+                const int run = rest / (D / DSV), sl = rest % (D / DSV);
+                const int64_t p0 = p0g + run * kTile;
+                const int r = run * kTile + lane;      // row within the group
+                const uint16_t* src = row_at(sq.v_res, a.v_new[b], h, p0, sl, DSV, lane);
+                Tile<DSV, kTile> tile;
+                values_load<DSV>(src, tile);
+                const GroupAddr ga = group_addr(sq, H, h, j, page, D, VB, VB, G);
+                values_compute<VB, DT, DSV, G>(tile, src, ga.vc + r * (D * VB / 8) + sl * (DSV * VB / 8),
+                                               ga.vs + r * (D / G) + sl * (DSV / G), ga.vz + r * (D / G) + sl * (DSV / G));
+            }
+        }
+    }
+    __syncthreads();
+    const int64_t first = st.L > st.np1 ? st.L : st.np1;  // first position that stays in the ring
+    const int64_t count = st.L1 - first;
+    if (count > 0) {
+        const uint16_t* knew = static_cast<const uint16_t*>(a.k_new[b]);
+        const uint16_t* vnew = static_cast<const uint16_t*>(a.v_new[b]);
+        uint16_t* kres = static_cast<uint16_t*>(sq.k_res);
+        uint16_t* vres = static_cast<uint16_t*>(sq.v_res);
+        constexpr int cpr = D / 8;  // 16-byte chunks per row
+        const int64_t total = count * H * cpr;
+        for (int64_t c = threadIdx.x; c < total; c += kThreads) {
+            const int part = static_cast<int>(c % cpr);
+            const int64_t rowi = c / cpr;
+            const int h = static_cast<int>(rowi % H);
+            const int64_t p = first + rowi / H;
+            const int64_t src = (static_cast<int64_t>(h) * n + (p - st.L)) * D + part * 8;
+            const int64_t dst = (static_cast<int64_t>(h) * ring + p % ring) * D + part * 8;
+            *reinterpret_cast<uint4*>(kres + dst) = __ldg(reinterpret_cast<const uint4*>(knew + src));
+            *reinterpret_cast<uint4*>(vres + dst) = __ldg(reinterpret_cast<const uint4*>(vnew + src));
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) a.kv_len[b] = static_cast<int32_t>(st.L1);
+}
+
 // Calls f.template operator()<BITS, DT, DS, G>() for the runtime bit width, input type,
 // slice width ds (32, 64 or 128) and group size g (32 or 64).
 template <typename F>
@@ -640,8 +728,22 @@ cudaError_t launch_quant_values(const CodecArgs& a, cudaStream_t stream) {
     });
 }
 
+// The fused one-launch append for head_dim 128 and at most G new tokens per sequence.
+template <int G>
+cudaError_t launch_append_step(const AppendArgs& a, cudaStream_t stream) {
+    auto go = [&]<int KB, int VB>() {
+        if (a.dtype == KIVI_F16) append_step_kernel<KB, VB, KIVI_F16, G><<<a.nseq, kThreads, 0, stream>>>(a);
+        else append_step_kernel<KB, VB, KIVI_BF16, G><<<a.nseq, kThreads, 0, stream>>>(a);
+        return cudaGetLastError();
+    };
+    if (a.kb == 2) return a.vb == 2 ? go.template operator()<2, 2>() : go.template operator()<2, 4>();
+    return a.vb == 2 ? go.template operator()<4, 2>() : go.template operator()<4, 4>();
+}
+
 cudaError_t launch_append_flush(const AppendArgs& a, cudaStream_t stream) {
     if (a.nseq == 0) return cudaSuccess;
+    if (a.D == 128 && a.max_new <= a.G)
+        return a.G == 64 ? launch_append_step<64>(a, stream) : launch_append_step<32>(a, stream);
     const int max_groups = (a.max_new + a.G - 1) / a.G;
     if (max_groups > 0) {
         // keys and values in two launches, so that each keeps one code path in the

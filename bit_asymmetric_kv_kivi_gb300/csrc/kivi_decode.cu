@@ -17,11 +17,12 @@ void decode_plan(int nseq, int H, int Hq, int D, int max_kv_len, int* chunk, int
                  size_t* counter_bytes, size_t* partial_bytes) {
     const int gq = H > 0 ? Hq / H : 0;
     if (gq == 1 || gq == 2 || gq == 4 || gq == 8) {
-        // decode_mma_kernel over S = nseq * H * (gq / 4 for gq 8, else 1) streams of up to four
-        // query heads: a ticket per stream; one record per segment, fewer than
-        // 2 S + kDecodeMaxCtas of them
-        const int per = gq < 4 ? gq : 4;
-        const size_t S = static_cast<size_t>(nseq) * H * (gq / per);
+        // decode_mma_kernel over streams of gq query heads, one per (sequence, kv head): a ticket
+        // per stream, one record of gq heads per segment, fewer than 2 S + kDecodeMaxCtas of
+        // them. gq = 8 also serves two queries at a query group of 4, as two streams of four
+        // heads per kv head; S = 2 nseq H records of eight heads cover both.
+        const int per = gq;
+        const size_t S = static_cast<size_t>(nseq) * H * (gq == 8 ? 2 : 1);
         *counter_bytes = ticket_bytes(nseq, H);
         *chunk = 0;
         *max_splits = 0;

@@ -389,8 +389,9 @@ struct MmaLayout {
     static constexpr int kStage = kCodeBytes + 2 * kMetaPad + 2 * 256;
     static constexpr int kNslot = 16 / KB;                               // key code pairs per 32-bit word
     static constexpr int kStageBytes = kWarps * kStages * kStage;
+    static constexpr int kPtRows(int gq) { return gq > 4 ? gq : 4; }   // probability rows per warp
     static constexpr int kSmemBytes(int gq) {
-        return kStageBytes + (gq * kD + kWarps * 4 * kPtLd + 2 * kWarps * gq + 8) * 4;
+        return kStageBytes + (gq * kD + kWarps * kPtRows(gq) * kPtLd + 2 * kWarps * gq + 8) * 4;
     }
 };
 
@@ -401,7 +402,7 @@ struct MmaLayout {
 struct MmaSmem {
     unsigned char* stages;   // [warp][stage][STAGE]
     float* qs;               // [GQ][kD]
-    float* pt_all;           // [warp][4][kPtLd]
+    float* pt_all;           // [warp][max(4, GQ)][kPtLd]
     float* red_m;            // [warp][GQ]
     float* red_l;            // [warp][GQ]
     int* s_misc;             // [8]
@@ -410,7 +411,7 @@ struct MmaSmem {
         stages = smem;
         qs = reinterpret_cast<float*>(smem + stage_bytes);
         pt_all = qs + gq * kD;
-        red_m = pt_all + kWarps * 4 * kPtLd;
+        red_m = pt_all + kWarps * (gq > 4 ? gq : 4) * kPtLd;
         red_l = red_m + kWarps * gq;
         s_misc = reinterpret_cast<int*>(red_l + kWarps * gq);
         red_acc = reinterpret_cast<float*>(smem);
@@ -824,9 +825,361 @@ a0 = code_slot<KB>(cw[0][w0], cws[0][w0], s0);
     __syncthreads();
 }
 
+// Packed tiles [ga, gb) of sequence b, kv head hk, for EIGHT query heads (a query group of
+// 8) at q row qrow: the same walk as group_segment, but one n8 tile holds eight heads and the
+// hi and lo parts of every product go to two MMAs over the same A fragments (accumulating
+// into one C), instead of two columns of one MMA. Each thread then owns one head's column
+// (gid) of both parts and builds them together: hi = q_h s, lo = (q_h s - hi) + q_l s, four
+// instructions for two registers. The kv head's tiles are read once for all eight heads.
+// C columns 2t and 2t + 1 are heads 2t and 2t + 1, so each thread keeps the online softmax
+// of two heads.
+template <int KB, int VB, int DT, int G>
+__device__ __forceinline__ void group_segment8(const DecodeArgs& a, const MmaSmem& sm, int b, int64_t qrow, int hk,
+                                               int64_t ga, int64_t gb) {
+    constexpr int GQ = 8;
+    using Lay = MmaLayout<KB, VB>;
+    constexpr int RBK = Lay::kKRowBytes, RBV = Lay::kVRowBytes;
+    constexpr int STAGE = Lay::kStage;
+    constexpr int NSLOT = Lay::kNslot;
+    constexpr int SHIFTK = CodeShift<KB>::kValue, SHIFTV = CodeShift<VB>::kValue;
+    constexpr int TPG = G / kTile;
+    constexpr int NVG = kD / G;
+    constexpr int VMETA = kTile * NVG * 2;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const kivi_seq& sq = a.seqs[b];
+    const int cap = sq.cap_tokens;
+    unsigned char* stages = sm.stages;
+    float* qs = sm.qs;
+    float* red_m = sm.red_m;
+    float* red_l = sm.red_l;
+    int* s_misc = sm.s_misc;
+    float* red_acc = sm.red_acc;
+    const int gid = lane >> 2, t = lane & 3;          // B column gid = head gid; C columns 2t, 2t+1 = heads
+
+    const int64_t gfirst = ga + warp;
+    const int n_my = gfirst < gb ? static_cast<int>((gb - gfirst + kWarps - 1) / kWarps) : 0;
+    unsigned char* my_st = stages + warp * kStages * STAGE;
+    float* pt = sm.pt_all + warp * GQ * kPtLd;
+
+    const bool paged = seq_paged(sq);
+    const int64_t hc = paged ? 0 : static_cast<int64_t>(hk) * cap;
+    const unsigned char* kc_base = sq.k_codes + hc * RBK;
+    const unsigned char* vc_base = sq.v_codes + hc * RBV;
+    const unsigned char* ks_base = reinterpret_cast<const unsigned char*>(sq.k_scale + hc / G * kD);
+    const unsigned char* kz_base = reinterpret_cast<const unsigned char*>(sq.k_zero + hc / G * kD);
+    const unsigned char* vs_base = reinterpret_cast<const unsigned char*>(sq.v_scale + hc * NVG);
+    const unsigned char* vz_base = reinterpret_cast<const unsigned char*>(sq.v_zero + hc * NVG);
+    constexpr int kKChunks = RBK / 16, kVChunks = RBV / 16;
+    constexpr int VL = VMETA / 16;
+    const int half = lane >> 4, off16 = (lane & 15) * 16;
+    const int vhalf = (lane / VL) & 1, voff16 = (lane % VL) * 16;
+    const bool v_issue = lane < 2 * VL;
+    const unsigned char* kc_lane = kc_base + lane * 16;
+    const unsigned char* vc_lane = vc_base + lane * 16;
+    const unsigned char* km_lane = (half ? kz_base : ks_base) + off16;
+    const unsigned char* vm_lane = (vhalf ? vz_base : vs_base) + voff16;
+    const int km_dst = Lay::kCodeBytes + half * Lay::kMetaPad + (off16 >> 6) * 80 + (off16 & 63);
+    const int vm_dst = Lay::kCodeBytes + 2 * Lay::kMetaPad + vhalf * 256 + voff16;
+    auto issue = [&](int slot, int64_t j, int32_t page) {
+        unsigned char* dst = my_st + slot * STAGE;
+        int64_t rt, kg;
+        if (paged) {
+            kg = static_cast<int64_t>(page) * a.H + hk;
+            rt = kg * TPG + (TPG > 1 ? j % TPG : 0);
+        } else {
+            rt = j;
+            kg = TPG > 1 ? j / TPG : j;
+        }
+#pragma unroll
+        for (int k = 0; k < kKChunks; ++k)
+            cp_async16(dst + lane * 16 + 512 * k, kc_lane + rt * (kTile * RBK) + 512 * k);
+#pragma unroll
+        for (int k = 0; k < kVChunks; ++k)
+            cp_async16(dst + kTile * RBK + lane * 16 + 512 * k, vc_lane + rt * (kTile * RBV) + 512 * k);
+        cp_async16(dst + km_dst, km_lane + kg * 256);
+        if (v_issue) cp_async16(dst + vm_dst, vm_lane + rt * VMETA);
+    };
+    auto page_of = [&](int i) -> int32_t {
+        return paged ? sq.block_table[(gfirst + static_cast<int64_t>(kWarps) * i) / TPG] : 0;
+    };
+#pragma unroll
+    for (int i = 0; i < kStages - 1; ++i) {
+        if (i < n_my) issue(i, gfirst + static_cast<int64_t>(kWarps) * i, page_of(i));
+        cp_async_commit();
+    }
+    int32_t pg_ahead = kStages - 1 < n_my ? page_of(kStages - 1) : 0;
+
+    load_q<DT, GQ>(a, qs, qrow);
+    __syncthreads();
+    float qmax_abs = 0.0f;
+    for (int i = tid; i < GQ * kD; i += kThreads) qmax_abs = fmaxf(qmax_abs, fabsf(qs[i]));
+    qmax_abs = warp_max(qmax_abs);
+    if (lane == 0) reinterpret_cast<float*>(s_misc)[1 + warp] = qmax_abs;
+    __syncthreads();
+    qmax_abs = fmaxf(fmaxf(reinterpret_cast<float*>(s_misc)[1], reinterpret_cast<float*>(s_misc)[2]),
+                     fmaxf(reinterpret_cast<float*>(s_misc)[3], reinterpret_cast<float*>(s_misc)[4]));
+    int qexp = 0;
+    if (qmax_abs > 0.0f) frexpf(qmax_abs, &qexp);
+    const float qpre = ldexpf(1.0f, -qexp), qpost = ldexpf(1.0f, qexp);
+
+    // q of head gid, hi and lo, in B-fragment order (slot s: channels c0 and c0 + NSLOT of t's span)
+    uint32_t qh[16], ql[16];
+#pragma unroll
+    for (int sl = 0; sl < 16; ++sl) {
+        const int c0 = 32 * t + (sl / NSLOT) * 2 * NSLOT + (sl % NSLOT), c1 = c0 + NSLOT;
+        const float v0 = qs[gid * kD + c0] * qpre, v1 = qs[gid * kD + c1] * qpre;
+        qh[sl] = pack_h2(v0, v1);
+        ql[sl] = pack_h2(v0 - h2_lo(qh[sl]), v1 - h2_hi(qh[sl]));
+    }
+    const uint32_t g3 = static_cast<uint32_t>(gid & 3);
+    const uint32_t sel_v = VB == 2 ? (g3 | (g3 << 4) | ((4 + g3) << 8) | ((4 + g3) << 12))
+                                   : ((gid & 1) ? 0x7632u : 0x5410u);
+    const int vbyte = VB == 2 ? 4 * (gid >> 2) : 4 * (gid >> 1);
+    const uint32_t sel_z = (gid & 1) ? 0x7632u : 0x5410u;
+
+    float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F}, l_run[2] = {0.0f, 0.0f};   // heads 2t, 2t + 1
+    float cv[8][4], cz[4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cv[i][0] = cv[i][1] = cv[i][2] = cv[i][3] = 0.0f;
+    cz[0] = cz[1] = cz[2] = cz[3] = 0.0f;
+
+    for (int it = 0; it < n_my; ++it) {
+        {
+            const int nxt = it + kStages - 1;
+            if (nxt < n_my) {
+                issue(nxt % kStages, gfirst + static_cast<int64_t>(kWarps) * nxt, pg_ahead);
+                pg_ahead = nxt + 1 < n_my ? page_of(nxt + 1) : 0;
+            }
+            cp_async_commit();
+        }
+        cp_async_wait<kStages - 1>();
+        __syncwarp();
+        const unsigned char* st = my_st + (it % kStages) * STAGE;
+        const unsigned char* kc = st;
+        const unsigned char* vc = st + kTile * RBK;
+        const unsigned char* ksm = st + Lay::kCodeBytes;
+        const unsigned char* kzm = ksm + Lay::kMetaPad;
+        const unsigned char* vsm = kzm + Lay::kMetaPad;
+        const unsigned char* vzm = vsm + 256;
+
+        uint32_t sp[16], zp[16];
+        {
+            uint32_t R[16], Z[16];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 r4 = *reinterpret_cast<const uint4*>(ksm + 80 * t + 16 * i);
+                const uint4 z4 = *reinterpret_cast<const uint4*>(kzm + 80 * t + 16 * i);
+                R[4 * i] = r4.x; R[4 * i + 1] = r4.y; R[4 * i + 2] = r4.z; R[4 * i + 3] = r4.w;
+                Z[4 * i] = z4.x; Z[4 * i + 1] = z4.y; Z[4 * i + 2] = z4.z; Z[4 * i + 3] = z4.w;
+            }
+#pragma unroll
+            for (int sl = 0; sl < 16; ++sl) {
+                const int rel = (sl / NSLOT) * 2 * NSLOT + (sl % NSLOT);
+                const uint32_t sel = (rel & 1) ? 0x7632u : 0x5410u;
+                sp[sl] = prmt(R[rel >> 1], R[(rel + NSLOT) >> 1], sel);
+                zp[sl] = prmt(Z[rel >> 1], Z[(rel + NSLOT) >> 1], sel);
+            }
+        }
+        // bias: A rows all z_k, B = q hi then q lo (two accumulators halve the chain)
+        float cb[4] = {0.0f, 0.0f, 0.0f, 0.0f}, cb2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            mma_f16(cb, zp[2 * ks], zp[2 * ks], zp[2 * ks + 1], zp[2 * ks + 1], qh[2 * ks], qh[2 * ks + 1]);
+            mma_f16(cb2, zp[2 * ks], zp[2 * ks], zp[2 * ks + 1], zp[2 * ks + 1], ql[2 * ks], ql[2 * ks + 1]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) cb[i] += cb2[i];
+
+        // scores: A = key codes, B = (q s_k) hi into c*, then lo into c*o
+        float c0[4] = {cb[0], cb[1], cb[0], cb[1]}, c1[4] = {cb[0], cb[1], cb[0], cb[1]};
+        float c0o[4] = {0.0f, 0.0f, 0.0f, 0.0f}, c1o[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        {
+            uint32_t cw[4][KB], cws[4][KB];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const unsigned char* row = kc + (gid + 8 * r) * RBK;
+                if constexpr (KB == 2) {
+                    const uint2 v = *reinterpret_cast<const uint2*>(row + 8 * t);
+                    cw[r][0] = v.x; cw[r][1] = v.y;
+                } else {
+                    const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * t);
+                    cw[r][0] = v.x; cw[r][1] = v.y; cw[r][2] = v.z; cw[r][3] = v.w;
+                }
+#pragma unroll
+                for (int w = 0; w < KB; ++w) cws[r][w] = cw[r][w] >> SHIFTK;
+            }
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const int s0 = 2 * ks, s1 = 2 * ks + 1;
+                const uint32_t h0 = hmul2(qh[s0], sp[s0]), h1 = hmul2(qh[s1], sp[s1]);
+                const uint32_t l0 = hfma2(ql[s0], sp[s0], hfma2(qh[s0], sp[s0], h0 ^ 0x80008000u));
+                const uint32_t l1 = hfma2(ql[s1], sp[s1], hfma2(qh[s1], sp[s1], h1 ^ 0x80008000u));
+                const int w0 = s0 / NSLOT, w1 = s1 / NSLOT;
+                uint32_t a0 = code_slot<KB>(cw[0][w0], cws[0][w0], s0), a1 = code_slot<KB>(cw[1][w0], cws[1][w0], s0);
+                uint32_t a2 = code_slot<KB>(cw[0][w1], cws[0][w1], s1), a3 = code_slot<KB>(cw[1][w1], cws[1][w1], s1);
+                mma_f16(c0, a0, a1, a2, a3, h0, h1);
+                mma_f16(c0o, a0, a1, a2, a3, l0, l1);
+                a0 = code_slot<KB>(cw[2][w0], cws[2][w0], s0); a1 = code_slot<KB>(cw[3][w0], cws[3][w0], s0);
+                a2 = code_slot<KB>(cw[2][w1], cws[2][w1], s1); a3 = code_slot<KB>(cw[3][w1], cws[3][w1], s1);
+                mma_f16(c1, a0, a1, a2, a3, h0, h1);
+                mma_f16(c1o, a0, a1, a2, a3, l0, l1);
+            }
+        }
+
+        // online softmax of heads 2t (e = 0) and 2t + 1 (e = 1) over tokens gid, gid+8, gid+16, gid+24
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            c0[i] = (c0[i] + c0o[i]) * qpost;
+            c1[i] = (c1[i] + c1o[i]) * qpost;
+        }
+        float p[2][4];
+        bool grow = false;
+        float mnew[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            float tmax = fmaxf(fmaxf(c0[e], c0[2 + e]), fmaxf(c1[e], c1[2 + e]));
+            tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 4));
+            tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
+            tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
+            mnew[e] = fmaxf(m_run[e], tmax);
+            grow |= mnew[e] > m_run[e];
+        }
+        if (__any_sync(kFull, grow)) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float alpha = exp2f(m_run[e] - mnew[e]);
+                l_run[e] *= alpha;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    cv[i][e] *= alpha;
+                    cv[i][2 + e] *= alpha;
+                }
+                cz[e] *= alpha;
+                cz[2 + e] *= alpha;
+                m_run[e] = mnew[e];
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            p[e][0] = exp2f(c0[e] - m_run[e]);
+            p[e][1] = exp2f(c0[2 + e] - m_run[e]);
+            p[e][2] = exp2f(c1[e] - m_run[e]);
+            p[e][3] = exp2f(c1[2 + e] - m_run[e]);
+            l_run[e] += (p[e][0] + p[e][1]) + (p[e][2] + p[e][3]);
+        }
+        // token 8r + j to column 8r + 2 (j % 4) + j / 4, as in group_segment
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) pt[(2 * t + e) * kPtLd + 8 * r + 2 * (gid & 3) + (gid >> 2)] = p[e][r];
+        __syncwarp();
+
+        // value side B operands of head gid: P' = p s_v hi and lo, and p hi and lo (z_v term)
+        uint32_t vbh[2][2][4], vbl[2][2][4], bph[2][2], bpl[2][2], za[2][2];
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int tau0 = 16 * k2 + 8 * e + t;
+                const float2 pp = *reinterpret_cast<const float2*>(pt + gid * kPtLd + 16 * k2 + 8 * e + 2 * t);
+                const uint32_t ph = pack_h2(pp.x, pp.y);
+                const uint32_t pl = pack_h2(pp.x - h2_lo(ph), pp.y - h2_hi(ph));
+                bph[k2][e] = ph;
+                bpl[k2][e] = pl;
+                uint32_t s0w[NVG / 2 > 0 ? NVG / 2 : 1], s1w[NVG / 2 > 0 ? NVG / 2 : 1];
+                if constexpr (NVG == 4) {
+                    const uint2 x0 = *reinterpret_cast<const uint2*>(vsm + tau0 * 8);
+                    const uint2 x1 = *reinterpret_cast<const uint2*>(vsm + (tau0 + 4) * 8);
+                    s0w[0] = x0.x; s0w[1] = x0.y; s1w[0] = x1.x; s1w[1] = x1.y;
+                } else {
+                    s0w[0] = *reinterpret_cast<const uint32_t*>(vsm + tau0 * 4);
+                    s1w[0] = *reinterpret_cast<const uint32_t*>(vsm + (tau0 + 4) * 4);
+                }
+#pragma unroll
+                for (int kg = 0; kg < 4; ++kg) {
+                    const int vg = kg / TPG;
+                    const uint32_t svp = prmt(s0w[vg >> 1], s1w[vg >> 1], (vg & 1) ? 0x7632u : 0x5410u);
+                    const uint32_t hv = hmul2(ph, svp);
+                    vbh[k2][e][kg] = hv;
+                    vbl[k2][e][kg] = hfma2(pl, svp, hfma2(ph, svp, hv ^ 0x80008000u));
+                }
+                const uint32_t zw0 = *reinterpret_cast<const uint32_t*>(vzm + tau0 * (2 * NVG) + 4 * ((gid & 3) >> 1));
+                const uint32_t zw1 = *reinterpret_cast<const uint32_t*>(vzm + (tau0 + 4) * (2 * NVG) + 4 * ((gid & 3) >> 1));
+                za[k2][e] = gid < NVG ? prmt(zw0, zw1, sel_z) : 0u;
+            }
+        }
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) {
+            mma_f16(cz, za[k2][0], 0u, za[k2][1], 0u, bph[k2][0], bph[k2][1]);
+            mma_f16(cz, za[k2][0], 0u, za[k2][1], 0u, bpl[k2][0], bpl[k2][1]);
+        }
+
+        // value codes (A = codes^T, rows = channels) against hi, then lo
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) {
+#pragma unroll
+            for (int kg = 0; kg < 4; ++kg) {
+                uint32_t wv[2], wvs[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int tau0 = 16 * k2 + 8 * e + t;
+                    const int off = kg * (RBV / 4) + vbyte;
+                    const uint32_t x0 = *reinterpret_cast<const uint32_t*>(vc + tau0 * RBV + off);
+                    const uint32_t x1 = *reinterpret_cast<const uint32_t*>(vc + (tau0 + 4) * RBV + off);
+                    wv[e] = prmt(x0, x1, sel_v);
+                    wvs[e] = wv[e] >> SHIFTV;
+                }
+                const uint32_t a00 = code_pair<VB, 0>(wv[0], wvs[0]), a01 = code_pair<VB, 1>(wv[0], wvs[0]);
+                const uint32_t a02 = code_pair<VB, 0>(wv[1], wvs[1]), a03 = code_pair<VB, 1>(wv[1], wvs[1]);
+                const uint32_t a10 = code_pair<VB, 2>(wv[0], wvs[0]), a11 = code_pair<VB, 3>(wv[0], wvs[0]);
+                const uint32_t a12 = code_pair<VB, 2>(wv[1], wvs[1]), a13 = code_pair<VB, 3>(wv[1], wvs[1]);
+                mma_f16(cv[2 * kg], a00, a01, a02, a03, vbh[k2][0][kg], vbh[k2][1][kg]);
+                mma_f16(cv[2 * kg + 1], a10, a11, a12, a13, vbh[k2][0][kg], vbh[k2][1][kg]);
+                mma_f16(cv[2 * kg], a00, a01, a02, a03, vbl[k2][0][kg], vbl[k2][1][kg]);
+                mma_f16(cv[2 * kg + 1], a10, a11, a12, a13, vbl[k2][0][kg], vbl[k2][1][kg]);
+            }
+        }
+        __syncwarp();
+    }
+    cp_async_wait<0>();
+
+    // warp state -> merge arrays (red_acc aliases the stages: wait for every warp)
+    float l_tot[2];
+    float zk[2][4];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        float x = l_run[e];
+        x += __shfl_xor_sync(kFull, x, 4);
+        x += __shfl_xor_sync(kFull, x, 8);
+        x += __shfl_xor_sync(kFull, x, 16);
+        l_tot[e] = x;
+#pragma unroll
+        for (int kg = 0; kg < 4; ++kg) zk[e][kg] = __shfl_sync(kFull, cz[e], 4 * (kg / TPG) + t);  // (group, head 2t + e)
+    }
+    __syncthreads();
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        const int kg = mt >> 1;
+        const int ch = 32 * kg + 4 * gid + 2 * (mt & 1);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            red_acc[(warp * GQ + 2 * t + e) * kD + ch] = cv[mt][e] + zk[e][kg];
+            red_acc[(warp * GQ + 2 * t + e) * kD + ch + 1] = cv[mt][2 + e] + zk[e][kg];
+        }
+    }
+    if (gid == 0) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            red_m[warp * GQ + 2 * t + e] = m_run[e];
+            red_l[warp * GQ + 2 * t + e] = l_tot[e];
+        }
+    }
+    __syncthreads();
+}
+
 template <int KB, int VB, int DT, int GQ, int G, int QS>
 __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_kernel(DecodeArgs a) {
-    static_assert(GQ == 1 || GQ == 2 || GQ == 4, "one n8 tile holds hi and lo of up to four heads");
+    static_assert(GQ == 1 || GQ == 2 || GQ == 4 || GQ == 8, "one n8 tile: hi and lo of up to four heads, or eight heads");
     static_assert(QS == 1 || (GQ == 4 && QS == 2), "streams per kv head");
     extern __shared__ __align__(16) unsigned char smem[];
     const MmaSmem sm(smem, MmaLayout<KB, VB>::kStageBytes, GQ);
@@ -940,8 +1293,12 @@ __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_ker
         if (k.w.u != 0 && k.x1 > k.x0) {
             if (k.x0 < k.w.ng) {
                 __syncthreads();   // the previous segment is done with qs and the shared arrays
-                group_segment<KB, VB, DT, GQ, G>(a, sm, k.b, stream_row<GQ, QS>(a, k.b, k.h), k.h / QS, k.x0,
-                                                 k.x1 < k.w.ng ? k.x1 : k.w.ng);
+                if constexpr (GQ == 8)
+                    group_segment8<KB, VB, DT, G>(a, sm, k.b, stream_row<GQ, QS>(a, k.b, k.h), k.h / QS, k.x0,
+                                                  k.x1 < k.w.ng ? k.x1 : k.w.ng);
+                else
+                    group_segment<KB, VB, DT, GQ, G>(a, sm, k.b, stream_row<GQ, QS>(a, k.b, k.h), k.h / QS, k.x0,
+                                                     k.x1 < k.w.ng ? k.x1 : k.w.ng);
                 finish(0);
                 k = current();
             }
@@ -1011,7 +1368,9 @@ cudaError_t launch_gq(const DecodeArgs& a, cudaStream_t stream) {
         case 1: return launch_mma<KB, VB, DT, 1, G>(a, stream);
         case 2: return launch_mma<KB, VB, DT, 2, G>(a, stream);
         case 4: return launch_mma<KB, VB, DT, 4, G>(a, stream);
-        case 8: return launch_mma<KB, VB, DT, 4, G, 2>(a, stream);
+        case 8:   // decode with a query group of 8: one stream of eight heads; two queries at group 4: one
+                  // stream of four heads per query (each with its own causal end)
+            return a.n_query > 1 ? launch_mma<KB, VB, DT, 4, G, 2>(a, stream) : launch_mma<KB, VB, DT, 8, G>(a, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -59,3 +59,14 @@ def test_workload_options_set_query_heads_and_sizes():
     assert (wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.lengths) == (16, 64, 8, (32768,) * 16)
     with pytest.raises(SystemExit):
         bench.workload_spec(argparse.Namespace(**{**vars(args), "q_heads": 12}))
+
+
+def test_oracle_parts_times_quantization_and_attention_apart(oracle_lib):
+    """The cpu_baseline's two parts on the tiny workload: positive median times, the
+    quantized token count and the attention context it reports."""
+    import bench
+    import synth
+    wl = synth.workload(0)
+    q_s, nq, a_s, L = bench.oracle_parts(wl, 2, 2, runs=3, quant_tokens=256)
+    assert q_s > 0 and a_s > 0
+    assert nq == 256 and L == wl.lengths[0] == 1024

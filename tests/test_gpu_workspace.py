@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 def _cache(nseq, hq, h, lengths, dtype, seed):
     wl = synth.Workload("ws", nseq, hq, h, 128, tuple(lengths), dtype, seed=seed)
     kcfg, ocfg = configs(2, dtype, hq, h)
-    cap = max(lengths) + 64
+    cap = (max(lengths) // 32 + 2) * 32
     cache = kivi.KVCache(kcfg, nseq, cap)
     refs = []
     ks, vs = [], []
