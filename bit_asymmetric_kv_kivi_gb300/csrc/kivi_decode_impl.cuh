@@ -1211,19 +1211,31 @@ __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_ker
     // first unit of sequence b, b, h (b = nseq ends the walk)
     __shared__ int64_t walk[7];
     volatile int64_t* vw = walk;
-    sched[tid] = mine;
-    __syncthreads();
-    if (tid == 0) {
-        vw[5] = a.nseq;
-        int64_t run = 0;
-        for (int i = 0; i < kThreads; ++i) {
-            const int64_t v = sched[i];
-            sched[i] = run;
-            run += v;
+    // exclusive scan of the threads' unit counts: within each warp by shuffles, then the four
+    // warp totals (a serial scan by one thread cost ~2 us at the start of every launch)
+    {
+        const int lane = tid & 31, warp = tid >> 5;
+        int64_t incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
         }
-        sched[kThreads] = run;
+        if (lane == 31) sched[kThreads + 1 + warp] = incl;
+        if (tid == 0) vw[5] = a.nseq;
+        __syncthreads();
+        int64_t before = 0, total = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const int64_t x = sched[kThreads + 1 + w];
+            before += w < warp ? x : 0;
+            total += x;
+        }
+        __syncthreads();   // every thread has read the warp totals
+        sched[tid] = before + incl - mine;
+        if (tid == 0) sched[kThreads] = total;
+        __syncthreads();
     }
-    __syncthreads();
     const int64_t U = sched[kThreads];
     const int64_t by_size = U / kMinUnitsPerCta > 1 ? U / kMinUnitsPerCta : 1;
     const int64_t Ceff = C < by_size ? C : by_size;
