@@ -436,8 +436,11 @@ def run_gpu_multi(args, rank, world, local_rank):
 
 
 def run_e2e(args, cache, wl, device, L_start, max_len, out_dev):
-    """Same step, with the step's inputs copied host -> device from pinned memory and the
-    attention output copied back, inside the timed region."""
+    """Same step through the public API, with every step's inputs copied host -> device from
+    pinned memory and its attention output copied back, inside the timed region. The copies
+    run on two copy streams (in and out) and overlap the compute of the neighbouring steps:
+    inputs and outputs are double-buffered, and events order each buffer's copy-in, use and
+    copy-out."""
     import torch
     B, Hq, H, D = wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
     n = min(args.steps, 50)
@@ -445,31 +448,58 @@ def run_e2e(args, cache, wl, device, L_start, max_len, out_dev):
     kn, vn, q = step_inputs(wl, L_start, n, device)
     kh, vh, qh = kn.cpu().pin_memory(), vn.cpu().pin_memory(), q.cpu().pin_memory()
     out_h = torch.empty((n, B, Hq, D), dtype=torch.float32).pin_memory()
-    kd = torch.empty((B, H, 1, D), dtype=tdt, device=device)
-    vd = torch.empty_like(kd)
-    qd = torch.empty((B, Hq, D), dtype=tdt, device=device)
-    kptr = torch.tensor([kd[b].data_ptr() for b in range(B)], dtype=torch.int64, device=device)
-    vptr = torch.tensor([vd[b].data_ptr() for b in range(B)], dtype=torch.int64, device=device)
+    kd = [torch.empty((B, H, 1, D), dtype=tdt, device=device) for _ in range(2)]
+    vd = [torch.empty_like(kd[0]) for _ in range(2)]
+    qd = [torch.empty((B, Hq, D), dtype=tdt, device=device) for _ in range(2)]
+    od = [out_dev, torch.empty_like(out_dev)]
+    kptr = [torch.tensor([kd[i][b].data_ptr() for b in range(B)], dtype=torch.int64, device=device) for i in range(2)]
+    vptr = [torch.tensor([vd[i][b].data_ptr() for b in range(B)], dtype=torch.int64, device=device) for i in range(2)]
     ones = torch.ones(B, dtype=torch.int32, device=device)
-    stream = torch.cuda.current_stream(device)
+    compute = torch.cuda.current_stream(device)
+    cin, cout = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of buffer i copied in
+    ev_used = [torch.cuda.Event() for _ in range(2)]    # buffer i's step done (inputs read, output written)
+    ev_out = [torch.cuda.Event() for _ in range(2)]     # output of buffer i copied out
+
+    def copy_in(s):
+        i = s & 1
+        with torch.cuda.stream(cin):
+            if s >= 2:
+                cin.wait_event(ev_used[i])              # step s - 2 has read kd/vd/qd[i]
+            kd[i].copy_(kh[s], non_blocking=True)
+            vd[i].copy_(vh[s], non_blocking=True)
+            qd[i].copy_(qh[s], non_blocking=True)
+            ev_in[i].record(cin)
+
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    e0.record(cin)
+    copy_in(0)
     for s in range(n):
-        kd.copy_(kh[s], non_blocking=True)
-        vd.copy_(vh[s], non_blocking=True)
-        qd.copy_(qh[s], non_blocking=True)
-        cache.append_ptrs(kptr, vptr, ones, 1)
-        cache.decode(qd, out_dev, wl.softmax_scale, max_kv_len=max_len)
-        out_h[s].copy_(out_dev, non_blocking=True)
-    e1.record(stream)
+        i = s & 1
+        compute.wait_event(ev_in[i])
+        if s >= 2:
+            compute.wait_event(ev_out[i])               # step s - 2's output has left od[i]
+        cache.append_ptrs(kptr[i], vptr[i], ones, 1)
+        cache.decode(qd[i], od[i], wl.softmax_scale, max_kv_len=max_len)
+        ev_used[i].record(compute)
+        if s + 1 < n:
+            copy_in(s + 1)                              # overlaps this step's compute
+        with torch.cuda.stream(cout):
+            cout.wait_event(ev_used[i])
+            out_h[s].copy_(od[i], non_blocking=True)
+            ev_out[i].record(cout)
+    cout.wait_stream(compute)
+    cout.wait_stream(cin)
+    e1.record(cout)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     kv_tokens = sum(sum(L + s + 1 for L in L_start) for s in range(n))
-    h2d = (kd.numel() + vd.numel() + qd.numel()) * 2
+    h2d = (kd[0].numel() + vd[0].numel() + qd[0].numel()) * 2
     d2h = out_dev.numel() * 4
     return {"value": kv_tokens / (ms / 1e3), "unit": "KV-tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms / n, "kv_tokens": kv_tokens, "steps": n}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms / n, "kv_tokens": kv_tokens, "steps": n,
+            "copies": "copy-in and copy-out streams overlapping compute, double-buffered inputs and outputs"}
 
 
 # ---------------------------------------------------------------- every workload in one line
@@ -705,7 +735,7 @@ def main():
                      "traffic": traffic,
                      "traffic_source": "ncu capture at 8 sequences, scaled by (token, kv head) units" if per_unit else None},
         "attn_kv_tokens_per_s": (res["kv_tokens"] / args.steps) / (avg_attn_ms / 1e3),
-        "e2e": {k: res["e2e"][k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")},
+        "e2e": {k: res["e2e"][k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step", "copies")},
         "gpu_launches": res["launches_per_step"] * args.steps,
         "prefill": res["prefill"],
         "clocks": res["clocks"],
