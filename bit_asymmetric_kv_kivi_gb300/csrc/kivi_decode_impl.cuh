@@ -26,9 +26,10 @@
 //        sum_t p z_v term is a small MMA of its own.
 //    q is rescaled by a power of two so that max|q| lies in (1/2, 1]; with
 //    |x| <= 65504 no f16 operand can overflow.
-//    Hq/Hkv = 8 runs as two streams of four query heads per kv head, each
-//    reading the kv head's tiles from DRAM (the kernel is issue-bound, so
-//    the second read costs little time).
+//    Hq/Hkv = 8 runs as one stream of eight query heads per kv head
+//    (group_segment8: the hi and lo parts of each product are two MMAs over
+//    the same unpacked codes), so every tile is read from DRAM once. Two
+//    queries at Hq/Hkv = 4 run as two streams of four heads, one per query.
 //  * other query groups (up to 32) run on decode_multi_kernel (kivi_multi_impl.cuh)
 //    with one query: its CTAs share each unpacked tile between warps of four heads.
 //
@@ -1185,8 +1186,9 @@ __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_ker
     const MmaSmem sm(smem, MmaLayout<KB, VB>::kStageBytes, GQ);
     int64_t* sched = reinterpret_cast<int64_t*>(smem);   // scan scratch: the stages are idle until the walk
     const int tid = threadIdx.x;
-    // streams: (sequence, h) with query heads h GQ .. h GQ + GQ - 1 and kv head h / QS; a query
-    // group of 8 is two streams of four heads per kv head (QS = 2), each reading the kv head
+    // streams: (sequence, h) with query heads h GQ .. h GQ + GQ - 1 and kv head h / QS; two
+    // queries at a query group of 4 are two streams per kv head (QS = 2), one per query, each
+    // reading the kv head
     const int C = gridDim.x, c = blockIdx.x, H = a.H * QS;
 
     // sequences without work: zeros for an empty one, NaN and a status for a bad length
