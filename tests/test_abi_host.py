@@ -125,15 +125,16 @@ def test_multi_query_arguments_rejected_before_launch(lib):
 def test_decode_workspace_plans_by_query_group(lib):
     """The workspace each query group needs, from the documented plans: tickets for two
     streams per (sequence, kv head) in every plan, then fewer than 2 S + 1024 records of
-    GQ (D + 4) floats, S the number of streams; a group of 8 runs two streams of four heads
-    per kv head; other groups take the multi-query plan with one query. One-query
-    multi-query calls of groups 1 to 8, and two-query calls of group 4, take the decode
-    plan."""
+    g (D + 4) floats, S the number of streams. A group of 8 runs one stream of eight heads
+    per kv head, but its plan counts two streams per kv head, so that it also covers two
+    queries at group 4 (two streams of four heads per kv head). Other groups take the
+    multi-query plan with one query. One-query multi-query calls of groups 1 to 8, and
+    two-query calls of group 4, take the decode plan."""
     nseq, H, D = 3, 8, 128
     tickets = ((2 * nseq * H * 4 + 255) // 256) * 256
     for g in (1, 2, 4, 8):
         cfg = kivi.Config(num_q_heads=g * H, num_kv_heads=H).c()
-        per, S = min(g, 4), nseq * H * (g // min(g, 4))
+        per, S = g, nseq * H * (2 if g == 8 else 1)
         want = tickets + (2 * S + 1024) * per * (D + 4) * 4
         assert lib.kivi_decode_workspace_bytes(cfg, nseq, 5000) == want, g
         assert lib.kivi_decode_multi_workspace_bytes(cfg, nseq, 1, 5000) == want, g
