@@ -117,6 +117,14 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// 2^x for the softmax weights and rescale factors (x <= 0): the ex2 approximation, results
+// below 2^-126 flushed to zero (such a weight adds nothing to an fp32 sum of weights >= 1)
+__device__ __forceinline__ float exp2_ftz(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Codes at bits I*BITS and 16 + I*BITS of w as an exact f16 pair (low, high half).
 // The field is OR-ed into the mantissa of 1024.0 and the 1024 removed by one fma
 // (the field's position scaled away by a power of two); fields that reach past the
@@ -378,21 +386,31 @@ __device__ __forceinline__ void finish_segment(const DecodeArgs& a, const Stream
 
 // ---------------------------------------------------------------- tensor-core kernel
 
+// Key zeros for the bias term: a warp computes sum_d q[d] z_k[group][d] for kZB of its tiles
+// at once (one m16 tile of MMAs, rows = tiles), from a private buffer of their key-zero rows
+// (256 bytes each), filled kZB tiles ahead. The 16-byte chunk c of row r sits at position
+// zpos(c, r), so that the reads (thread t: chunks 4t .. 4t + 3 of rows gid and gid + 8, one
+// chunk per instruction) fall on distinct shared-memory banks.
+constexpr int kZB = 16;
+constexpr int kZRow = 256;
+__device__ __forceinline__ int zpos(int c, int r) { return (c & ~3) | ((c + (c >> 2) + r) & 3); }
+
 template <int KB, int VB>
 struct MmaLayout {
     static constexpr int kKRowBytes = kD * KB / 8;                       // packed key row: 32 or 64 bytes
     static constexpr int kVRowBytes = kD * VB / 8;                       // and value row
-    // kc, vc, ks, kz, vs, vz; each 64-byte channel span of ks and kz is padded to 80 bytes so
-    // that the four spans read together fall on distinct shared-memory banks; vs and vz take
-    // 256 bytes each (128 used when G = 64)
+    // kc, vc, ks, vs, vz; each 64-byte channel span of ks is padded to 80 bytes so that the
+    // four spans read together fall on distinct shared-memory banks; vs and vz take 256 bytes
+    // each (128 used when G = 64)
     static constexpr int kMetaPad = 320;
     static constexpr int kCodeBytes = kTile * (kKRowBytes + kVRowBytes);
-    static constexpr int kStage = kCodeBytes + 2 * kMetaPad + 2 * 256;
+    static constexpr int kStage = kCodeBytes + kMetaPad + 2 * 256;
     static constexpr int kNslot = 16 / KB;                               // key code pairs per 32-bit word
     static constexpr int kStageBytes = kWarps * kStages * kStage;
+    static constexpr int kZBytes = kWarps * kZB * kZRow;                 // the warps' key-zero buffers
     static constexpr int kPtRows(int gq) { return gq > 4 ? gq : 4; }   // probability rows per warp
     static constexpr int kSmemBytes(int gq) {
-        return kStageBytes + (gq * kD + kWarps * kPtRows(gq) * kPtLd + 2 * kWarps * gq + 8) * 4;
+        return kStageBytes + kZBytes + (gq * kD + kWarps * kPtRows(gq) * kPtLd + 2 * kWarps * gq + 8) * 4;
     }
 };
 
@@ -402,6 +420,7 @@ struct MmaLayout {
 // channels 32t + m*2*NSLOT + i and + NSLOT, with m = s / NSLOT, i = s % NSLOT.
 struct MmaSmem {
     unsigned char* stages;   // [warp][stage][STAGE]
+    unsigned char* zbuf;     // [warp][kZB][kZRow]
     float* qs;               // [GQ][kD]
     float* pt_all;           // [warp][max(4, GQ)][kPtLd]
     float* red_m;            // [warp][GQ]
@@ -410,7 +429,8 @@ struct MmaSmem {
     float* red_acc;          // [warp][GQ][kD], aliases the stages once they are drained
     __device__ MmaSmem(unsigned char* smem, int stage_bytes, int gq) {
         stages = smem;
-        qs = reinterpret_cast<float*>(smem + stage_bytes);
+        zbuf = smem + stage_bytes;
+        qs = reinterpret_cast<float*>(zbuf + kWarps * kZB * kZRow);
         pt_all = qs + gq * kD;
         red_m = pt_all + kWarps * (gq > 4 ? gq : 4) * kPtLd;
         red_l = red_m + kWarps * gq;
@@ -473,6 +493,54 @@ __device__ __forceinline__ void residual_segment(const DecodeArgs& a, const MmaS
     __syncthreads();
 }
 
+// Bias term of kZB tiles of a warp, sum_d q[d] z_k[tile][d] per B column, from the key zeros
+// in zb (row r = the tile r places after the batch's first): A = the zeros (row = tile), each
+// register the channel pair of key-score slot s (so the B constants of the scores serve as
+// they are); B = bh, then bl when NB == 2 (two MMAs into one C). c = the C rows gid and
+// gid + 8, columns 2t and 2t + 1.
+template <int NSLOT, int NB>
+__device__ __forceinline__ void bias_batch(const unsigned char* zb, int gid, int t, const uint32_t (&bh)[16],
+                                           const uint32_t (&bl)[16], float (&c)[4]) {
+    float c2[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // a second accumulator halves the dependent chain
+    c[0] = c[1] = c[2] = c[3] = 0.0f;
+    // two halves: chunks 2h, 2h + 1 of the thread's span (its words 8h .. 8h + 7) hold the
+    // channel pairs of slots 8h .. 8h + 7, i.e. of k-steps 4h .. 4h + 3
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t Z0[8], Z1[8];   // rows gid and gid + 8
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int ch = 4 * t + 2 * h + j;
+            const uint4 u0 = *reinterpret_cast<const uint4*>(zb + gid * kZRow + 16 * zpos(ch, gid));
+            const uint4 u1 = *reinterpret_cast<const uint4*>(zb + (gid + 8) * kZRow + 16 * zpos(ch, gid + 8));
+            Z0[4 * j] = u0.x; Z0[4 * j + 1] = u0.y; Z0[4 * j + 2] = u0.z; Z0[4 * j + 3] = u0.w;
+            Z1[4 * j] = u1.x; Z1[4 * j + 1] = u1.y; Z1[4 * j + 2] = u1.z; Z1[4 * j + 3] = u1.w;
+        }
+#pragma unroll
+        for (int ks = 4 * h; ks < 4 * h + 4; ++ks) {
+            uint32_t za[4];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int sl = 2 * ks + e;
+                const int rel = (sl / NSLOT) * 2 * NSLOT + (sl % NSLOT) - 16 * h;   // channel in the half
+                const uint32_t sel = (rel & 1) ? 0x7632u : 0x5410u;
+                za[2 * e] = prmt(Z0[rel >> 1], Z0[(rel + NSLOT) >> 1], sel);
+                za[2 * e + 1] = prmt(Z1[rel >> 1], Z1[(rel + NSLOT) >> 1], sel);
+            }
+            if constexpr (NB == 2) {
+                mma_f16(c, za[0], za[1], za[2], za[3], bh[2 * ks], bh[2 * ks + 1]);
+                mma_f16(c2, za[0], za[1], za[2], za[3], bl[2 * ks], bl[2 * ks + 1]);
+            } else if (ks & 1) {
+                mma_f16(c2, za[0], za[1], za[2], za[3], bh[2 * ks], bh[2 * ks + 1]);
+            } else {
+                mma_f16(c, za[0], za[1], za[2], za[3], bh[2 * ks], bh[2 * ks + 1]);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] += c2[i];
+}
+
 // Packed tiles [ga, gb) of sequence b, kv head hk, for the GQ query heads at q row qrow, on
 // the tensor cores; leaves the merged warp states
 // in red_* (synchronized). Issues its first stages, then loads the stream's q into qs.
@@ -522,8 +590,8 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
     const unsigned char* vz_base = reinterpret_cast<const unsigned char*>(sq.v_zero + hc * NVG);
 
     // Per-lane cp.async plan of one tile: code rows as 16-byte chunks (lane + 32k), then one
-    // chunk of key scale / zero (lanes 0-15 / 16-31) and of value scale / zero (lanes 0-15 /
-    // 16-31 for G = 32; lanes 0-7 / 8-15 for G = 64).
+    // chunk of key scales (lanes 0-15) and of value scale / zero (lanes 0-15 / 16-31 for
+    // G = 32; lanes 0-7 / 8-15 for G = 64). Key zeros travel apart, kZB tiles at a time.
     constexpr int kKChunks = RBK / 16, kVChunks = RBV / 16;   // per lane, per code block
     constexpr int VL = VMETA / 16;                             // lanes per kind of value metadata
     const int half = lane >> 4, off16 = (lane & 15) * 16;
@@ -531,10 +599,10 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
     const bool v_issue = lane < 2 * VL;
     const unsigned char* kc_lane = kc_base + lane * 16;
     const unsigned char* vc_lane = vc_base + lane * 16;
-    const unsigned char* km_lane = (half ? kz_base : ks_base) + off16;
+    const unsigned char* km_lane = ks_base + off16;
     const unsigned char* vm_lane = (vhalf ? vz_base : vs_base) + voff16;
-    const int km_dst = Lay::kCodeBytes + half * Lay::kMetaPad + (off16 >> 6) * 80 + (off16 & 63);
-    const int vm_dst = Lay::kCodeBytes + 2 * Lay::kMetaPad + vhalf * 256 + voff16;
+    const int km_dst = Lay::kCodeBytes + (off16 >> 6) * 80 + (off16 & 63);
+    const int vm_dst = Lay::kCodeBytes + Lay::kMetaPad + vhalf * 256 + voff16;
     auto issue = [&](int slot, int64_t j, int32_t page) {
         unsigned char* dst = my_st + slot * STAGE;
         int64_t rt, kg;
@@ -551,7 +619,7 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
 #pragma unroll
         for (int k = 0; k < kVChunks; ++k)
             cp_async16(dst + kTile * RBK + lane * 16 + 512 * k, vc_lane + rt * (kTile * RBV) + 512 * k);
-        cp_async16(dst + km_dst, km_lane + kg * 256);
+        if (half == 0) cp_async16(dst + km_dst, km_lane + kg * 256);
         if (v_issue) cp_async16(dst + vm_dst, vm_lane + rt * VMETA);
     };
 
@@ -560,6 +628,22 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
     auto page_of = [&](int i) -> int32_t {
         return paged ? sq.block_table[(gfirst + static_cast<int64_t>(kWarps) * i) / TPG] : 0;
     };
+    // key zeros of this warp's tiles [i0, i0 + kZB) (those below n_my) into its buffer: lane L
+    // copies chunk L % 16 of rows L / 16, L / 16 + 2, ...
+    unsigned char* zb = sm.zbuf + warp * kZB * kZRow;
+    auto issue_z = [&](int i0) {
+        const int zc = lane & 15;
+#pragma unroll
+        for (int m = 0; m < kZB / 2; ++m) {
+            const int r = (lane >> 4) + 2 * m, i = i0 + r;
+            if (i < n_my) {
+                const int64_t j = gfirst + static_cast<int64_t>(kWarps) * i;
+                const int64_t kg = paged ? static_cast<int64_t>(sq.block_table[j / TPG]) * a.H + hk : j / TPG;
+                cp_async16(zb + r * kZRow + 16 * zpos(zc, r), kz_base + kg * 256 + zc * 16);
+            }
+        }
+    };
+    issue_z(0);   // joins the first stage's group
 #pragma unroll
     for (int i = 0; i < kStages - 1; ++i) {
         if (i < n_my) issue(i, gfirst + static_cast<int64_t>(kWarps) * i, page_of(i));
@@ -610,7 +694,7 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
 #pragma unroll
     for (int i = 0; i < 8; ++i) cv[i][0] = cv[i][1] = cv[i][2] = cv[i][3] = 0.0f;
     cz[0] = cz[1] = cz[2] = cz[3] = 0.0f;
-
+    float bz_lo = 0.0f, bz_hi = 0.0f;   // the current bias batch: tiles gid and gid + 8, head t
 
     for (int it = 0; it < n_my; ++it) {
         {
@@ -627,43 +711,42 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
         const unsigned char* kc = st;
         const unsigned char* vc = st + kTile * RBK;
         const unsigned char* ksm = st + Lay::kCodeBytes;
-        const unsigned char* kzm = ksm + Lay::kMetaPad;
-        const unsigned char* vsm = kzm + Lay::kMetaPad;    // [32 tokens][NVG] fp16
+        const unsigned char* vsm = ksm + Lay::kMetaPad;    // [32 tokens][NVG] fp16
         const unsigned char* vzm = vsm + 256;
 
-        // ---- key scale / zero pairs of this thread's span
-        uint32_t sp[16], zp[16];
+        // ---- bias of this tile for head t: computed for kZB tiles at the first of them (their
+        // zeros landed with this tile's stage), after which the buffer takes the next batch
+        const int zr = it & (kZB - 1);
+        if (zr == 0) {
+            float bz[4];
+            bias_batch<NSLOT, 1>(zb, gid, t, cB, cB, bz);
+            bz_lo = bz[0] + bz[1];      // tile it + gid, head t (hi and lo columns)
+            bz_hi = bz[2] + bz[3];      // tile it + gid + 8
+            __syncwarp();
+            if (it + kZB < n_my) issue_z(it + kZB);
+        }
+        const float bias = __shfl_sync(kFull, zr < 8 ? bz_lo : bz_hi, 4 * (zr & 7) + t);
+
+        // ---- key scale pairs of this thread's span
+        uint32_t sp[16];
         {
-            uint32_t R[16], Z[16];
+            uint32_t R[16];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint4 r4 = *reinterpret_cast<const uint4*>(ksm + 80 * t + 16 * i);
-                const uint4 z4 = *reinterpret_cast<const uint4*>(kzm + 80 * t + 16 * i);
                 R[4 * i] = r4.x; R[4 * i + 1] = r4.y; R[4 * i + 2] = r4.z; R[4 * i + 3] = r4.w;
-                Z[4 * i] = z4.x; Z[4 * i + 1] = z4.y; Z[4 * i + 2] = z4.z; Z[4 * i + 3] = z4.w;
             }
 #pragma unroll
             for (int s = 0; s < 16; ++s) {
                 const int rel = (s / NSLOT) * 2 * NSLOT + (s % NSLOT);
                 const uint32_t sel = (rel & 1) ? 0x7632u : 0x5410u;
                 sp[s] = prmt(R[rel >> 1], R[(rel + NSLOT) >> 1], sel);
-                zp[s] = prmt(Z[rel >> 1], Z[(rel + NSLOT) >> 1], sel);
             }
         }
 
-        // ---- bias: every row of A is z_k, B = q (hi / lo column)
-        // two accumulators (even / odd k-steps) halve the dependent MMA chain
-        float cb[4] = {0.0f, 0.0f, 0.0f, 0.0f}, cb2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-        for (int ks = 0; ks < 8; ks += 2) {
-            mma_f16(cb, zp[2 * ks], zp[2 * ks], zp[2 * ks + 1], zp[2 * ks + 1], cB[2 * ks], cB[2 * ks + 1]);
-            mma_f16(cb2, zp[2 * ks + 2], zp[2 * ks + 2], zp[2 * ks + 3], zp[2 * ks + 3], cB[2 * ks + 2], cB[2 * ks + 3]);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) cb[i] += cb2[i];
-
-        // ---- scores: A = key codes (tokens gid + 8r), B = (q * s_k) hi / lo
-        float c0[4] = {cb[0], cb[1], cb[2], cb[3]}, c1[4] = {cb[0], cb[1], cb[2], cb[3]};
+        // ---- scores: A = key codes (tokens gid + 8r), B = (q * s_k) hi / lo; the bias enters
+        // through the hi column
+        float c0[4] = {bias, 0.0f, bias, 0.0f}, c1[4] = {bias, 0.0f, bias, 0.0f};
         float c0o[4] = {0.0f, 0.0f, 0.0f, 0.0f}, c1o[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // odd k-steps
         {
             uint32_t cw[4][KB], cws[4][KB];
@@ -700,21 +783,18 @@ a0 = code_slot<KB>(cw[0][w0], cws[0][w0], s0);
             }
         }
 
-        // ---- online softmax for head t over tokens gid, gid+8, gid+16, gid+24
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            c0[i] += c0o[i];
-            c1[i] += c1o[i];
-        }
-        float S[4] = {(c0[0] + c0[1]) * qpost, (c0[2] + c0[3]) * qpost, (c1[0] + c1[1]) * qpost,
-                      (c1[2] + c1[3]) * qpost};
+        // ---- online softmax for head t over tokens gid, gid+8, gid+16, gid+24; the scores are
+        // in units of the prescaled q, and qpost (a power of two) scales them exactly inside
+        // the max and the exponent
+        const float S[4] = {(c0[0] + c0o[0]) + (c0[1] + c0o[1]), (c0[2] + c0o[2]) + (c0[3] + c0o[3]),
+                            (c1[0] + c1o[0]) + (c1[1] + c1o[1]), (c1[2] + c1o[2]) + (c1[3] + c1o[3])};
         float tmax = fmaxf(fmaxf(S[0], S[1]), fmaxf(S[2], S[3]));
         tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 4));
         tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
         tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
-        const float mnew = fmaxf(m_run, tmax);
+        const float mnew = fmaxf(m_run, tmax * qpost);
         if (__any_sync(kFull, mnew > m_run)) {
-            const float alpha = exp2f(m_run - mnew);
+            const float alpha = exp2_ftz(m_run - mnew);
             l_run *= alpha;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -725,7 +805,7 @@ a0 = code_slot<KB>(cw[0][w0], cws[0][w0], s0);
         }
         float p[4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) p[r] = (GQ >= 4 || t < GQ) ? exp2f(S[r] - m_run) : 0.0f;
+        for (int r = 0; r < 4; ++r) p[r] = (GQ >= 4 || t < GQ) ? exp2_ftz(fmaf(S[r], qpost, -m_run)) : 0.0f;
         l_run += (p[0] + p[1]) + (p[2] + p[3]);
 #pragma unroll
         // token 8r + j goes to column 8r + 2 (j % 4) + j / 4: the value side pairs tokens
@@ -877,10 +957,10 @@ __device__ __forceinline__ void group_segment8(const DecodeArgs& a, const MmaSme
     const bool v_issue = lane < 2 * VL;
     const unsigned char* kc_lane = kc_base + lane * 16;
     const unsigned char* vc_lane = vc_base + lane * 16;
-    const unsigned char* km_lane = (half ? kz_base : ks_base) + off16;
+    const unsigned char* km_lane = ks_base + off16;
     const unsigned char* vm_lane = (vhalf ? vz_base : vs_base) + voff16;
-    const int km_dst = Lay::kCodeBytes + half * Lay::kMetaPad + (off16 >> 6) * 80 + (off16 & 63);
-    const int vm_dst = Lay::kCodeBytes + 2 * Lay::kMetaPad + vhalf * 256 + voff16;
+    const int km_dst = Lay::kCodeBytes + (off16 >> 6) * 80 + (off16 & 63);
+    const int vm_dst = Lay::kCodeBytes + Lay::kMetaPad + vhalf * 256 + voff16;
     auto issue = [&](int slot, int64_t j, int32_t page) {
         unsigned char* dst = my_st + slot * STAGE;
         int64_t rt, kg;
@@ -897,12 +977,28 @@ __device__ __forceinline__ void group_segment8(const DecodeArgs& a, const MmaSme
 #pragma unroll
         for (int k = 0; k < kVChunks; ++k)
             cp_async16(dst + kTile * RBK + lane * 16 + 512 * k, vc_lane + rt * (kTile * RBV) + 512 * k);
-        cp_async16(dst + km_dst, km_lane + kg * 256);
+        if (half == 0) cp_async16(dst + km_dst, km_lane + kg * 256);
         if (v_issue) cp_async16(dst + vm_dst, vm_lane + rt * VMETA);
     };
     auto page_of = [&](int i) -> int32_t {
         return paged ? sq.block_table[(gfirst + static_cast<int64_t>(kWarps) * i) / TPG] : 0;
     };
+    // key zeros of this warp's tiles [i0, i0 + kZB) (those below n_my) into its buffer: lane L
+    // copies chunk L % 16 of rows L / 16, L / 16 + 2, ...
+    unsigned char* zb = sm.zbuf + warp * kZB * kZRow;
+    auto issue_z = [&](int i0) {
+        const int zc = lane & 15;
+#pragma unroll
+        for (int m = 0; m < kZB / 2; ++m) {
+            const int r = (lane >> 4) + 2 * m, i = i0 + r;
+            if (i < n_my) {
+                const int64_t j = gfirst + static_cast<int64_t>(kWarps) * i;
+                const int64_t kg = paged ? static_cast<int64_t>(sq.block_table[j / TPG]) * a.H + hk : j / TPG;
+                cp_async16(zb + r * kZRow + 16 * zpos(zc, r), kz_base + kg * 256 + zc * 16);
+            }
+        }
+    };
+    issue_z(0);   // joins the first stage's group
 #pragma unroll
     for (int i = 0; i < kStages - 1; ++i) {
         if (i < n_my) issue(i, gfirst + static_cast<int64_t>(kWarps) * i, page_of(i));
@@ -943,6 +1039,7 @@ __device__ __forceinline__ void group_segment8(const DecodeArgs& a, const MmaSme
 #pragma unroll
     for (int i = 0; i < 8; ++i) cv[i][0] = cv[i][1] = cv[i][2] = cv[i][3] = 0.0f;
     cz[0] = cz[1] = cz[2] = cz[3] = 0.0f;
+    float bz[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // the current bias batch (C rows gid, gid + 8)
 
     for (int it = 0; it < n_my; ++it) {
         {
@@ -959,40 +1056,38 @@ __device__ __forceinline__ void group_segment8(const DecodeArgs& a, const MmaSme
         const unsigned char* kc = st;
         const unsigned char* vc = st + kTile * RBK;
         const unsigned char* ksm = st + Lay::kCodeBytes;
-        const unsigned char* kzm = ksm + Lay::kMetaPad;
-        const unsigned char* vsm = kzm + Lay::kMetaPad;
+        const unsigned char* vsm = ksm + Lay::kMetaPad;
         const unsigned char* vzm = vsm + 256;
 
-        uint32_t sp[16], zp[16];
+        // bias of this tile for heads 2t and 2t + 1 (batched as in group_segment)
+        const int zr = it & (kZB - 1);
+        if (zr == 0) {
+            bias_batch<NSLOT, 2>(zb, gid, t, qh, ql, bz);
+            __syncwarp();
+            if (it + kZB < n_my) issue_z(it + kZB);
+        }
+        const int zsrc = 4 * (zr & 7) + t;
+        const float bias0 = __shfl_sync(kFull, zr < 8 ? bz[0] : bz[2], zsrc);
+        const float bias1 = __shfl_sync(kFull, zr < 8 ? bz[1] : bz[3], zsrc);
+
+        uint32_t sp[16];
         {
-            uint32_t R[16], Z[16];
+            uint32_t R[16];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint4 r4 = *reinterpret_cast<const uint4*>(ksm + 80 * t + 16 * i);
-                const uint4 z4 = *reinterpret_cast<const uint4*>(kzm + 80 * t + 16 * i);
                 R[4 * i] = r4.x; R[4 * i + 1] = r4.y; R[4 * i + 2] = r4.z; R[4 * i + 3] = r4.w;
-                Z[4 * i] = z4.x; Z[4 * i + 1] = z4.y; Z[4 * i + 2] = z4.z; Z[4 * i + 3] = z4.w;
             }
 #pragma unroll
             for (int sl = 0; sl < 16; ++sl) {
                 const int rel = (sl / NSLOT) * 2 * NSLOT + (sl % NSLOT);
                 const uint32_t sel = (rel & 1) ? 0x7632u : 0x5410u;
                 sp[sl] = prmt(R[rel >> 1], R[(rel + NSLOT) >> 1], sel);
-                zp[sl] = prmt(Z[rel >> 1], Z[(rel + NSLOT) >> 1], sel);
             }
         }
-        // bias: A rows all z_k, B = q hi then q lo (two accumulators halve the chain)
-        float cb[4] = {0.0f, 0.0f, 0.0f, 0.0f}, cb2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            mma_f16(cb, zp[2 * ks], zp[2 * ks], zp[2 * ks + 1], zp[2 * ks + 1], qh[2 * ks], qh[2 * ks + 1]);
-            mma_f16(cb2, zp[2 * ks], zp[2 * ks], zp[2 * ks + 1], zp[2 * ks + 1], ql[2 * ks], ql[2 * ks + 1]);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) cb[i] += cb2[i];
 
         // scores: A = key codes, B = (q s_k) hi into c*, then lo into c*o
-        float c0[4] = {cb[0], cb[1], cb[0], cb[1]}, c1[4] = {cb[0], cb[1], cb[0], cb[1]};
+        float c0[4] = {bias0, bias1, bias0, bias1}, c1[4] = {bias0, bias1, bias0, bias1};
         float c0o[4] = {0.0f, 0.0f, 0.0f, 0.0f}, c1o[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         {
             uint32_t cw[4][KB], cws[4][KB];
@@ -1028,10 +1123,11 @@ __device__ __forceinline__ void group_segment8(const DecodeArgs& a, const MmaSme
         }
 
         // online softmax of heads 2t (e = 0) and 2t + 1 (e = 1) over tokens gid, gid+8, gid+16, gid+24
+        // (scores in units of the prescaled q; qpost applied exactly inside the max and the exponent)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            c0[i] = (c0[i] + c0o[i]) * qpost;
-            c1[i] = (c1[i] + c1o[i]) * qpost;
+            c0[i] += c0o[i];
+            c1[i] += c1o[i];
         }
         float p[2][4];
         bool grow = false;
@@ -1042,13 +1138,13 @@ __device__ __forceinline__ void group_segment8(const DecodeArgs& a, const MmaSme
             tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 4));
             tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
             tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
-            mnew[e] = fmaxf(m_run[e], tmax);
+            mnew[e] = fmaxf(m_run[e], tmax * qpost);
             grow |= mnew[e] > m_run[e];
         }
         if (__any_sync(kFull, grow)) {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const float alpha = exp2f(m_run[e] - mnew[e]);
+                const float alpha = exp2_ftz(m_run[e] - mnew[e]);
                 l_run[e] *= alpha;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -1062,10 +1158,10 @@ __device__ __forceinline__ void group_segment8(const DecodeArgs& a, const MmaSme
         }
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            p[e][0] = exp2f(c0[e] - m_run[e]);
-            p[e][1] = exp2f(c0[2 + e] - m_run[e]);
-            p[e][2] = exp2f(c1[e] - m_run[e]);
-            p[e][3] = exp2f(c1[2 + e] - m_run[e]);
+            p[e][0] = exp2_ftz(fmaf(c0[e], qpost, -m_run[e]));
+            p[e][1] = exp2_ftz(fmaf(c0[2 + e], qpost, -m_run[e]));
+            p[e][2] = exp2_ftz(fmaf(c1[e], qpost, -m_run[e]));
+            p[e][3] = exp2_ftz(fmaf(c1[2 + e], qpost, -m_run[e]));
             l_run[e] += (p[e][0] + p[e][1]) + (p[e][2] + p[e][3]);
         }
         // token 8r + j to column 8r + 2 (j % 4) + j / 4, as in group_segment
@@ -1182,6 +1278,11 @@ template <int KB, int VB, int DT, int GQ, int G, int QS>
 __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_kernel(DecodeArgs a) {
     static_assert(GQ == 1 || GQ == 2 || GQ == 4 || GQ == 8, "one n8 tile: hi and lo of up to four heads, or eight heads");
     static_assert(QS == 1 || (GQ == 4 && QS == 2), "streams per kv head");
+    // finish_segment's scratch (after red_acc: GQ weights per segment, at most kMaxCtas + 1
+    // segments per stream) stays in the stages and key-zero buffers, which are idle by then
+    static_assert((GQ * (kWarps + 1) * kD + GQ + (kMaxCtas + 2) * GQ) * 4 <=
+                      MmaLayout<KB, VB>::kStageBytes + MmaLayout<KB, VB>::kZBytes,
+                  "merge scratch below the q buffer");
     extern __shared__ __align__(16) unsigned char smem[];
     const MmaSmem sm(smem, MmaLayout<KB, VB>::kStageBytes, GQ);
     int64_t* sched = reinterpret_cast<int64_t*>(smem);   // scan scratch: the stages are idle until the walk
