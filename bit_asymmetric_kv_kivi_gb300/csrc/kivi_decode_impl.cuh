@@ -603,30 +603,33 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
     const unsigned char* vm_lane = (vhalf ? vz_base : vs_base) + voff16;
     const int km_dst = Lay::kCodeBytes + (off16 >> 6) * 80 + (off16 & 63);
     const int vm_dst = Lay::kCodeBytes + Lay::kMetaPad + vhalf * 256 + voff16;
-    auto issue = [&](int slot, int64_t j, int32_t page) {
+    // Tile and group indices are 32-bit (a stream has fewer than 2^32 tiles, a page pool fewer
+    // than 2^32 / (H TPG) pages), so each address is one 32 x 32 -> 64-bit multiply-add.
+    auto issue = [&](int slot, uint32_t j, int32_t page) {
         unsigned char* dst = my_st + slot * STAGE;
-        int64_t rt, kg;
+        uint32_t rt, kg;
         if (paged) {
-            kg = static_cast<int64_t>(page) * a.H + hk;
-            rt = kg * TPG + (TPG > 1 ? j % TPG : 0);
+            kg = static_cast<uint32_t>(page) * static_cast<uint32_t>(a.H) + static_cast<uint32_t>(hk);
+            rt = kg * TPG + (TPG > 1 ? j % TPG : 0u);
         } else {
             rt = j;
             kg = TPG > 1 ? j / TPG : j;
         }
+        const unsigned char* kc = kc_lane + static_cast<uint64_t>(rt) * (kTile * RBK);
+        const unsigned char* vc = vc_lane + static_cast<uint64_t>(rt) * (kTile * RBV);
 #pragma unroll
-        for (int k = 0; k < kKChunks; ++k)
-            cp_async16(dst + lane * 16 + 512 * k, kc_lane + rt * (kTile * RBK) + 512 * k);
+        for (int k = 0; k < kKChunks; ++k) cp_async16(dst + lane * 16 + 512 * k, kc + 512 * k);
 #pragma unroll
-        for (int k = 0; k < kVChunks; ++k)
-            cp_async16(dst + kTile * RBK + lane * 16 + 512 * k, vc_lane + rt * (kTile * RBV) + 512 * k);
-        if (half == 0) cp_async16(dst + km_dst, km_lane + kg * 256);
-        if (v_issue) cp_async16(dst + vm_dst, vm_lane + rt * VMETA);
+        for (int k = 0; k < kVChunks; ++k) cp_async16(dst + kTile * RBK + lane * 16 + 512 * k, vc + 512 * k);
+        if (half == 0) cp_async16(dst + km_dst, km_lane + static_cast<uint64_t>(kg) * 256);
+        if (v_issue) cp_async16(dst + vm_dst, vm_lane + static_cast<uint64_t>(rt) * VMETA);
     };
 
     // page of this warp's i-th tile (paged sequences); the in-loop issue uses an entry
     // loaded one iteration earlier, so the table read stays off the critical path
+    const uint32_t gfirst32 = static_cast<uint32_t>(gfirst);
     auto page_of = [&](int i) -> int32_t {
-        return paged ? sq.block_table[(gfirst + static_cast<int64_t>(kWarps) * i) / TPG] : 0;
+        return paged ? sq.block_table[(gfirst32 + kWarps * static_cast<uint32_t>(i)) / TPG] : 0;
     };
     // key zeros of this warp's tiles [i0, i0 + kZB) (those below n_my) into its buffer: lane L
     // copies chunk L % 16 of rows L / 16, L / 16 + 2, ...
@@ -637,16 +640,18 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
         for (int m = 0; m < kZB / 2; ++m) {
             const int r = (lane >> 4) + 2 * m, i = i0 + r;
             if (i < n_my) {
-                const int64_t j = gfirst + static_cast<int64_t>(kWarps) * i;
-                const int64_t kg = paged ? static_cast<int64_t>(sq.block_table[j / TPG]) * a.H + hk : j / TPG;
-                cp_async16(zb + r * kZRow + 16 * zpos(zc, r), kz_base + kg * 256 + zc * 16);
+                const uint32_t j = gfirst32 + kWarps * static_cast<uint32_t>(i);
+                const uint32_t kg = paged ? static_cast<uint32_t>(sq.block_table[j / TPG]) * static_cast<uint32_t>(a.H) +
+                                                static_cast<uint32_t>(hk)
+                                          : j / TPG;
+                cp_async16(zb + r * kZRow + 16 * zpos(zc, r), kz_base + static_cast<uint64_t>(kg) * 256 + zc * 16);
             }
         }
     };
     issue_z(0);   // joins the first stage's group
 #pragma unroll
     for (int i = 0; i < kStages - 1; ++i) {
-        if (i < n_my) issue(i, gfirst + static_cast<int64_t>(kWarps) * i, page_of(i));
+        if (i < n_my) issue(i, gfirst32 + kWarps * i, page_of(i));
         cp_async_commit();
     }
     int32_t pg_ahead = kStages - 1 < n_my ? page_of(kStages - 1) : 0;
@@ -669,7 +674,14 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
     const float qpre = ldexpf(1.0f, -qexp), qpost = ldexpf(1.0f, qexp);
 
     // per-thread constants of the key-side B operand (column gid, thread t's span)
-    uint32_t cY[16], cX[16], cZ[16], cB[16];
+    // B = hfma2(cX, s, hfma2(cY, s, -RN(q_hi s) or 0)): q_hi s rounded in the hi columns, its
+    // exact rounding error plus q_lo s in the lo columns. The negated product comes from a
+    // constant cZ = -q_hi (lo columns) or 0; with 2-bit keys it is formed from the product
+    // itself instead (one more instruction per slot, sixteen fewer live registers, which
+    // measured faster there and slower with 4-bit keys).
+    constexpr bool kKeepZ = KB != 2;
+    uint32_t cY[16], cX[16], cZ[kKeepZ ? 16 : 1];
+    const uint32_t pmask = part ? 0xffffffffu : 0u;
 #pragma unroll
     for (int s = 0; s < 16; ++s) {
         const int c0 = 32 * t + (s / NSLOT) * 2 * NSLOT + (s % NSLOT), c1 = c0 + NSLOT;
@@ -679,9 +691,14 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
         const uint32_t ql = pack_h2(v0 - h2_lo(qh), v1 - h2_hi(qh));
         cY[s] = qh;
         cX[s] = part ? ql : 0u;
-        cZ[s] = part ? (qh ^ 0x80008000u) : 0u;
-        cB[s] = part ? ql : qh;
+        if constexpr (kKeepZ) cZ[s] = (qh ^ 0x80008000u) & pmask;
     }
+    auto bkey = [&](const uint32_t (&sp)[16], int sl) -> uint32_t {
+        uint32_t neg;
+        if constexpr (kKeepZ) neg = hmul2(cZ[sl], sp[sl]);
+        else neg = (hmul2(cY[sl], sp[sl]) ^ 0x80008000u) & pmask;
+        return hfma2(cX[sl], sp[sl], hfma2(cY[sl], sp[sl], neg));
+    };
     // value side: byte / half-word selectors of this thread's four channels per channel group
     const uint32_t g3 = static_cast<uint32_t>(gid & 3);
     const uint32_t sel_v = VB == 2 ? (g3 | (g3 << 4) | ((4 + g3) << 8) | ((4 + g3) << 12))
@@ -700,7 +717,7 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
         {
             const int nxt = it + kStages - 1;
             if (nxt < n_my) {
-                issue(nxt % kStages, gfirst + static_cast<int64_t>(kWarps) * nxt, pg_ahead);
+                issue(nxt % kStages, gfirst32 + kWarps * static_cast<uint32_t>(nxt), pg_ahead);
                 pg_ahead = nxt + 1 < n_my ? page_of(nxt + 1) : 0;
             }
             cp_async_commit();
@@ -718,6 +735,9 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
         // zeros landed with this tile's stage), after which the buffer takes the next batch
         const int zr = it & (kZB - 1);
         if (zr == 0) {
+            uint32_t cB[16];   // B of the bias: q hi or lo of column gid, by the column's part
+#pragma unroll
+            for (int sl = 0; sl < 16; ++sl) cB[sl] = part ? cX[sl] : cY[sl];
             float bz[4];
             bias_batch<NSLOT, 1>(zb, gid, t, cB, cB, bz);
             bz_lo = bz[0] + bz[1];      // tile it + gid, head t (hi and lo columns)
@@ -766,8 +786,7 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const int s0 = 2 * ks, s1 = 2 * ks + 1;
-                const uint32_t b0 = hfma2(cX[s0], sp[s0], hfma2(cY[s0], sp[s0], hmul2(cZ[s0], sp[s0])));
-                const uint32_t b1 = hfma2(cX[s1], sp[s1], hfma2(cY[s1], sp[s1], hmul2(cZ[s1], sp[s1])));
+                const uint32_t b0 = bkey(sp, s0), b1 = bkey(sp, s1);
                 const int w0 = s0 / NSLOT, w1 = s1 / NSLOT;
                 uint32_t a0, a1, a2, a3;
 a0 = code_slot<KB>(cw[0][w0], cws[0][w0], s0);
@@ -961,27 +980,30 @@ __device__ __forceinline__ void group_segment8(const DecodeArgs& a, const MmaSme
     const unsigned char* vm_lane = (vhalf ? vz_base : vs_base) + voff16;
     const int km_dst = Lay::kCodeBytes + (off16 >> 6) * 80 + (off16 & 63);
     const int vm_dst = Lay::kCodeBytes + Lay::kMetaPad + vhalf * 256 + voff16;
-    auto issue = [&](int slot, int64_t j, int32_t page) {
+    // Tile and group indices are 32-bit (a stream has fewer than 2^32 tiles, a page pool fewer
+    // than 2^32 / (H TPG) pages), so each address is one 32 x 32 -> 64-bit multiply-add.
+    auto issue = [&](int slot, uint32_t j, int32_t page) {
         unsigned char* dst = my_st + slot * STAGE;
-        int64_t rt, kg;
+        uint32_t rt, kg;
         if (paged) {
-            kg = static_cast<int64_t>(page) * a.H + hk;
-            rt = kg * TPG + (TPG > 1 ? j % TPG : 0);
+            kg = static_cast<uint32_t>(page) * static_cast<uint32_t>(a.H) + static_cast<uint32_t>(hk);
+            rt = kg * TPG + (TPG > 1 ? j % TPG : 0u);
         } else {
             rt = j;
             kg = TPG > 1 ? j / TPG : j;
         }
+        const unsigned char* kc = kc_lane + static_cast<uint64_t>(rt) * (kTile * RBK);
+        const unsigned char* vc = vc_lane + static_cast<uint64_t>(rt) * (kTile * RBV);
 #pragma unroll
-        for (int k = 0; k < kKChunks; ++k)
-            cp_async16(dst + lane * 16 + 512 * k, kc_lane + rt * (kTile * RBK) + 512 * k);
+        for (int k = 0; k < kKChunks; ++k) cp_async16(dst + lane * 16 + 512 * k, kc + 512 * k);
 #pragma unroll
-        for (int k = 0; k < kVChunks; ++k)
-            cp_async16(dst + kTile * RBK + lane * 16 + 512 * k, vc_lane + rt * (kTile * RBV) + 512 * k);
-        if (half == 0) cp_async16(dst + km_dst, km_lane + kg * 256);
-        if (v_issue) cp_async16(dst + vm_dst, vm_lane + rt * VMETA);
+        for (int k = 0; k < kVChunks; ++k) cp_async16(dst + kTile * RBK + lane * 16 + 512 * k, vc + 512 * k);
+        if (half == 0) cp_async16(dst + km_dst, km_lane + static_cast<uint64_t>(kg) * 256);
+        if (v_issue) cp_async16(dst + vm_dst, vm_lane + static_cast<uint64_t>(rt) * VMETA);
     };
+    const uint32_t gfirst32 = static_cast<uint32_t>(gfirst);
     auto page_of = [&](int i) -> int32_t {
-        return paged ? sq.block_table[(gfirst + static_cast<int64_t>(kWarps) * i) / TPG] : 0;
+        return paged ? sq.block_table[(gfirst32 + kWarps * static_cast<uint32_t>(i)) / TPG] : 0;
     };
     // key zeros of this warp's tiles [i0, i0 + kZB) (those below n_my) into its buffer: lane L
     // copies chunk L % 16 of rows L / 16, L / 16 + 2, ...
@@ -992,16 +1014,18 @@ __device__ __forceinline__ void group_segment8(const DecodeArgs& a, const MmaSme
         for (int m = 0; m < kZB / 2; ++m) {
             const int r = (lane >> 4) + 2 * m, i = i0 + r;
             if (i < n_my) {
-                const int64_t j = gfirst + static_cast<int64_t>(kWarps) * i;
-                const int64_t kg = paged ? static_cast<int64_t>(sq.block_table[j / TPG]) * a.H + hk : j / TPG;
-                cp_async16(zb + r * kZRow + 16 * zpos(zc, r), kz_base + kg * 256 + zc * 16);
+                const uint32_t j = gfirst32 + kWarps * static_cast<uint32_t>(i);
+                const uint32_t kg = paged ? static_cast<uint32_t>(sq.block_table[j / TPG]) * static_cast<uint32_t>(a.H) +
+                                                static_cast<uint32_t>(hk)
+                                          : j / TPG;
+                cp_async16(zb + r * kZRow + 16 * zpos(zc, r), kz_base + static_cast<uint64_t>(kg) * 256 + zc * 16);
             }
         }
     };
     issue_z(0);   // joins the first stage's group
 #pragma unroll
     for (int i = 0; i < kStages - 1; ++i) {
-        if (i < n_my) issue(i, gfirst + static_cast<int64_t>(kWarps) * i, page_of(i));
+        if (i < n_my) issue(i, gfirst32 + kWarps * i, page_of(i));
         cp_async_commit();
     }
     int32_t pg_ahead = kStages - 1 < n_my ? page_of(kStages - 1) : 0;
@@ -1045,7 +1069,7 @@ __device__ __forceinline__ void group_segment8(const DecodeArgs& a, const MmaSme
         {
             const int nxt = it + kStages - 1;
             if (nxt < n_my) {
-                issue(nxt % kStages, gfirst + static_cast<int64_t>(kWarps) * nxt, pg_ahead);
+                issue(nxt % kStages, gfirst32 + kWarps * static_cast<uint32_t>(nxt), pg_ahead);
                 pg_ahead = nxt + 1 < n_my ? page_of(nxt + 1) : 0;
             }
             cp_async_commit();
