@@ -1372,7 +1372,7 @@ __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_ker
     if (mine > 0 && lo >= start && lo < start + mine) {
         int64_t p = start;
         for (int b = b_lo; b < b_hi; ++b) {
-            const int64_t ub = static_cast<int64_t>(H) * seq_work<G>(a, b).u;
+            const int64_t us = seq_work<G>(a, b).u, ub = static_cast<int64_t>(H) * us;
             if (lo < p + ub) {
                 vw[0] = lo;
                 vw[1] = hi;
@@ -1380,7 +1380,7 @@ __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_ker
                 vw[3] = Ceff;
                 vw[4] = p;
                 vw[5] = b;
-                vw[6] = 0;
+                vw[6] = (lo - p) / us;   // the stream holding lo (the walk need not visit those before it)
                 break;
             }
             p += ub;
@@ -1430,6 +1430,7 @@ __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_ker
         Cur k = current();
         if (k.Ps >= vw[1]) break;
         if (k.w.u != 0 && k.x1 > k.x0) {
+            bool q_ready = false;   // qs holds this stream's q (loaded by its group segment here)
             if (k.x0 < k.w.ng) {
                 __syncthreads();   // the previous segment is done with qs and the shared arrays
                 if constexpr (GQ == 8)
@@ -1440,12 +1441,15 @@ __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_ker
                                                      k.x1 < k.w.ng ? k.x1 : k.w.ng);
                 finish(0);
                 k = current();
+                q_ready = true;
             }
             if (k.x1 > k.w.ng) {
                 const int64_t u0 = (k.x0 > k.w.ng ? k.x0 : k.w.ng) - k.w.ng, u1 = k.x1 - k.w.ng;
-                __syncthreads();
-                load_q<DT, GQ>(a, sm.qs, stream_row<GQ, QS>(a, k.b, k.h));
-                __syncthreads();
+                __syncthreads();   // the merge arrays and qs are free
+                if (!q_ready) {
+                    load_q<DT, GQ>(a, sm.qs, stream_row<GQ, QS>(a, k.b, k.h));
+                    __syncthreads();
+                }
                 // the stream's query i sees tokens below L - n_query + 1 + i (L for decode)
                 const int nq = QS > 1 && a.n_query > 1 ? a.n_query : 1;
                 const int64_t lend = k.w.L - (nq - 1 - stream_query<GQ, QS>(a, k.h));
