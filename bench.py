@@ -332,7 +332,10 @@ def run_gpu(args, rank, world, local_rank, full=True):
     res = {
         "total_ms": total_ms, "attn_ms": attn_ms, "kv_tokens": kv_tokens, "attn_bytes": bytes_per_step,
         "attn_units": units_per_step,
-        "clocks": clk.summary(), "e2e": e2e, "launches_per_step": 2, "cap": cap, "flush": flush,
+        "clocks": clk.summary(), "e2e": e2e, "cap": cap, "flush": flush,
+        # the one-launch append, then decode_mma_kernel and its merge kernel (query groups 1, 2,
+        # 4 and 8) or decode_multi_kernel (other groups)
+        "launches_per_step": 1 + (2 if Hq // H in (1, 2, 4, 8) else 1),
         "prefill": {"ms": prefill_ms, "algorithmic_bytes": prefill_bytes,
                     "GBps": prefill_bytes / (prefill_ms / 1e3) / 1e9 if prefill_ms > 0 else None},
     }
@@ -415,6 +418,8 @@ def run_gpu_multi(args, rank, world, local_rank):
     value = sum(pairs) * world / (total_ms / 1e3)
     avg_ms = sum(attn_ms) / len(attn_ms)
     achieved = sum(nbytes) / len(nbytes) / (avg_ms / 1e3) / 1e9
+    # one query at query groups 1, 2, 4 and 8, and two queries at group 4, run on the decode kernel
+    on_mma = (N == 1 and Hq // H in (1, 2, 4, 8)) or (N == 2 and Hq // H == 4)
     peak, peak_kind = measured_hbm_peak()
     return {
         "metric": f"verification step ({N} queries per sequence): query x KV-token pairs/s", "value": value,
@@ -426,12 +431,14 @@ def run_gpu_multi(args, rank, world, local_rank):
                                f"G={G}, R={wl.residual}, {wl.dtype}", "n_query": N,
                    "l2": "flushed before every step" if flush else "no flush: the cache is larger than L2",
                    "layout": "paged" if args.paged else "contiguous"},
-        "roofline": {"bound": "hbm", "kernel": "decode_mma_kernel" if (N == 1 and Hq // H in (1, 2, 4, 8)) or
-                     (N == 2 and Hq // H == 4) else "decode_multi_kernel", "achieved": achieved, "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": "decode_mma_kernel" if on_mma else "decode_multi_kernel",
+                     "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "avg_launch_ms": avg_ms,
                      "algorithmic_bytes_per_launch": sum(nbytes) / len(nbytes), "traffic": None},
         "attn_pairs_per_s": sum(pairs) / (sum(attn_ms) / 1e3),
-        "gpu_launches": (2 if N <= wl.group else 4) * args.steps, "clocks": clk.summary(),
+        # the append (one launch up to G new tokens, three beyond), then decode_mma_kernel and its
+        # merge kernel, or decode_multi_kernel
+        "gpu_launches": ((1 if N <= wl.group else 3) + (2 if on_mma else 1)) * args.steps, "clocks": clk.summary(),
     }
 
 

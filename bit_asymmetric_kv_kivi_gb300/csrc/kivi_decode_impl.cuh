@@ -299,15 +299,28 @@ struct StreamSegs {
     int nseg;
 };
 
+// The segments of stream s whose units start at Ps (w: its sequence's work), under the split
+// of U units over Ceff CTAs.
+__device__ __forceinline__ StreamSegs stream_segs(int64_t s, int64_t Ps, const SeqWork& w, int64_t U, int64_t Ceff) {
+    StreamSegs ss;
+    const int64_t Ws = Ps + kStreamOverhead;
+    ss.s = s;
+    ss.cg0 = owner(Ws, U, Ceff);
+    ss.cg1 = w.ng > 0 ? owner(Ws + w.ng - 1, U, Ceff) : ss.cg0 - 1;
+    ss.cr0 = owner(Ws + w.ng, U, Ceff);
+    ss.cr1 = w.rt > 0 ? owner(Ps + w.u - 1, U, Ceff) : ss.cr0 - 1;
+    ss.nseg = static_cast<int>((ss.cg1 - ss.cg0 + 1) + (ss.cr1 - ss.cr0 + 1));
+    return ss;
+}
+
 // Merges the four warps' states of one segment (red_* in shared memory, filled and
-// synchronized by the caller), then writes the output (the stream's only segment) or
-// the segment's partial record; the last CTA of the stream to arrive merges them all.
-// An empty state (m = -inf, l = 0) contributes nothing. scratch: shared memory for
-// GQ * nseg floats from scratch[0] and GQ before it, free once red_* have been read.
+// synchronized by the caller), then writes the output (the stream's only segment) or the
+// segment's partial record (m, l, acc[kD]) per head at index seg; decode_merge_kernel merges
+// the records of streams with several segments. An empty state (m = -inf, l = 0)
+// contributes nothing.
 template <int GQ>
-__device__ __forceinline__ void finish_segment(const DecodeArgs& a, const StreamSegs& ss, int64_t seg, float* out_s,
-                                               const float* red_m, const float* red_l, const float* red_acc,
-                                               int* s_last, float* scratch) {
+__device__ __forceinline__ void write_segment(const DecodeArgs& a, int nseg, int64_t seg, float* out_s,
+                                              const float* red_m, const float* red_l, const float* red_acc) {
     const int tid = threadIdx.x;
     constexpr int64_t rec = kD + 4;
     for (int i = tid; i < GQ * kD; i += kThreads) {
@@ -324,7 +337,7 @@ __device__ __forceinline__ void finish_segment(const DecodeArgs& a, const Stream
                 num = fmaf(red_acc[(w * GQ + hh) * kD + d], f, num);
             }
         }
-        if (ss.nseg == 1) {
+        if (nseg == 1) {
             out_s[i] = num / den;
         } else {
             float* r = a.partials + (seg * GQ + hh) * rec;
@@ -335,53 +348,101 @@ __device__ __forceinline__ void finish_segment(const DecodeArgs& a, const Stream
             }
         }
     }
-    if (ss.nseg == 1) return;
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) *s_last = atomicAdd(&a.counters[ss.s], 1) == ss.nseg - 1;
-    __syncthreads();
-    if (!*s_last) return;
-    __threadfence();
-    // the stream's records: k-th segment -> record index; one warp per head finds the
-    // running max and the weights exp2(m - M) of all records at once (loads in parallel),
-    // then every output sums its records with independent loads
+}
+
+// The record of the k-th segment of stream ss (its packed segments first), head hh.
+template <int GQ>
+__device__ __forceinline__ float* segment_record(const DecodeArgs& a, const StreamSegs& ss, int k, int hh) {
     const int ng_cnt = static_cast<int>(ss.cg1 - ss.cg0 + 1);
-    auto rec_at = [&](int k, int hh) -> float* {
-        const int64_t idx = k < ng_cnt ? 2 * ss.s + ss.cg0 + k : 2 * ss.s + 1 + ss.cr0 + (k - ng_cnt);
-        return a.partials + (idx * GQ + hh) * rec;
-    };
-    const int lane = tid & 31, warp = tid >> 5;
-    for (int hh = warp; hh < GQ; hh += kWarps) {
-        float M = -CUDART_INF_F;
-        for (int k = lane; k < ss.nseg; k += 32) M = fmaxf(M, __ldcg(rec_at(k, hh) + kD));
-        M = warp_max(M);
-        float den = 0.0f;
-        for (int k = lane; k < ss.nseg; k += 32) {
-            const float* r = rec_at(k, hh);
-            const float ms = __ldcg(r + kD);
-            const float f = ms == -CUDART_INF_F ? 0.0f : exp2f(ms - M);
-            scratch[k * GQ + hh] = f;
-            den = fmaf(__ldcg(r + kD + 1), f, den);
+    const int64_t idx = k < ng_cnt ? 2 * ss.s + ss.cg0 + k : 2 * ss.s + 1 + ss.cr0 + (k - ng_cnt);
+    return a.partials + (idx * GQ + hh) * (kD + 4);
+}
+
+// Merges the records of a stream with several segments into its output, then sets them back
+// to zero (every call leaves the workspace as it found it, whatever plan the next call has).
+// Thread d owns channel d of every head and folds the records in one pass with the
+// log-sum-exp rescaling (a record with a larger max rescales what came before), so the loads
+// of all records are independent of one another.
+template <int GQ>
+__device__ __forceinline__ void merge_stream(const DecodeArgs& a, const StreamSegs& ss, float* out_s) {
+    static_assert(kThreads == kD, "one thread per channel");
+    const int d = threadIdx.x;
+    float M[GQ], den[GQ], num[GQ];
+#pragma unroll
+    for (int hh = 0; hh < GQ; ++hh) {
+        M[hh] = -CUDART_INF_F;
+        den[hh] = 0.0f;
+        num[hh] = 0.0f;
+    }
+#pragma unroll 4
+    for (int k = 0; k < ss.nseg; ++k) {
+#pragma unroll
+        for (int hh = 0; hh < GQ; ++hh) {
+            const float* r = segment_record<GQ>(a, ss, k, hh);
+            const float mk = __ldcg(r + kD), lk = __ldcg(r + kD + 1), xk = __ldcg(r + d);
+            if (mk == -CUDART_INF_F) continue;   // an empty segment adds nothing
+            const float Mn = fmaxf(M[hh], mk);
+            const float f = exp2f(M[hh] - Mn), w = exp2f(mk - Mn);   // f = 0 while M is -inf
+            den[hh] = fmaf(den[hh], f, lk * w);
+            num[hh] = fmaf(num[hh], f, xk * w);
+            M[hh] = Mn;
         }
-        den = warp_sum(den);
-        if (lane == 0) scratch[-GQ + hh] = den;
     }
-    __syncthreads();
-    for (int i = tid; i < GQ * kD; i += kThreads) {
-        const int hh = i / kD, d = i - hh * kD;
-        float num = 0.0f;
-#pragma unroll 8
-        for (int k = 0; k < ss.nseg; ++k) num = fmaf(scratch[k * GQ + hh], __ldcg(rec_at(k, hh) + d), num);
-        out_s[i] = num / scratch[-GQ + hh];
-    }
-    // the stream's records back to zero (each segment's GQ records are contiguous): every call
-    // leaves the workspace as it found it (all zero), whatever plan the next call has
+#pragma unroll
+    for (int hh = 0; hh < GQ; ++hh) out_s[hh * kD + d] = num[hh] / den[hh];
+    // the stream's records back to zero (each segment's GQ records are contiguous) once every
+    // thread has read them
     __syncthreads();
     for (int k = 0; k < ss.nseg; ++k) {
-        float4* z = reinterpret_cast<float4*>(rec_at(k, 0));
-        for (int i = tid; i < GQ * static_cast<int>(rec) / 4; i += kThreads) z[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        float4* z = reinterpret_cast<float4*>(segment_record<GQ>(a, ss, k, 0));
+        for (int i = d; i < GQ * (kD + 4) / 4; i += kThreads) z[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     }
-    if (tid == 0) a.counters[ss.s] = 0;
+}
+
+// Units of the streams of sequences [b_lo, b_hi) (this thread's run), the units before them
+// (an exclusive scan over the CTA's threads) and the total U. sched: shared memory for
+// kThreads + 1 + kWarps int64. Contains barriers: every thread of the CTA calls it.
+struct UnitScan {
+    int b_lo, b_hi;
+    int64_t mine, start, U;
+};
+template <int G>
+__device__ __forceinline__ UnitScan scan_units(const DecodeArgs& a, int H, int64_t* sched) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    UnitScan us;
+    const int per = (a.nseq + kThreads - 1) / kThreads;
+    us.b_lo = tid * per < a.nseq ? tid * per : a.nseq;
+    us.b_hi = us.b_lo + per < a.nseq ? us.b_lo + per : a.nseq;
+    us.mine = 0;
+    for (int b = us.b_lo; b < us.b_hi; ++b) us.mine += static_cast<int64_t>(H) * seq_work<G>(a, b).u;
+    // within each warp by shuffles, then the four warp totals (a serial scan by one thread
+    // cost ~2 us at the start of every launch)
+    int64_t incl = us.mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) sched[kThreads + 1 + warp] = incl;
+    __syncthreads();
+    int64_t before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const int64_t x = sched[kThreads + 1 + w];
+        before += w < warp ? x : 0;
+        total += x;
+    }
+    __syncthreads();   // every thread has read the warp totals
+    us.start = before + incl - us.mine;
+    us.U = total;
+    return us;
+}
+
+// The number of CTAs the units are split over: the grid, or fewer when there are fewer
+// than kMinUnitsPerCta units per CTA.
+__device__ __forceinline__ int64_t effective_ctas(int64_t U, int64_t C) {
+    const int64_t by_size = U / kMinUnitsPerCta > 1 ? U / kMinUnitsPerCta : 1;
+    return C < by_size ? C : by_size;
 }
 
 // ---------------------------------------------------------------- tensor-core kernel
@@ -1302,15 +1363,13 @@ template <int KB, int VB, int DT, int GQ, int G, int QS>
 __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_kernel(DecodeArgs a) {
     static_assert(GQ == 1 || GQ == 2 || GQ == 4 || GQ == 8, "one n8 tile: hi and lo of up to four heads, or eight heads");
     static_assert(QS == 1 || (GQ == 4 && QS == 2), "streams per kv head");
-    // finish_segment's scratch (after red_acc: GQ weights per segment, at most kMaxCtas + 1
-    // segments per stream) stays in the stages and key-zero buffers, which are idle by then
-    static_assert((GQ * (kWarps + 1) * kD + GQ + (kMaxCtas + 2) * GQ) * 4 <=
-                      MmaLayout<KB, VB>::kStageBytes + MmaLayout<KB, VB>::kZBytes,
-                  "merge scratch below the q buffer");
     extern __shared__ __align__(16) unsigned char smem[];
     const MmaSmem sm(smem, MmaLayout<KB, VB>::kStageBytes, GQ);
     int64_t* sched = reinterpret_cast<int64_t*>(smem);   // scan scratch: the stages are idle until the walk
     const int tid = threadIdx.x;
+    // the merge kernel behind this one may be scheduled from now on (it waits for this grid's
+    // completion before it reads anything this grid writes)
+    asm volatile("griddepcontrol.launch_dependents;");
     // streams: (sequence, h) with query heads h GQ .. h GQ + GQ - 1 and kv head h / QS; two
     // queries at a query group of 4 are two streams per kv head (QS = 2), one per query, each
     // reading the kv head
@@ -1326,49 +1385,21 @@ __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_ker
         if (w.bad && tid == 0) set_status(a.status, KIVI_ERR_LENGTH);
     }
 
-    // units before each thread's run of sequences (exclusive scan), the total U, and this
-    // CTA's range [lo, hi)
-    const int per = (a.nseq + kThreads - 1) / kThreads;
-    const int b_lo = tid * per < a.nseq ? tid * per : a.nseq;
-    const int b_hi = b_lo + per < a.nseq ? b_lo + per : a.nseq;
-    int64_t mine = 0;
-    for (int b = b_lo; b < b_hi; ++b) mine += static_cast<int64_t>(H) * seq_work<G>(a, b).u;
     // the walk state lives in shared memory and is read back (volatile) around each
     // segment, so that the hot loops do not hold it in registers: lo, hi, U, Ceff, the
     // first unit of sequence b, b, h (b = nseq ends the walk)
     __shared__ int64_t walk[7];
     volatile int64_t* vw = walk;
-    // exclusive scan of the threads' unit counts: within each warp by shuffles, then the four
-    // warp totals (a serial scan by one thread cost ~2 us at the start of every launch)
-    {
-        const int lane = tid & 31, warp = tid >> 5;
-        int64_t incl = mine;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int64_t y = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o) incl += y;
-        }
-        if (lane == 31) sched[kThreads + 1 + warp] = incl;
-        if (tid == 0) vw[5] = a.nseq;
-        __syncthreads();
-        int64_t before = 0, total = 0;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const int64_t x = sched[kThreads + 1 + w];
-            before += w < warp ? x : 0;
-            total += x;
-        }
-        __syncthreads();   // every thread has read the warp totals
-        sched[tid] = before + incl - mine;
-        if (tid == 0) sched[kThreads] = total;
-        __syncthreads();
-    }
-    const int64_t U = sched[kThreads];
-    const int64_t by_size = U / kMinUnitsPerCta > 1 ? U / kMinUnitsPerCta : 1;
-    const int64_t Ceff = C < by_size ? C : by_size;
+    if (tid == 0) vw[5] = a.nseq;
+    // units before each thread's run of sequences (exclusive scan), the total U, and this
+    // CTA's range [lo, hi)
+    const UnitScan us = scan_units<G>(a, H, sched);
+    const int b_lo = us.b_lo, b_hi = us.b_hi;
+    const int64_t mine = us.mine, U = us.U;
+    const int64_t Ceff = effective_ctas(U, C);
     if (U == 0 || c >= Ceff) return;
     const int64_t lo = c * U / Ceff, hi = (c + 1) * U / Ceff;
-    const int64_t start = sched[tid];
+    const int64_t start = us.start;
     if (mine > 0 && lo >= start && lo < start + mine) {
         int64_t p = start;
         for (int b = b_lo; b < b_hi; ++b) {
@@ -1407,19 +1438,15 @@ __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_ker
         k.x1 = (hi_ < k.Ps + k.w.u ? hi_ : k.Ps + k.w.u) - k.Ws;
         return k;
     };
+    // the segment's output (the stream's only segment) or its partial record at 2 s + part + c,
+    // which is unique (each step to the next segment raises the stream, the part or the CTA)
+    // and below 2 S + Ceff
     auto finish = [&](int part) {
         const Cur k = current();
-        const int64_t U_ = vw[2], Ceff_ = vw[3];
-        StreamSegs ss;
-        ss.s = static_cast<int64_t>(k.b) * H + k.h;
-        ss.cg0 = owner(k.Ws, U_, Ceff_);
-        ss.cg1 = k.w.ng > 0 ? owner(k.Ws + k.w.ng - 1, U_, Ceff_) : ss.cg0 - 1;
-        ss.cr0 = owner(k.Ws + k.w.ng, U_, Ceff_);
-        ss.cr1 = k.w.rt > 0 ? owner(k.Ps + k.w.u - 1, U_, Ceff_) : ss.cr0 - 1;
-        ss.nseg = static_cast<int>((ss.cg1 - ss.cg0 + 1) + (ss.cr1 - ss.cr0 + 1));
+        const int64_t s_ = static_cast<int64_t>(k.b) * H + k.h;
+        const StreamSegs ss = stream_segs(s_, k.Ps, k.w, vw[2], vw[3]);
         float* out_s = a.out + stream_row<GQ, QS>(a, k.b, k.h) * kD;
-        finish_segment<GQ>(a, ss, 2 * ss.s + part + c, out_s, sm.red_m, sm.red_l, sm.red_acc, &sm.s_misc[0],
-                           reinterpret_cast<float*>(smem) + GQ * (kWarps + 1) * kD + GQ);
+        write_segment<GQ>(a, ss.nseg, 2 * s_ + part + c, out_s, sm.red_m, sm.red_l, sm.red_acc);
     };
 
     while (true) {
@@ -1494,6 +1521,41 @@ int resident_ctas(K kernel, int smem, std::atomic<int>* cache) {
     return n;
 }
 
+// Merges the streams that the C CTAs of decode_mma_kernel split into several segments: it
+// recomputes the same plan (the row of units, its split over effective_ctas(U, C) CTAs), and
+// each of its CTAs merges the records of a stride of streams (merge_stream). Launched right
+// behind the decode kernel as a programmatic dependent: its launch and its plan (which reads
+// only kv_len and the sequence table) overlap the decode tail, and griddepcontrol.wait holds
+// every thread until the decode grid has completed and its records are visible.
+constexpr int kMergeCtas = 1024;   // grid bound (a grid-stride loop covers more streams)
+template <int GQ, int G, int QS>
+__global__ void __launch_bounds__(kThreads) decode_merge_kernel(DecodeArgs a, int C) {
+    __shared__ int64_t sched[kThreads + 1 + kWarps];
+    __shared__ int64_t stream_at[2];   // first unit of the stream, units of one of its sequence's streams
+    const int H = a.H * QS;
+    const UnitScan us = scan_units<G>(a, H, sched);
+    const int64_t Ceff = effective_ctas(us.U, C);
+    const int64_t S = us.U == 0 ? 0 : static_cast<int64_t>(a.nseq) * H;
+    for (int64_t s = blockIdx.x; s < S; s += gridDim.x) {
+        const int b = static_cast<int>(s / H), h = static_cast<int>(s % H);
+        if (b >= us.b_lo && b < us.b_hi) {   // the thread whose run holds sequence b
+            int64_t p = us.start;
+            for (int bb = us.b_lo; bb < b; ++bb) p += static_cast<int64_t>(H) * seq_work<G>(a, bb).u;
+            const int64_t u = seq_work<G>(a, b).u;
+            stream_at[0] = p + h * u;
+            stream_at[1] = u;
+        }
+        __syncthreads();
+        const int64_t Ps = stream_at[0], u = stream_at[1];
+        __syncthreads();   // every thread has read stream_at
+        if (u == 0) continue;
+        const StreamSegs ss = stream_segs(s, Ps, seq_work<G>(a, b), us.U, Ceff);
+        if (ss.nseg < 2) continue;
+        asm volatile("griddepcontrol.wait;" ::: "memory");   // returns at once after the first time
+        merge_stream<GQ>(a, ss, a.out + stream_row<GQ, QS>(a, b, h) * kD);
+    }
+}
+
 template <int KB, int VB, int DT, int GQ, int G, int QS = 1>
 cudaError_t launch_mma(const DecodeArgs& a, cudaStream_t stream) {
     constexpr int smem = MmaLayout<KB, VB>::kSmemBytes(GQ);
@@ -1501,7 +1563,20 @@ cudaError_t launch_mma(const DecodeArgs& a, cudaStream_t stream) {
     const int n = resident_ctas(decode_mma_kernel<KB, VB, DT, GQ, G, QS>, smem, ctas);
     if (n <= 0) return cudaErrorInvalidValue;
     decode_mma_kernel<KB, VB, DT, GQ, G, QS><<<n, kThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t S = static_cast<int64_t>(a.nseq) * a.H * QS;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(S < kMergeCtas ? S : kMergeCtas));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_merge_kernel<GQ, G, QS>, a, n);
 }
 
 template <int KB, int VB, int DT, int G>

@@ -213,17 +213,20 @@ kivi_status kivi_append_flush(const kivi_cfg* cfg, int32_t nseq, const kivi_seq*
  *   max_kv_len host bound on every kv_len_b (sizes the grid and the workspace)
  *   workspace_dev, workspace_bytes: at least kivi_decode_workspace_bytes()
  *              bytes, zero-filled before its first use; every call leaves it
- *              zero-filled again (the kernels reset their split tickets and
- *              clear the partial records they merge), so one workspace serves
- *              any sequence of decode and multi-query calls whose sizes it
- *              covers. Calls that share a workspace must not overlap.
+ *              zero-filled again (every partial record is cleared by the
+ *              kernel that merges it, and split tickets are reset), so one
+ *              workspace serves any sequence of decode and multi-query calls
+ *              whose sizes it covers. Calls that share a workspace must not
+ *              overlap.
  *   status_dev one int32 (may be NULL)
  * A sequence with kv_len 0 gets zeros. Device error KIVI_ERR_LENGTH: kv_len_b
  * outside [0, max_kv_len] or more tokens than the sequence can hold; that
  * sequence's output rows are set to NaN.
  * Query groups 1, 2, 4 and 8 run on a persistent tensor-core kernel (a group of
- * 8 as two streams of four heads, each reading the kv head); any other
- * group up to 32 on the multi-query kernel with one query.
+ * 8 as one stream of eight heads per kv head), followed on the same stream by
+ * a small kernel that merges the partial records of the sequences and kv
+ * heads it split over several CTAs; any other group up to 32 runs on the
+ * multi-query kernel with one query.
  * Errors: KIVI_ERR_UNSUPPORTED unless D == 128 and Hq/Hkv <= 32.
  */
 kivi_status kivi_decode_attn(const kivi_cfg* cfg, int32_t nseq, const kivi_seq* seqs_dev,
