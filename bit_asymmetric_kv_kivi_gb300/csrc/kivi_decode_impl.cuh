@@ -168,8 +168,8 @@ struct CodeShift {
 // One 32-token tile of residual tokens [ts, min(ts+32, t1)) for one warp, lane = token:
 // scores against the widened stored keys, online-softmax update and value accumulation
 // into the lane-layout state (lane owns channels [4 lane, 4 lane + 4)). Every global
-// load of the tile is issued before its first use (the key row, then the lane's value
-// slices of all 32 tokens), so a tile waits for memory twice, not once per token.
+// load of the tile (the key row, then the lane's value slices of all 32 tokens) is issued
+// before the first use of any, so a tile waits for memory once.
 template <int DT, int GQ>
 __device__ __forceinline__ void residual_tile(const uint16_t* kres, const uint16_t* vres, int ring, int64_t ts,
                                               int64_t t1, const float* qs, int lane, float (&m)[GQ], float (&l)[GQ],
@@ -181,24 +181,12 @@ __device__ __forceinline__ void residual_tile(const uint16_t* kres, const uint16
     float sc[GQ];
 #pragma unroll
     for (int hh = 0; hh < GQ; ++hh) sc[hh] = 0.0f;
+    uint4 kr[kD / 8];
     {
-        uint4 kr[kD / 8];
         const int slot = slot0 + lane >= ring ? slot0 + lane - ring : slot0 + lane;
         const uint4* krow = reinterpret_cast<const uint4*>(kres + static_cast<int64_t>(slot) * kD);
 #pragma unroll
         for (int w = 0; w < kD / 8; ++w) kr[w] = valid ? __ldg(krow + w) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int w = 0; w < kD / 8; ++w) {
-            const uint32_t words[4] = {kr[w].x, kr[w].y, kr[w].z, kr[w].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float k0 = widen<DT>(static_cast<uint16_t>(words[e] & 0xffffu));
-                const float k1 = widen<DT>(static_cast<uint16_t>(words[e] >> 16));
-                const int d = 8 * w + 2 * e;
-#pragma unroll
-                for (int hh = 0; hh < GQ; ++hh) sc[hh] = fmaf(qs[hh * kD + d + 1], k1, fmaf(qs[hh * kD + d], k0, sc[hh]));
-            }
-        }
     }
     uint2 vr[32];
 #pragma unroll
@@ -206,6 +194,18 @@ __device__ __forceinline__ void residual_tile(const uint16_t* kres, const uint16
         const int slot = slot0 + tau >= ring ? slot0 + tau - ring : slot0 + tau;
         vr[tau] = tau < ntok ? __ldg(reinterpret_cast<const uint2*>(vres + static_cast<int64_t>(slot) * kD + lane * kCpl))
                              : make_uint2(0, 0);
+    }
+#pragma unroll
+    for (int w = 0; w < kD / 8; ++w) {
+        const uint32_t words[4] = {kr[w].x, kr[w].y, kr[w].z, kr[w].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float k0 = widen<DT>(static_cast<uint16_t>(words[e] & 0xffffu));
+            const float k1 = widen<DT>(static_cast<uint16_t>(words[e] >> 16));
+            const int d = 8 * w + 2 * e;
+#pragma unroll
+            for (int hh = 0; hh < GQ; ++hh) sc[hh] = fmaf(qs[hh * kD + d + 1], k1, fmaf(qs[hh * kD + d], k0, sc[hh]));
+        }
     }
     float pr[GQ];
 #pragma unroll
