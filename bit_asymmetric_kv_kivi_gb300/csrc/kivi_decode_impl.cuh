@@ -169,7 +169,8 @@ struct CodeShift {
 // scores against the widened stored keys, online-softmax update and value accumulation
 // into the lane-layout state (lane owns channels [4 lane, 4 lane + 4)). Every global
 // load of the tile (the key row, then the lane's value slices of all 32 tokens) is issued
-// before the first use of any, so a tile waits for memory once.
+// before the first use of any, so a tile waits for memory once (for up to four heads; with
+// eight, the value loads follow the scores).
 template <int DT, int GQ>
 __device__ __forceinline__ void residual_tile(const uint16_t* kres, const uint16_t* vres, int ring, int64_t ts,
                                               int64_t t1, const float* qs, int lane, float (&m)[GQ], float (&l)[GQ],
@@ -189,12 +190,15 @@ __device__ __forceinline__ void residual_tile(const uint16_t* kres, const uint16
         for (int w = 0; w < kD / 8; ++w) kr[w] = valid ? __ldg(krow + w) : make_uint4(0, 0, 0, 0);
     }
     uint2 vr[32];
+    auto load_values = [&]() {
 #pragma unroll
-    for (int tau = 0; tau < 32; ++tau) {
-        const int slot = slot0 + tau >= ring ? slot0 + tau - ring : slot0 + tau;
-        vr[tau] = tau < ntok ? __ldg(reinterpret_cast<const uint2*>(vres + static_cast<int64_t>(slot) * kD + lane * kCpl))
-                             : make_uint2(0, 0);
-    }
+        for (int tau = 0; tau < 32; ++tau) {
+            const int slot = slot0 + tau >= ring ? slot0 + tau - ring : slot0 + tau;
+            vr[tau] = tau < ntok ? __ldg(reinterpret_cast<const uint2*>(vres + static_cast<int64_t>(slot) * kD + lane * kCpl))
+                                 : make_uint2(0, 0);
+        }
+    };
+    if constexpr (GQ <= 4) load_values();   // at eight heads the lane state leaves no room to hold them early
 #pragma unroll
     for (int w = 0; w < kD / 8; ++w) {
         const uint32_t words[4] = {kr[w].x, kr[w].y, kr[w].z, kr[w].w};
@@ -207,6 +211,7 @@ __device__ __forceinline__ void residual_tile(const uint16_t* kres, const uint16
             for (int hh = 0; hh < GQ; ++hh) sc[hh] = fmaf(qs[hh * kD + d + 1], k1, fmaf(qs[hh * kD + d], k0, sc[hh]));
         }
     }
+    if constexpr (GQ > 4) load_values();
     float pr[GQ];
 #pragma unroll
     for (int hh = 0; hh < GQ; ++hh) {
