@@ -13,20 +13,25 @@ static size_t ticket_bytes(int nseq, int H) {
     return ((2 * static_cast<size_t>(nseq) * H * sizeof(int32_t) + 255) / 256) * 256;
 }
 
+void mma_plan(int nseq, int H, int D, int per, int streams_per_kv_head, size_t* counter_bytes, size_t* partial_bytes) {
+    // decode_mma_kernel over streams of `per` query heads, streams_per_kv_head per (sequence,
+    // kv head): one record of `per` heads per segment, fewer than 2 S + kDecodeMaxCtas of them.
+    // The tickets in front are the multi-query kernel's; this kernel takes none.
+    const size_t S = static_cast<size_t>(nseq) * H * streams_per_kv_head;
+    *counter_bytes = ticket_bytes(nseq, H);
+    *partial_bytes = (2 * S + kDecodeMaxCtas) * per * (D + 4) * sizeof(float);
+}
+
 void decode_plan(int nseq, int H, int Hq, int D, int max_kv_len, int* chunk, int* max_splits,
                  size_t* counter_bytes, size_t* partial_bytes) {
     const int gq = H > 0 ? Hq / H : 0;
     if (gq == 1 || gq == 2 || gq == 4 || gq == 8) {
-        // decode_mma_kernel over streams of gq query heads, one per (sequence, kv head): a ticket
-        // per stream, one record of gq heads per segment, fewer than 2 S + kDecodeMaxCtas of
-        // them. gq = 8 also serves two queries at a query group of 4, as two streams of four
-        // heads per kv head; S = 2 nseq H records of eight heads cover both.
-        const int per = gq;
-        const size_t S = static_cast<size_t>(nseq) * H * (gq == 8 ? 2 : 1);
-        *counter_bytes = ticket_bytes(nseq, H);
+        // the persistent kernel, one stream of gq heads per kv head. gq = 8 also serves two
+        // queries at a query group of 4, as two streams of four heads per kv head: records
+        // for two streams of eight heads cover both.
         *chunk = 0;
         *max_splits = 0;
-        *partial_bytes = (2 * S + kDecodeMaxCtas) * per * (D + 4) * sizeof(float);
+        mma_plan(nseq, H, D, gq, gq == 8 ? 2 : 1, counter_bytes, partial_bytes);
         return;
     }
     // other query groups (up to 32): decode_multi_kernel with one query per sequence
@@ -36,8 +41,10 @@ void decode_plan(int nseq, int H, int Hq, int D, int max_kv_len, int* chunk, int
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     if (a.nseq == 0) return cudaSuccess;
     const int gq = a.Hq / a.H;
-    // multi-query calls reach here only with streams whose heads share one query
-    if (a.n_query > 1 && (gq % 4 != 0 || gq * a.n_query != 8)) return cudaErrorInvalidValue;
+    // multi-query calls reach here only with one query, or with 2, 4 or 8 queries at a query
+    // group of 4 (one stream of four heads per query and kv head)
+    if (a.n_query > 1 && (gq != 4 || (a.n_query != 2 && a.n_query != 4 && a.n_query != 8)))
+        return cudaErrorInvalidValue;
     if (gq != 1 && gq != 2 && gq != 4 && gq != 8) {
         DecodeArgs m = a;
         m.n_query = 0;     // decode: one query per sequence, empty sequences give zeros

@@ -1367,7 +1367,7 @@ __device__ __forceinline__ void group_segment8(const DecodeArgs& a, const MmaSme
 template <int KB, int VB, int DT, int GQ, int G, int QS>
 __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_kernel(DecodeArgs a) {
     static_assert(GQ == 1 || GQ == 2 || GQ == 4 || GQ == 8, "one n8 tile: hi and lo of up to four heads, or eight heads");
-    static_assert(QS == 1 || (GQ == 4 && QS == 2), "streams per kv head");
+    static_assert(QS == 1 || (GQ == 4 && (QS == 2 || QS == 4 || QS == 8)), "streams per kv head");
     extern __shared__ __align__(16) unsigned char smem[];
     const MmaSmem sm(smem, MmaLayout<KB, VB>::kStageBytes, GQ);
     int64_t* sched = reinterpret_cast<int64_t*>(smem);   // scan scratch: the stages are idle until the walk
@@ -1594,6 +1594,8 @@ cudaError_t launch_gq(const DecodeArgs& a, cudaStream_t stream) {
         case 8:   // decode with a query group of 8: one stream of eight heads; two queries at group 4: one
                   // stream of four heads per query (each with its own causal end)
             return a.n_query > 1 ? launch_mma<KB, VB, DT, 4, G, 2>(a, stream) : launch_mma<KB, VB, DT, 8, G>(a, stream);
+        case 16: return launch_mma<KB, VB, DT, 4, G, 4>(a, stream);   // four queries at group 4
+        case 32: return launch_mma<KB, VB, DT, 4, G, 8>(a, stream);   // eight queries at group 4
         default: return cudaErrorInvalidValue;
     }
 }

@@ -175,6 +175,10 @@ struct DecodeArgs {
 // Bound on the persistent decode grid (CTAs); sizes its workspace.
 constexpr int kDecodeMaxCtas = 1024;
 
+// Workspace of decode_mma_kernel: tickets (unused by it), then records for streams of `per`
+// query heads, streams_per_kv_head per (sequence, kv head).
+void mma_plan(int nseq, int H, int D, int per, int streams_per_kv_head, size_t* counter_bytes, size_t* partial_bytes);
+
 // Split policy and workspace layout shared by kivi_decode_workspace_bytes and the launch.
 void decode_plan(int nseq, int H, int Hq, int D, int max_kv_len, int* chunk, int* max_splits,
                  size_t* counter_bytes, size_t* partial_bytes);

@@ -129,7 +129,7 @@ def test_decode_workspace_plans_by_query_group(lib):
     per kv head, but its plan counts two streams per kv head, so that it also covers two
     queries at group 4 (two streams of four heads per kv head). Other groups take the
     multi-query plan with one query. One-query multi-query calls of groups 1 to 8, and
-    two-query calls of group 4, take the decode plan."""
+    calls of 2, 4 or 8 queries at group 4, take the decode kernel's plans."""
     nseq, H, D = 3, 8, 128
     tickets = ((2 * nseq * H * 4 + 255) // 256) * 256
     for g in (1, 2, 4, 8):
@@ -141,6 +141,12 @@ def test_decode_workspace_plans_by_query_group(lib):
     # two queries at group 4: the decode plan of 8 (query, head) pairs per kv head
     cfg4, cfg8 = (kivi.Config(num_q_heads=g * H, num_kv_heads=H).c() for g in (4, 8))
     assert lib.kivi_decode_multi_workspace_bytes(cfg4, nseq, 2, 5000) == lib.kivi_decode_workspace_bytes(cfg8, nseq, 5000)
+    # four and eight queries at group 4: one stream of four heads per query and kv head
+    for nq in (4, 8):
+        S = nseq * H * nq
+        assert lib.kivi_decode_multi_workspace_bytes(cfg4, nseq, nq, 5000) == tickets + (2 * S + 1024) * 4 * (D + 4) * 4
+    # other counts at group 4 (3, 5) take the multi-query plan, whose size depends on max_kv_len
+    assert lib.kivi_decode_multi_workspace_bytes(cfg4, nseq, 3, 5000) != lib.kivi_decode_multi_workspace_bytes(cfg4, nseq, 3, 50000)
     cfg16 = kivi.Config(num_q_heads=16 * H, num_kv_heads=H).c()
     assert lib.kivi_decode_workspace_bytes(cfg16, nseq, 5000) == lib.kivi_decode_multi_workspace_bytes(cfg16, nseq, 1, 5000)
 

@@ -122,8 +122,8 @@ def test_llama3_8b_gqa_full_size_variants(kb, vb, G, R):
 
 @pytest.mark.parametrize("nq", [2, 4])
 def test_verification_step_full_size(nq):
-    """Draft tokens (two: the decode kernel, two streams per kv head; four: the multi-query
-    kernel) appended to every sequence in one call, then their queries attend causally
+    """Draft tokens (two or four: the decode kernel, one stream per query and kv head)
+    appended to every sequence in one call, then their queries attend causally
     (kivi_decode_multi_attn over the whole batch)."""
     wl = synth.workload(2)
     L, B = wl.lengths[0], wl.batch

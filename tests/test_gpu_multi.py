@@ -54,8 +54,10 @@ CASES = [  # (k_bits, v_bits, G, R, query group, n_query)
     (2, 2, 32, 128, 8, 1), (2, 2, 32, 128, 8, 4), (4, 4, 32, 128, 4, 4), (4, 4, 32, 128, 8, 2),
     (2, 2, 64, 64, 4, 4), (4, 2, 64, 64, 2, 7), (2, 4, 32, 64, 4, 8), (4, 2, 32, 128, 1, 12),
     (2, 4, 64, 128, 8, 3), (4, 4, 64, 64, 1, 1),
-    # two queries at group 4 run on the decode kernel: two streams per kv head, one per query
-    (4, 2, 64, 64, 4, 2), (2, 4, 32, 64, 4, 2), (4, 4, 64, 128, 4, 2),
+    # 2, 4 and 8 queries at group 4 run on the decode kernel: one stream per query and kv head
+    (4, 2, 64, 64, 4, 2), (2, 4, 32, 64, 4, 2), (4, 4, 64, 128, 4, 2), (4, 2, 64, 128, 4, 8),
+    # counts the decode kernel does not take at group 4 stay on the multi-query kernel
+    (2, 2, 32, 128, 4, 3), (4, 4, 64, 64, 4, 5),
 ]
 
 
