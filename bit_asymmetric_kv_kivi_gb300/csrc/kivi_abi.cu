@@ -143,25 +143,23 @@ kivi_status kivi_decode_attn(const kivi_cfg* cfg, int32_t nseq, const kivi_seq* 
 }
 
 // Multi-query calls that run on the persistent decode kernel: one query with a query group
-// of 1, 2, 4 or 8 (decode attention; kv_len 0 stays a length error), and 2, 4 or 8 queries
-// with a group of 4 (one stream of four heads per query and kv head, each stopping at its
-// query's causal end).
+// of 1, 2, 4 or 8 (decode attention; kv_len 0 stays a length error), and several queries at
+// a group of 4 or 8 (one stream of the group's heads per query and kv head, each stopping at
+// its query's causal end).
 static bool multi_is_decode(const kivi_cfg* cfg, int32_t n_query) {
     const int g = cfg->num_q_heads / cfg->num_kv_heads;
-    return (n_query == 1 && (g == 1 || g == 2 || g == 4 || g == 8)) ||
-           (g == 4 && (n_query == 2 || n_query == 4 || n_query == 8));
+    return (n_query == 1 && (g == 1 || g == 2 || g == 4 || g == 8)) || (n_query > 1 && (g == 4 || g == 8));
 }
 
 static void multi_or_decode_plan(const kivi_cfg* cfg, int32_t nseq, int32_t n_query, int32_t max_kv_len, int* chunk,
                                  int* max_splits, size_t* cb, size_t* pb) {
-    if (multi_is_decode(cfg, n_query) && n_query <= 2) {
-        // one query: the decode plan; two at group 4: the plan of group 8 (8 pairs per kv head)
-        kivi::decode_plan(nseq, cfg->num_kv_heads, cfg->num_q_heads * n_query, cfg->head_dim, max_kv_len, chunk,
-                          max_splits, cb, pb);
+    if (multi_is_decode(cfg, n_query) && n_query == 1) {
+        kivi::decode_plan(nseq, cfg->num_kv_heads, cfg->num_q_heads, cfg->head_dim, max_kv_len, chunk, max_splits, cb,
+                          pb);
     } else if (multi_is_decode(cfg, n_query)) {
-        *chunk = 0;   // 4 or 8 queries at group 4: n_query streams of four heads per kv head
+        *chunk = 0;   // n_query streams of the group's heads per kv head
         *max_splits = 0;
-        kivi::mma_plan(nseq, cfg->num_kv_heads, cfg->head_dim, 4, n_query, cb, pb);
+        kivi::mma_plan(nseq, cfg->num_kv_heads, cfg->head_dim, cfg->num_q_heads / cfg->num_kv_heads, n_query, cb, pb);
     } else
         kivi::multi_plan(nseq, cfg->num_kv_heads, cfg->num_q_heads, cfg->head_dim, n_query, max_kv_len, chunk,
                          max_splits, cb, pb);

@@ -26,12 +26,10 @@ void decode_plan(int nseq, int H, int Hq, int D, int max_kv_len, int* chunk, int
                  size_t* counter_bytes, size_t* partial_bytes) {
     const int gq = H > 0 ? Hq / H : 0;
     if (gq == 1 || gq == 2 || gq == 4 || gq == 8) {
-        // the persistent kernel, one stream of gq heads per kv head. gq = 8 also serves two
-        // queries at a query group of 4, as two streams of four heads per kv head: records
-        // for two streams of eight heads cover both.
+        // the persistent kernel, one stream of gq heads per kv head
         *chunk = 0;
         *max_splits = 0;
-        mma_plan(nseq, H, D, gq, gq == 8 ? 2 : 1, counter_bytes, partial_bytes);
+        mma_plan(nseq, H, D, gq, 1, counter_bytes, partial_bytes);
         return;
     }
     // other query groups (up to 32): decode_multi_kernel with one query per sequence
@@ -41,10 +39,9 @@ void decode_plan(int nseq, int H, int Hq, int D, int max_kv_len, int* chunk, int
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     if (a.nseq == 0) return cudaSuccess;
     const int gq = a.Hq / a.H;
-    // multi-query calls reach here only with one query, or with 2, 4 or 8 queries at a query
-    // group of 4 (one stream of four heads per query and kv head)
-    if (a.n_query > 1 && (gq != 4 || (a.n_query != 2 && a.n_query != 4 && a.n_query != 8)))
-        return cudaErrorInvalidValue;
+    // multi-query calls reach here only with one query, or with up to 32 / gq queries at a
+    // query group of 4 or 8 (one stream of gq heads per query and kv head)
+    if (a.n_query > 1 && ((gq != 4 && gq != 8) || a.n_query * gq > 32)) return cudaErrorInvalidValue;
     if (gq != 1 && gq != 2 && gq != 4 && gq != 8) {
         DecodeArgs m = a;
         m.n_query = 0;     // decode: one query per sequence, empty sequences give zeros

@@ -505,22 +505,21 @@ struct MmaSmem {
     }
 };
 
-// Streams of sequence b: h = 0 .. QS Hkv - 1, kv head h / QS. The kv head's V = nq g
-// (query, head) pairs, nq = max(n_query, 1) and g = Hq / Hkv, are numbered query-major
-// (v = i g + j), and stream h takes v0 = (h % QS) GQ .. v0 + GQ - 1, all of one query
-// i = v0 / g (GQ divides g whenever QS > 1). stream_row is the row of its first query head
-// in q and out ([nseq][nq][Hq][D]); stream_query is i.
-// (QS = 1 serves only one query per sequence and g = GQ: row b Hq + h GQ, query 0.)
-template <int GQ, int QS>
+// Streams of sequence b: h = 0 .. QS Hkv - 1, kv head h / QS. For decode (MQ = 0) QS = 1
+// and a stream holds the GQ = Hq / Hkv query heads of its kv head. With several queries
+// (MQ = 1) QS = n_query and stream h holds the GQ = Hq / Hkv heads of query h % QS. stream_row
+// is the row of the stream's first query head in q and out ([nseq][nq][Hq][D], nq = 1 for
+// decode); stream_query is its query.
+template <int GQ, int MQ>
 __device__ __forceinline__ int64_t stream_row(const DecodeArgs& a, int b, int h) {
-    if constexpr (QS == 1) return static_cast<int64_t>(b) * a.Hq + h * GQ;
-    const int g = a.Hq / a.H, nq = a.n_query > 1 ? a.n_query : 1, v0 = (h % QS) * GQ;
-    return (static_cast<int64_t>(b) * nq + v0 / g) * a.Hq + (h / QS) * g + v0 % g;
+    if constexpr (!MQ) return static_cast<int64_t>(b) * a.Hq + h * GQ;
+    const int nq = a.n_query;
+    return (static_cast<int64_t>(b) * nq + h % nq) * a.Hq + (h / nq) * GQ;
 }
-template <int GQ, int QS>
+template <int MQ>
 __device__ __forceinline__ int stream_query(const DecodeArgs& a, int h) {
-    if constexpr (QS == 1) return 0;
-    return (h % QS) * GQ / (a.Hq / a.H);
+    if constexpr (!MQ) return 0;
+    return h % a.n_query;
 }
 
 // q rows [row, row + GQ) into shared memory, scaled by softmax_scale * log2(e); the
@@ -1364,10 +1363,10 @@ __device__ __forceinline__ void group_segment8(const DecodeArgs& a, const MmaSme
     __syncthreads();
 }
 
-template <int KB, int VB, int DT, int GQ, int G, int QS>
+template <int KB, int VB, int DT, int GQ, int G, int MQ>
 __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_kernel(DecodeArgs a) {
     static_assert(GQ == 1 || GQ == 2 || GQ == 4 || GQ == 8, "one n8 tile: hi and lo of up to four heads, or eight heads");
-    static_assert(QS == 1 || (GQ == 4 && (QS == 2 || QS == 4 || QS == 8)), "streams per kv head");
+    static_assert(MQ == 0 || GQ == 4 || GQ == 8, "several queries: one stream per query at query groups 4 and 8");
     extern __shared__ __align__(16) unsigned char smem[];
     const MmaSmem sm(smem, MmaLayout<KB, VB>::kStageBytes, GQ);
     int64_t* sched = reinterpret_cast<int64_t*>(smem);   // scan scratch: the stages are idle until the walk
@@ -1375,16 +1374,16 @@ __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_ker
     // the merge kernel behind this one may be scheduled from now on (it waits for this grid's
     // completion before it reads anything this grid writes)
     asm volatile("griddepcontrol.launch_dependents;");
-    // streams: (sequence, h) with query heads h GQ .. h GQ + GQ - 1 and kv head h / QS; two
-    // queries at a query group of 4 are two streams per kv head (QS = 2), one per query, each
-    // reading the kv head
+    // streams: (sequence, h), kv head h / QS: decode has one per kv head (its GQ query heads);
+    // several queries (MQ) have one per query and kv head, each reading the kv head
+    const int QS = MQ ? a.n_query : 1;   // streams per kv head
     const int C = gridDim.x, c = blockIdx.x, H = a.H * QS;
 
     // sequences without work: zeros for an empty one, NaN and a status for a bad length
     for (int b = c; b < a.nseq; b += C) {
         const SeqWork w = seq_work<G>(a, b);
         if (w.u != 0) continue;
-        const int rows = a.Hq * (QS > 1 && a.n_query > 1 ? a.n_query : 1);
+        const int rows = a.Hq * QS;
         float* o = a.out + static_cast<int64_t>(b) * rows * kD;
         for (int i = tid; i < rows * kD; i += kThreads) o[i] = w.bad ? CUDART_NAN_F : 0.0f;
         if (w.bad && tid == 0) set_status(a.status, KIVI_ERR_LENGTH);
@@ -1450,7 +1449,7 @@ __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_ker
         const Cur k = current();
         const int64_t s_ = static_cast<int64_t>(k.b) * H + k.h;
         const StreamSegs ss = stream_segs(s_, k.Ps, k.w, vw[2], vw[3]);
-        float* out_s = a.out + stream_row<GQ, QS>(a, k.b, k.h) * kD;
+        float* out_s = a.out + stream_row<GQ, MQ>(a, k.b, k.h) * kD;
         write_segment<GQ>(a, ss.nseg, 2 * s_ + part + c, out_s, sm.red_m, sm.red_l, sm.red_acc);
     };
 
@@ -1466,10 +1465,10 @@ __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_ker
             if (k.x0 < k.w.ng) {
                 __syncthreads();   // the previous segment is done with qs and the shared arrays
                 if constexpr (GQ == 8)
-                    group_segment8<KB, VB, DT, G>(a, sm, k.b, stream_row<GQ, QS>(a, k.b, k.h), k.h / QS, k.x0,
+                    group_segment8<KB, VB, DT, G>(a, sm, k.b, stream_row<GQ, MQ>(a, k.b, k.h), k.h / QS, k.x0,
                                                   k.x1 < k.w.ng ? k.x1 : k.w.ng);
                 else
-                    group_segment<KB, VB, DT, GQ, G>(a, sm, k.b, stream_row<GQ, QS>(a, k.b, k.h), k.h / QS, k.x0,
+                    group_segment<KB, VB, DT, GQ, G>(a, sm, k.b, stream_row<GQ, MQ>(a, k.b, k.h), k.h / QS, k.x0,
                                                      k.x1 < k.w.ng ? k.x1 : k.w.ng);
                 finish(0);
                 k = current();
@@ -1479,12 +1478,11 @@ __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_ker
                 const int64_t u0 = (k.x0 > k.w.ng ? k.x0 : k.w.ng) - k.w.ng, u1 = k.x1 - k.w.ng;
                 __syncthreads();   // the merge arrays and qs are free
                 if (!q_ready) {
-                    load_q<DT, GQ>(a, sm.qs, stream_row<GQ, QS>(a, k.b, k.h));
+                    load_q<DT, GQ>(a, sm.qs, stream_row<GQ, MQ>(a, k.b, k.h));
                     __syncthreads();
                 }
                 // the stream's query i sees tokens below L - n_query + 1 + i (L for decode)
-                const int nq = QS > 1 && a.n_query > 1 ? a.n_query : 1;
-                const int64_t lend = k.w.L - (nq - 1 - stream_query<GQ, QS>(a, k.h));
+                const int64_t lend = k.w.L - (QS - 1 - stream_query<MQ>(a, k.h));
                 residual_segment<DT, GQ, G>(a, sm, k.b, k.h / QS, k.w, lend, (u0 + kResidualWeight - 1) / kResidualWeight,
                                          (u1 + kResidualWeight - 1) / kResidualWeight);
                 finish(1);
@@ -1533,11 +1531,11 @@ int resident_ctas(K kernel, int smem, std::atomic<int>* cache) {
 // only kv_len and the sequence table) overlap the decode tail, and griddepcontrol.wait holds
 // every thread until the decode grid has completed and its records are visible.
 constexpr int kMergeCtas = 1024;   // grid bound (a grid-stride loop covers more streams)
-template <int GQ, int G, int QS>
+template <int GQ, int G, int MQ>
 __global__ void __launch_bounds__(kThreads) decode_merge_kernel(DecodeArgs a, int C) {
     __shared__ int64_t sched[kThreads + 1 + kWarps];
     __shared__ int64_t stream_at[2];   // first unit of the stream, units of one of its sequence's streams
-    const int H = a.H * QS;
+    const int H = a.H * (MQ ? a.n_query : 1);
     const UnitScan us = scan_units<G>(a, H, sched);
     const int64_t Ceff = effective_ctas(us.U, C);
     const int64_t S = us.U == 0 ? 0 : static_cast<int64_t>(a.nseq) * H;
@@ -1557,20 +1555,20 @@ __global__ void __launch_bounds__(kThreads) decode_merge_kernel(DecodeArgs a, in
         const StreamSegs ss = stream_segs(s, Ps, seq_work<G>(a, b), us.U, Ceff);
         if (ss.nseg < 2) continue;
         asm volatile("griddepcontrol.wait;" ::: "memory");   // returns at once after the first time
-        merge_stream<GQ>(a, ss, a.out + stream_row<GQ, QS>(a, b, h) * kD);
+        merge_stream<GQ>(a, ss, a.out + stream_row<GQ, MQ>(a, b, h) * kD);
     }
 }
 
-template <int KB, int VB, int DT, int GQ, int G, int QS = 1>
+template <int KB, int VB, int DT, int GQ, int G, int MQ = 0>
 cudaError_t launch_mma(const DecodeArgs& a, cudaStream_t stream) {
     constexpr int smem = MmaLayout<KB, VB>::kSmemBytes(GQ);
     static std::atomic<int> ctas[kMaxDevices];
-    const int n = resident_ctas(decode_mma_kernel<KB, VB, DT, GQ, G, QS>, smem, ctas);
+    const int n = resident_ctas(decode_mma_kernel<KB, VB, DT, GQ, G, MQ>, smem, ctas);
     if (n <= 0) return cudaErrorInvalidValue;
-    decode_mma_kernel<KB, VB, DT, GQ, G, QS><<<n, kThreads, smem, stream>>>(a);
+    decode_mma_kernel<KB, VB, DT, GQ, G, MQ><<<n, kThreads, smem, stream>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int64_t S = static_cast<int64_t>(a.nseq) * a.H * QS;
+    const int64_t S = static_cast<int64_t>(a.nseq) * a.H * (MQ ? a.n_query : 1);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(S < kMergeCtas ? S : kMergeCtas));
     cfg.blockDim = dim3(kThreads);
@@ -1581,21 +1579,22 @@ cudaError_t launch_mma(const DecodeArgs& a, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_merge_kernel<GQ, G, QS>, a, n);
+    return cudaLaunchKernelEx(&cfg, decode_merge_kernel<GQ, G, MQ>, a, n);
 }
 
 template <int KB, int VB, int DT, int G>
 cudaError_t launch_gq(const DecodeArgs& a, cudaStream_t stream) {
-    // (query, head) pairs per kv head: the query group, times n_query for multi-query calls
-    switch (a.Hq / a.H * (a.n_query > 1 ? a.n_query : 1)) {
+    const int g = a.Hq / a.H;
+    if (a.n_query > 1) {   // several queries: one stream of the g heads of each query per kv head
+        if (g == 4) return launch_mma<KB, VB, DT, 4, G, 1>(a, stream);
+        if (g == 8) return launch_mma<KB, VB, DT, 8, G, 1>(a, stream);
+        return cudaErrorInvalidValue;
+    }
+    switch (g) {
         case 1: return launch_mma<KB, VB, DT, 1, G>(a, stream);
         case 2: return launch_mma<KB, VB, DT, 2, G>(a, stream);
         case 4: return launch_mma<KB, VB, DT, 4, G>(a, stream);
-        case 8:   // decode with a query group of 8: one stream of eight heads; two queries at group 4: one
-                  // stream of four heads per query (each with its own causal end)
-            return a.n_query > 1 ? launch_mma<KB, VB, DT, 4, G, 2>(a, stream) : launch_mma<KB, VB, DT, 8, G>(a, stream);
-        case 16: return launch_mma<KB, VB, DT, 4, G, 4>(a, stream);   // four queries at group 4
-        case 32: return launch_mma<KB, VB, DT, 4, G, 8>(a, stream);   // eight queries at group 4
+        case 8: return launch_mma<KB, VB, DT, 8, G>(a, stream);
         default: return cudaErrorInvalidValue;
     }
 }

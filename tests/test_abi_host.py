@@ -125,28 +125,25 @@ def test_multi_query_arguments_rejected_before_launch(lib):
 def test_decode_workspace_plans_by_query_group(lib):
     """The workspace each query group needs, from the documented plans: tickets for two
     streams per (sequence, kv head) in every plan, then fewer than 2 S + 1024 records of
-    g (D + 4) floats, S the number of streams. A group of 8 runs one stream of eight heads
-    per kv head, but its plan counts two streams per kv head, so that it also covers two
-    queries at group 4 (two streams of four heads per kv head). Other groups take the
-    multi-query plan with one query. One-query multi-query calls of groups 1 to 8, and
-    calls of 2, 4 or 8 queries at group 4, take the decode kernel's plans."""
+    g (D + 4) floats, S the number of streams: one per kv head for decode at query groups
+    1, 2, 4 and 8, one per query and kv head for multi-query calls at groups 4 and 8. Other
+    groups and other multi-query calls take the multi-query plan, whose size depends on
+    max_kv_len."""
     nseq, H, D = 3, 8, 128
     tickets = ((2 * nseq * H * 4 + 255) // 256) * 256
     for g in (1, 2, 4, 8):
         cfg = kivi.Config(num_q_heads=g * H, num_kv_heads=H).c()
-        per, S = g, nseq * H * (2 if g == 8 else 1)
-        want = tickets + (2 * S + 1024) * per * (D + 4) * 4
+        want = tickets + (2 * nseq * H + 1024) * g * (D + 4) * 4
         assert lib.kivi_decode_workspace_bytes(cfg, nseq, 5000) == want, g
         assert lib.kivi_decode_multi_workspace_bytes(cfg, nseq, 1, 5000) == want, g
-    # two queries at group 4: the decode plan of 8 (query, head) pairs per kv head
-    cfg4, cfg8 = (kivi.Config(num_q_heads=g * H, num_kv_heads=H).c() for g in (4, 8))
-    assert lib.kivi_decode_multi_workspace_bytes(cfg4, nseq, 2, 5000) == lib.kivi_decode_workspace_bytes(cfg8, nseq, 5000)
-    # four and eight queries at group 4: one stream of four heads per query and kv head
-    for nq in (4, 8):
-        S = nseq * H * nq
-        assert lib.kivi_decode_multi_workspace_bytes(cfg4, nseq, nq, 5000) == tickets + (2 * S + 1024) * 4 * (D + 4) * 4
-    # other counts at group 4 (3, 5) take the multi-query plan, whose size depends on max_kv_len
-    assert lib.kivi_decode_multi_workspace_bytes(cfg4, nseq, 3, 5000) != lib.kivi_decode_multi_workspace_bytes(cfg4, nseq, 3, 50000)
+    for g, nqs in ((4, range(2, 9)), (8, range(2, 5))):
+        cfg = kivi.Config(num_q_heads=g * H, num_kv_heads=H).c()
+        for nq in nqs:
+            S = nseq * H * nq
+            want = tickets + (2 * S + 1024) * g * (D + 4) * 4
+            assert lib.kivi_decode_multi_workspace_bytes(cfg, nseq, nq, 5000) == want, (g, nq)
+    cfg2 = kivi.Config(num_q_heads=2 * H, num_kv_heads=H).c()
+    assert lib.kivi_decode_multi_workspace_bytes(cfg2, nseq, 2, 5000) != lib.kivi_decode_multi_workspace_bytes(cfg2, nseq, 2, 50000)
     cfg16 = kivi.Config(num_q_heads=16 * H, num_kv_heads=H).c()
     assert lib.kivi_decode_workspace_bytes(cfg16, nseq, 5000) == lib.kivi_decode_multi_workspace_bytes(cfg16, nseq, 1, 5000)
 

@@ -54,10 +54,10 @@ CASES = [  # (k_bits, v_bits, G, R, query group, n_query)
     (2, 2, 32, 128, 8, 1), (2, 2, 32, 128, 8, 4), (4, 4, 32, 128, 4, 4), (4, 4, 32, 128, 8, 2),
     (2, 2, 64, 64, 4, 4), (4, 2, 64, 64, 2, 7), (2, 4, 32, 64, 4, 8), (4, 2, 32, 128, 1, 12),
     (2, 4, 64, 128, 8, 3), (4, 4, 64, 64, 1, 1),
-    # 2, 4 and 8 queries at group 4 run on the decode kernel: one stream per query and kv head
+    # several queries at groups 4 and 8 run on the decode kernel: one stream per query and kv
+    # head (the cases above at groups 1 and 2 with several queries run on the multi-query kernel)
     (4, 2, 64, 64, 4, 2), (2, 4, 32, 64, 4, 2), (4, 4, 64, 128, 4, 2), (4, 2, 64, 128, 4, 8),
-    # counts the decode kernel does not take at group 4 stay on the multi-query kernel
-    (2, 2, 32, 128, 4, 3), (4, 4, 64, 64, 4, 5),
+    (2, 2, 32, 128, 4, 3), (4, 4, 64, 64, 4, 5), (2, 2, 32, 128, 8, 3),
 ]
 
 
@@ -155,12 +155,12 @@ def test_multi_query_after_streaming_appends_and_paged_layout(kb, vb, G, R, nq):
         assert np.array_equal(oc, op), step
 
 
-@pytest.mark.parametrize("nq", [6, 2])
-def test_multi_query_bad_lengths(nq):
-    """kv_len below n_query: NaN rows and KIVI_ERR_LENGTH for that sequence only (six
-    queries on the multi-query kernel, two on the decode kernel); n_query * group above 32
-    is refused before launch."""
-    H, g = 1, 4
+@pytest.mark.parametrize("g,nq", [(4, 6), (4, 2), (2, 6)])
+def test_multi_query_bad_lengths(g, nq):
+    """kv_len below n_query: NaN rows and KIVI_ERR_LENGTH for that sequence only (at query
+    group 4 on the decode kernel, at group 2 on the multi-query kernel); n_query * group
+    above 32 is refused before launch."""
+    H = 1
     lengths = (nq - 1, 200)
     wl = synth.Workload("multi-bad", len(lengths), g * H, H, 128, lengths, "f16", seed=430)
     kcfg, ocfg = configs(2, "f16", g * H, H)
@@ -172,17 +172,18 @@ def test_multi_query_bad_lengths(nq):
     want = refs[1].decode_multi(qb[1], wl.softmax_scale)
     assert np.max(np.abs(out[1] - want)) <= ATTN_TOL
     with pytest.raises(kivi.KiviError):
-        cache.decode_multi(dev_tensor(np.zeros((2, 9, 4, 128), np.uint16), "f16"))
+        cache.decode_multi(dev_tensor(np.zeros((2, 32 // g + 1, g, 128), np.uint16), "f16"))
 
 
-@pytest.mark.parametrize("nq", [2, 3])
-def test_decode_and_multi_query_share_one_workspace(nq):
+@pytest.mark.parametrize("g,nq", [(4, 2), (4, 3), (2, 3)])
+def test_decode_and_multi_query_share_one_workspace(g, nq):
     """kivi_decode_attn and kivi_decode_multi_attn alternate on one cache and one workspace
-    (the binding keeps one per cache). With 64 (sequence, kv head) streams the decode
-    tickets fill the first 256 bytes exactly; two queries run the decode kernel over 128
-    streams, three the multi-query kernel. Neither call may leave the other's counters
-    disturbed, and decode repeats bit for bit."""
-    H, g = 8, 4
+    (the binding keeps one per cache). With 64 (sequence, kv head) streams the tickets fill
+    the first 256 bytes exactly; at query group 4 the queries run the decode kernel over
+    nq x 64 streams, at group 2 the multi-query kernel (next to the decode kernel's decode).
+    Neither call may leave the other's counters or records disturbed, and decode repeats bit
+    for bit."""
+    H = 8
     lengths = (700, 1000, 150, 3000, 64, 2000, 999, 128)
     wl = synth.Workload("shared-ws", len(lengths), g * H, H, 128, lengths, "f16", seed=440)
     kcfg, ocfg = configs(2, "f16", g * H, H)
@@ -200,11 +201,11 @@ def test_decode_and_multi_query_share_one_workspace(nq):
         assert err <= ATTN_TOL, err
 
 
-@pytest.mark.parametrize("g,nq", [(4, 2), (8, 2)])
+@pytest.mark.parametrize("g,nq", [(4, 2), (8, 2), (2, 2)])
 def test_plans_with_different_stream_counts_share_one_workspace(g, nq):
     """Calls whose plans count different streams alternate on one workspace: two queries
-    at group 4 run the decode kernel with two streams per kv head next to one-stream
-    decode, and group 8 decodes with two streams next to the multi-query kernel. The
+    at groups 4 and 8 run the decode kernel with two streams per kv head next to one-stream
+    decode, and at group 2 the multi-query kernel runs next to the decode kernel. The
     sequences are long enough that the first CTA writes a partial record right after the
     tickets, so a record region overlapping another plan's tickets would corrupt the next
     call (8000 tokens: about 41 schedule units per CTA, past a stream's 32 units of setup,
