@@ -418,8 +418,9 @@ def run_gpu_multi(args, rank, world, local_rank):
     value = sum(pairs) * world / (total_ms / 1e3)
     avg_ms = sum(attn_ms) / len(attn_ms)
     achieved = sum(nbytes) / len(nbytes) / (avg_ms / 1e3) / 1e9
-    # one query at query groups 1, 2, 4 and 8, and several queries at groups 4 and 8, run on the decode kernel
-    on_mma = (N == 1 and Hq // H in (1, 2, 4, 8)) or (N > 1 and Hq // H in (4, 8))
+    # one query at query groups 1, 2, 4 and 8, several queries at groups 4 and 8, and two queries
+    # at groups 1 and 2 run on the decode kernel
+    on_mma = (N == 1 and Hq // H in (1, 2, 4, 8)) or (N > 1 and Hq // H in (4, 8)) or (N == 2 and Hq // H in (1, 2))
     peak, peak_kind = measured_hbm_peak()
     return {
         "metric": f"verification step ({N} queries per sequence): query x KV-token pairs/s", "value": value,

@@ -143,12 +143,14 @@ kivi_status kivi_decode_attn(const kivi_cfg* cfg, int32_t nseq, const kivi_seq* 
 }
 
 // Multi-query calls that run on the persistent decode kernel: one query with a query group
-// of 1, 2, 4 or 8 (decode attention; kv_len 0 stays a length error), and several queries at
-// a group of 4 or 8 (one stream of the group's heads per query and kv head, each stopping at
-// its query's causal end).
+// of 1, 2, 4 or 8 (decode attention; kv_len 0 stays a length error), several queries at a
+// group of 4 or 8, and two queries at a group of 1 or 2 (one stream of the group's heads per
+// query and kv head, each stopping at its query's causal end). Below four or eight (query,
+// head) pairs per kv head that beat the multi-query kernel, whose shared unpack wins beyond.
 static bool multi_is_decode(const kivi_cfg* cfg, int32_t n_query) {
     const int g = cfg->num_q_heads / cfg->num_kv_heads;
-    return (n_query == 1 && (g == 1 || g == 2 || g == 4 || g == 8)) || (n_query > 1 && (g == 4 || g == 8));
+    return (n_query == 1 && (g == 1 || g == 2 || g == 4 || g == 8)) || (n_query > 1 && (g == 4 || g == 8)) ||
+           (n_query == 2 && (g == 1 || g == 2));
 }
 
 static void multi_or_decode_plan(const kivi_cfg* cfg, int32_t nseq, int32_t n_query, int32_t max_kv_len, int* chunk,

@@ -39,9 +39,11 @@ void decode_plan(int nseq, int H, int Hq, int D, int max_kv_len, int* chunk, int
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     if (a.nseq == 0) return cudaSuccess;
     const int gq = a.Hq / a.H;
-    // multi-query calls reach here only with one query, or with up to 32 / gq queries at a
-    // query group of 4 or 8 (one stream of gq heads per query and kv head)
-    if (a.n_query > 1 && ((gq != 4 && gq != 8) || a.n_query * gq > 32)) return cudaErrorInvalidValue;
+    // multi-query calls reach here only with one query, with up to 32 / gq queries at a query
+    // group of 4 or 8, or with two queries at a group of 1 or 2 (one stream of gq heads per
+    // query and kv head)
+    if (a.n_query > 1 && !(((gq == 4 || gq == 8) && a.n_query * gq <= 32) || ((gq == 1 || gq == 2) && a.n_query == 2)))
+        return cudaErrorInvalidValue;
     if (gq != 1 && gq != 2 && gq != 4 && gq != 8) {
         DecodeArgs m = a;
         m.n_query = 0;     // decode: one query per sequence, empty sequences give zeros

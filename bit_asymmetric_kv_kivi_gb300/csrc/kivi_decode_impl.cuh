@@ -1366,7 +1366,7 @@ __device__ __forceinline__ void group_segment8(const DecodeArgs& a, const MmaSme
 template <int KB, int VB, int DT, int GQ, int G, int MQ>
 __global__ void __launch_bounds__(kThreads, KB + VB <= 6 ? 3 : 2) decode_mma_kernel(DecodeArgs a) {
     static_assert(GQ == 1 || GQ == 2 || GQ == 4 || GQ == 8, "one n8 tile: hi and lo of up to four heads, or eight heads");
-    static_assert(MQ == 0 || GQ == 4 || GQ == 8, "several queries: one stream per query at query groups 4 and 8");
+    static_assert(MQ == 0 || GQ == 1 || GQ == 2 || GQ == 4 || GQ == 8, "one n8 tile per stream");
     extern __shared__ __align__(16) unsigned char smem[];
     const MmaSmem sm(smem, MmaLayout<KB, VB>::kStageBytes, GQ);
     int64_t* sched = reinterpret_cast<int64_t*>(smem);   // scan scratch: the stages are idle until the walk
@@ -1586,9 +1586,13 @@ template <int KB, int VB, int DT, int G>
 cudaError_t launch_gq(const DecodeArgs& a, cudaStream_t stream) {
     const int g = a.Hq / a.H;
     if (a.n_query > 1) {   // several queries: one stream of the g heads of each query per kv head
-        if (g == 4) return launch_mma<KB, VB, DT, 4, G, 1>(a, stream);
-        if (g == 8) return launch_mma<KB, VB, DT, 8, G, 1>(a, stream);
-        return cudaErrorInvalidValue;
+        switch (g) {
+            case 1: return launch_mma<KB, VB, DT, 1, G, 1>(a, stream);
+            case 2: return launch_mma<KB, VB, DT, 2, G, 1>(a, stream);
+            case 4: return launch_mma<KB, VB, DT, 4, G, 1>(a, stream);
+            case 8: return launch_mma<KB, VB, DT, 8, G, 1>(a, stream);
+            default: return cudaErrorInvalidValue;
+        }
     }
     switch (g) {
         case 1: return launch_mma<KB, VB, DT, 1, G>(a, stream);

@@ -260,11 +260,12 @@ size_t kivi_decode_workspace_bytes(const kivi_cfg* cfg, int32_t nseq, int32_t ma
  * Errors: KIVI_ERR_ARG for n_query < 1; KIVI_ERR_UNSUPPORTED unless D == 128
  * and n_query * Hq / Hkv <= 32.
  * n_query == 1 with Hq / Hkv of 1, 2, 4 or 8 runs the kernels of kivi_decode_attn
- * (one query attends to every token), and so do n_query of 2, 4 and 8 with
- * Hq / Hkv == 4 (one stream of four heads per query and kv head, each ending its
- * residual range at its query's causal end); the length errors above apply.
- * Other calls run on a multi-query kernel that unpacks each tile once for all
- * (query, head) pairs of its kv head.
+ * (one query attends to every token), and so do calls with several queries at
+ * Hq / Hkv of 4 or 8 and with two queries at Hq / Hkv of 1 or 2 (one stream of
+ * the group's heads per query and kv head, each ending its residual range at its
+ * query's causal end); the length errors above apply. Other calls run on a
+ * multi-query kernel that unpacks each tile once for all (query, head) pairs of
+ * its kv head.
  */
 kivi_status kivi_decode_multi_attn(const kivi_cfg* cfg, int32_t nseq, const kivi_seq* seqs_dev,
                                    const int32_t* kv_len_dev, int32_t n_query, const void* q_dev,

@@ -126,9 +126,9 @@ def test_decode_workspace_plans_by_query_group(lib):
     """The workspace each query group needs, from the documented plans: tickets for two
     streams per (sequence, kv head) in every plan, then fewer than 2 S + 1024 records of
     g (D + 4) floats, S the number of streams: one per kv head for decode at query groups
-    1, 2, 4 and 8, one per query and kv head for multi-query calls at groups 4 and 8. Other
-    groups and other multi-query calls take the multi-query plan, whose size depends on
-    max_kv_len."""
+    1, 2, 4 and 8, one per query and kv head for multi-query calls at groups 4 and 8 and for
+    two queries at groups 1 and 2. Other groups and other multi-query calls take the
+    multi-query plan, whose size depends on max_kv_len."""
     nseq, H, D = 3, 8, 128
     tickets = ((2 * nseq * H * 4 + 255) // 256) * 256
     for g in (1, 2, 4, 8):
@@ -142,8 +142,11 @@ def test_decode_workspace_plans_by_query_group(lib):
             S = nseq * H * nq
             want = tickets + (2 * S + 1024) * g * (D + 4) * 4
             assert lib.kivi_decode_multi_workspace_bytes(cfg, nseq, nq, 5000) == want, (g, nq)
-    cfg2 = kivi.Config(num_q_heads=2 * H, num_kv_heads=H).c()
-    assert lib.kivi_decode_multi_workspace_bytes(cfg2, nseq, 2, 5000) != lib.kivi_decode_multi_workspace_bytes(cfg2, nseq, 2, 50000)
+    for g in (1, 2):   # two queries at groups 1 and 2: the decode kernel; more: the multi-query plan
+        cfg = kivi.Config(num_q_heads=g * H, num_kv_heads=H).c()
+        want = tickets + (2 * nseq * H * 2 + 1024) * g * (D + 4) * 4
+        assert lib.kivi_decode_multi_workspace_bytes(cfg, nseq, 2, 5000) == want, g
+        assert lib.kivi_decode_multi_workspace_bytes(cfg, nseq, 3, 5000) != lib.kivi_decode_multi_workspace_bytes(cfg, nseq, 3, 50000)
     cfg16 = kivi.Config(num_q_heads=16 * H, num_kv_heads=H).c()
     assert lib.kivi_decode_workspace_bytes(cfg16, nseq, 5000) == lib.kivi_decode_multi_workspace_bytes(cfg16, nseq, 1, 5000)
 

@@ -55,9 +55,12 @@ CASES = [  # (k_bits, v_bits, G, R, query group, n_query)
     (2, 2, 64, 64, 4, 4), (4, 2, 64, 64, 2, 7), (2, 4, 32, 64, 4, 8), (4, 2, 32, 128, 1, 12),
     (2, 4, 64, 128, 8, 3), (4, 4, 64, 64, 1, 1),
     # several queries at groups 4 and 8 run on the decode kernel: one stream per query and kv
-    # head (the cases above at groups 1 and 2 with several queries run on the multi-query kernel)
+    # head (the cases above at groups 1 and 2 with more than two queries run on the
+    # multi-query kernel)
     (4, 2, 64, 64, 4, 2), (2, 4, 32, 64, 4, 2), (4, 4, 64, 128, 4, 2), (4, 2, 64, 128, 4, 8),
     (2, 2, 32, 128, 4, 3), (4, 4, 64, 64, 4, 5), (2, 2, 32, 128, 8, 3),
+    # two queries at groups 1 and 2 also run on the decode kernel
+    (2, 2, 32, 128, 1, 2), (4, 4, 64, 64, 2, 2), (2, 4, 32, 128, 2, 2),
 ]
 
 
@@ -201,11 +204,11 @@ def test_decode_and_multi_query_share_one_workspace(g, nq):
         assert err <= ATTN_TOL, err
 
 
-@pytest.mark.parametrize("g,nq", [(4, 2), (8, 2), (2, 2)])
+@pytest.mark.parametrize("g,nq", [(4, 2), (8, 2), (2, 2), (2, 3)])
 def test_plans_with_different_stream_counts_share_one_workspace(g, nq):
     """Calls whose plans count different streams alternate on one workspace: two queries
-    at groups 4 and 8 run the decode kernel with two streams per kv head next to one-stream
-    decode, and at group 2 the multi-query kernel runs next to the decode kernel. The
+    run the decode kernel with two streams per kv head next to one-stream decode, and three
+    queries at group 2 run the multi-query kernel next to the decode kernel. The
     sequences are long enough that the first CTA writes a partial record right after the
     tickets, so a record region overlapping another plan's tickets would corrupt the next
     call (8000 tokens: about 41 schedule units per CTA, past a stream's 32 units of setup,
