@@ -20,7 +20,8 @@
 //        A operand, unpacked to exact f16 integers (one lop3 + one fma per
 //        pair). Q is the B operand as an f16 hi + lo pair (two columns per
 //        head), built with an exact-error product in f16, so the sum carries
-//        about 22 bits; bias = sum_d q z_k is one more small MMA.
+//        about 22 bits; bias = sum_d q z_k is an MMA over 16 groups at once
+//        (groups as rows).
 //      - Values: O[d][head] += sum_t c[t][d] * P'[t][head] with
 //        P' = p * s_v[t][group(d)] (hi + lo again), channels as M; the
 //        sum_t p z_v term is a small MMA of its own.
@@ -28,15 +29,16 @@
 //    |x| <= 65504 no f16 operand can overflow.
 //    Hq/Hkv = 8 runs as one stream of eight query heads per kv head
 //    (group_segment8: the hi and lo parts of each product are two MMAs over
-//    the same unpacked codes), so every tile is read from DRAM once. Two
-//    queries at Hq/Hkv = 4 run as two streams of four heads, one per query.
+//    the same unpacked codes), so every tile is read from DRAM once. Several
+//    queries (multi-query attention at Hq/Hkv = 4 or 8, and two queries at 1
+//    or 2) run as one stream per query and kv head, the count set at run time.
 //  * other query groups (up to 32) run on decode_multi_kernel (kivi_multi_impl.cuh)
 //    with one query: its CTAs share each unpacked tile between warps of four heads.
 //
-// Every segment writes (m, l, acc[128]) for its query heads to the workspace;
-// the last CTA of a (sequence, kv head) to finish (an atomic ticket, no
-// waiting) merges the records with the log-sum-exp rescaling and writes the
-// fp32 output.
+// Every segment writes (m, l, acc[128]) for its query heads to the workspace, or its
+// output when it holds the whole stream; decode_merge_kernel, launched behind the
+// decode kernel as a programmatic dependent, merges the records of every stream split
+// over several CTAs with the log-sum-exp rescaling and writes the fp32 output.
 //
 // This header holds the kernels as templates over the key and value code widths
 // (KB, VB), the input type, the query group and G; each translation unit that
