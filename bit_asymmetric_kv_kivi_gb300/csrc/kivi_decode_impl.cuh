@@ -18,7 +18,8 @@
 //      - Scores: S[token][head] = sum_d c[token][d] * Q[d][head] + bias[head],
 //        Q = q * s_k (softmax scale and log2(e) folded into q). Codes are the
 //        A operand, unpacked to exact f16 integers (one lop3 + one fma per
-//        pair). Q is the B operand as an f16 hi + lo pair (two columns per
+//        pair; 4-bit keys: one lop3 + two e4m3 converts per four codes, as
+//        c * 2^-9). Q is the B operand as an f16 hi + lo pair (two columns per
 //        head), built with an exact-error product in f16, so the sum carries
 //        about 22 bits; bias = sum_d q z_k is an MMA over 16 groups at once
 //        (groups as rows).
@@ -159,6 +160,29 @@ __device__ __forceinline__ uint32_t code_slot(uint32_t w, uint32_t ws, int s) {
         default: return code_pair<BITS, 7 % kN>(w, ws);
     }
 }
+
+// 4-bit codes as e4m3 bytes: a byte holding b <= 15 reads as exactly b * 2^-9 (the
+// subnormals and the first binade share one step), so one mask leaves four codes in bytes
+// and two converts widen them to two exact f16 pairs, 0.75 instructions per code against
+// one for code_pair. The convert issues at a quarter of the rate of lop3 and hfma2; it
+// measured faster for 4-bit keys only (2-bit fields need more masks and shifts per byte).
+__device__ __forceinline__ void e4m3_pairs(uint32_t y, uint32_t& lo, uint32_t& hi) {
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %2; cvt.rn.f16x2.e4m3x2 %0, l; cvt.rn.f16x2.e4m3x2 %1, h; }"
+        : "=r"(lo), "=r"(hi) : "r"(y));
+}
+constexpr float kE4m3Unit = 512.0f;   // 2^9: a code c widened through e4m3 reads c / 512
+
+// Key slot s (0..15) of a thread's 32-channel span: channel offsets of its pair, (off, off +
+// gap). With code_pair (CVT false) slot s of word s / NSLOT pairs the fields at bits KB i
+// and 16 + KB i, i = s % NSLOT. With the convert (CVT, 4-bit) the slots 2i and 2i + 1 are
+// the halves of one convert of word i / 2: codes (m, m + 2) and (m + 4, m + 6) of the word's
+// eight, m = i % 2.
+template <int KB, bool CVT>
+__host__ __device__ constexpr int kslot_off(int s) {
+    return CVT ? (s / 4) * 8 + ((s % 4) >> 1) + (s & 1) * 4 : (s / (16 / KB)) * 2 * (16 / KB) + s % (16 / KB);
+}
+template <int KB, bool CVT>
+__host__ __device__ constexpr int kslot_gap() { return CVT ? 2 : 16 / KB; }
 
 template <int BITS>
 struct CodeShift {
@@ -571,10 +595,10 @@ __device__ __forceinline__ void residual_segment(const DecodeArgs& a, const MmaS
 
 // Bias term of kZB tiles of a warp, sum_d q[d] z_k[tile][d] per B column, from the key zeros
 // in zb (row r = the tile r places after the batch's first): A = the zeros (row = tile), each
-// register the channel pair of key-score slot s (so the B constants of the scores serve as
-// they are); B = bh, then bl when NB == 2 (two MMAs into one C). c = the C rows gid and
-// gid + 8, columns 2t and 2t + 1.
-template <int NSLOT, int NB>
+// register the channel pair of key-score slot s under the caller's slot map CVT (so the B
+// constants of the scores serve as they are); B = bh, then bl when NB == 2 (two MMAs into
+// one C). c = the C rows gid and gid + 8, columns 2t and 2t + 1.
+template <int NSLOT, int NB, bool CVT = false>
 __device__ __forceinline__ void bias_batch(const unsigned char* zb, int gid, int t, const uint32_t (&bh)[16],
                                            const uint32_t (&bl)[16], float (&c)[4]) {
     float c2[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // a second accumulator halves the dependent chain
@@ -598,10 +622,11 @@ __device__ __forceinline__ void bias_batch(const unsigned char* zb, int gid, int
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int sl = 2 * ks + e;
-                const int rel = (sl / NSLOT) * 2 * NSLOT + (sl % NSLOT) - 16 * h;   // channel in the half
+                const int rel = kslot_off<16 / NSLOT, CVT>(sl) - 16 * h;   // channel in the half
+                const int rel1 = rel + kslot_gap<16 / NSLOT, CVT>();
                 const uint32_t sel = (rel & 1) ? 0x7632u : 0x5410u;
-                za[2 * e] = prmt(Z0[rel >> 1], Z0[(rel + NSLOT) >> 1], sel);
-                za[2 * e + 1] = prmt(Z1[rel >> 1], Z1[(rel + NSLOT) >> 1], sel);
+                za[2 * e] = prmt(Z0[rel >> 1], Z0[rel1 >> 1], sel);
+                za[2 * e + 1] = prmt(Z1[rel >> 1], Z1[rel1 >> 1], sel);
             }
             if constexpr (NB == 2) {
                 mma_f16(c, za[0], za[1], za[2], za[3], bh[2 * ks], bh[2 * ks + 1]);
@@ -631,6 +656,11 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
     constexpr int TPG = G / kTile;            // tiles per key group
     constexpr int NVG = kD / G;               // value channel groups per token
     constexpr int VMETA = kTile * NVG * 2;    // bytes of value scales (or zeros) of one tile
+    // 4-bit key codes are widened through e4m3 (e4m3_pairs): the scores then come out in
+    // units of 2^-9, undone inside the exponent, with the key bias scaled to match. (Value
+    // codes keep code_pair: through e4m3 they measured slower, their words needing a shift
+    // and a byte interleave of two tokens first.)
+    constexpr bool kCvtK = KB == 4;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const kivi_seq& sq = a.seqs[b];
     const int cap = sq.cap_tokens;
@@ -760,7 +790,7 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
     const uint32_t pmask = part ? 0xffffffffu : 0u;
 #pragma unroll
     for (int s = 0; s < 16; ++s) {
-        const int c0 = 32 * t + (s / NSLOT) * 2 * NSLOT + (s % NSLOT), c1 = c0 + NSLOT;
+        const int c0 = 32 * t + kslot_off<KB, kCvtK>(s), c1 = c0 + kslot_gap<KB, kCvtK>();
         const float v0 = hv ? qs[(hv ? hh : 0) * kD + c0] * qpre : 0.0f;
         const float v1 = hv ? qs[(hv ? hh : 0) * kD + c1] * qpre : 0.0f;
         const uint32_t qh = pack_h2(v0, v1);
@@ -815,9 +845,10 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
 #pragma unroll
             for (int sl = 0; sl < 16; ++sl) cB[sl] = part ? cX[sl] : cY[sl];
             float bz[4];
-            bias_batch<NSLOT, 1>(zb, gid, t, cB, cB, bz);
-            bz_lo = bz[0] + bz[1];      // tile it + gid, head t (hi and lo columns)
-            bz_hi = bz[2] + bz[3];      // tile it + gid + 8
+            bias_batch<NSLOT, 1, kCvtK>(zb, gid, t, cB, cB, bz);
+            constexpr float kBiasUnit = kCvtK ? 1.0f / kE4m3Unit : 1.0f;   // to the scores' unit
+            bz_lo = (bz[0] + bz[1]) * kBiasUnit;      // tile it + gid, head t (hi and lo columns)
+            bz_hi = (bz[2] + bz[3]) * kBiasUnit;      // tile it + gid + 8
             __syncwarp();
             if (it + kZB < n_my) issue_z(it + kZB);
         }
@@ -834,9 +865,9 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
             }
 #pragma unroll
             for (int s = 0; s < 16; ++s) {
-                const int rel = (s / NSLOT) * 2 * NSLOT + (s % NSLOT);
+                const int rel = kslot_off<KB, kCvtK>(s);
                 const uint32_t sel = (rel & 1) ? 0x7632u : 0x5410u;
-                sp[s] = prmt(R[rel >> 1], R[(rel + NSLOT) >> 1], sel);
+                sp[s] = prmt(R[rel >> 1], R[(rel + kslot_gap<KB, kCvtK>()) >> 1], sel);
             }
         }
 
@@ -857,7 +888,7 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
                     cw[r][0] = v.x; cw[r][1] = v.y; cw[r][2] = v.z; cw[r][3] = v.w;
                 }
 #pragma unroll
-                for (int w = 0; w < KB; ++w) cws[r][w] = cw[r][w] >> SHIFTK;
+                for (int w = 0; w < KB; ++w) cws[r][w] = cw[r][w] >> (kCvtK ? 4 : SHIFTK);
             }
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
@@ -865,7 +896,20 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
                 const uint32_t b0 = bkey(sp, s0), b1 = bkey(sp, s1);
                 const int w0 = s0 / NSLOT, w1 = s1 / NSLOT;
                 uint32_t a0, a1, a2, a3;
-a0 = code_slot<KB>(cw[0][w0], cws[0][w0], s0);
+                if constexpr (kCvtK) {
+                    // k-step ks: word ks / 2, codes at the low nibble of each byte of the word
+                    // (ks even) or of the word shifted by 4
+                    uint32_t ak[4][2];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+                        e4m3_pairs(((ks & 1) ? cws[r][ks >> 1] : cw[r][ks >> 1]) & 0x0F0F0F0Fu, ak[r][0], ak[r][1]);
+                    if (ks & 1) mma_f16(c0o, ak[0][0], ak[1][0], ak[0][1], ak[1][1], b0, b1);
+                    else mma_f16(c0, ak[0][0], ak[1][0], ak[0][1], ak[1][1], b0, b1);
+                    if (ks & 1) mma_f16(c1o, ak[2][0], ak[3][0], ak[2][1], ak[3][1], b0, b1);
+                    else mma_f16(c1, ak[2][0], ak[3][0], ak[2][1], ak[3][1], b0, b1);
+                    continue;
+                }
+                a0 = code_slot<KB>(cw[0][w0], cws[0][w0], s0);
                 a1 = code_slot<KB>(cw[1][w0], cws[1][w0], s0);
                 a2 = code_slot<KB>(cw[0][w1], cws[0][w1], s1);
                 a3 = code_slot<KB>(cw[1][w1], cws[1][w1], s1);
@@ -887,7 +931,8 @@ a0 = code_slot<KB>(cw[0][w0], cws[0][w0], s0);
         tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 4));
         tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
         tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
-        const float mnew = fmaxf(m_run, tmax * qpost);
+        const float spost = kCvtK ? qpost * kE4m3Unit : qpost;   // exact: both powers of two
+        const float mnew = fmaxf(m_run, tmax * spost);
         if (__any_sync(kFull, mnew > m_run)) {
             const float alpha = exp2_ftz(m_run - mnew);
             l_run *= alpha;
@@ -900,7 +945,7 @@ a0 = code_slot<KB>(cw[0][w0], cws[0][w0], s0);
         }
         float p[4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) p[r] = (GQ >= 4 || t < GQ) ? exp2_ftz(fmaf(S[r], qpost, -m_run)) : 0.0f;
+        for (int r = 0; r < 4; ++r) p[r] = (GQ >= 4 || t < GQ) ? exp2_ftz(fmaf(S[r], spost, -m_run)) : 0.0f;
         l_run += (p[0] + p[1]) + (p[2] + p[3]);
 #pragma unroll
         // token 8r + j goes to column 8r + 2 (j % 4) + j / 4: the value side pairs tokens
