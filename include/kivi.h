@@ -221,7 +221,8 @@ kivi_status kivi_append_flush(const kivi_cfg* cfg, int32_t nseq, const kivi_seq*
  *   status_dev one int32 (may be NULL)
  * A sequence with kv_len 0 gets zeros. Device error KIVI_ERR_LENGTH: kv_len_b
  * outside [0, max_kv_len] or more tokens than the sequence can hold; that
- * sequence's output rows are set to NaN.
+ * sequence's output rows are set to NaN. Domain of q: finite, with
+ * |softmax_scale * q| <= 2^100 (far beyond it fp32 logits overflow anyway).
  * Query groups 1, 2, 4 and 8 run on a persistent tensor-core kernel (a group of
  * 8 as one stream of eight heads per kv head), followed on the same stream by
  * a small kernel that merges the partial records of the sequences and kv
@@ -257,6 +258,7 @@ size_t kivi_decode_workspace_bytes(const kivi_cfg* cfg, int32_t nseq, int32_t ma
  *              kivi_decode_multi_workspace_bytes() for the size
  * Device error KIVI_ERR_LENGTH: kv_len_b < n_query, kv_len_b > max_kv_len or
  * more tokens than the sequence can hold; that sequence's output rows are NaN.
+ * Domain of q: as kivi_decode_attn.
  * Errors: KIVI_ERR_ARG for n_query < 1; KIVI_ERR_UNSUPPORTED unless D == 128
  * and n_query * Hq / Hkv <= 32.
  * n_query == 1 with Hq / Hkv of 1, 2, 4 or 8 runs the kernels of kivi_decode_attn
