@@ -183,6 +183,22 @@ __host__ __device__ constexpr int kslot_off(int s) {
 }
 template <int KB, bool CVT>
 __host__ __device__ constexpr int kslot_gap() { return CVT ? 2 : 16 / KB; }
+// A slot map must cover the span's 32 channels once, pair channels of equal parity (one prmt
+// selector per pair) and keep slots 8h .. 8h + 7 in channels 16h .. 16h + 15 (the bias
+// batch reads the key zeros in those halves).
+template <int KB, bool CVT>
+constexpr bool kslot_map_ok() {
+    bool seen[32] = {};
+    for (int s = 0; s < 16; ++s) {
+        const int c0 = kslot_off<KB, CVT>(s), c1 = c0 + kslot_gap<KB, CVT>();
+        if (c0 < 0 || c1 >= 32 || seen[c0] || seen[c1] || ((c0 ^ c1) & 1)) return false;
+        if (c0 / 16 != s / 8 || c1 / 16 != s / 8) return false;
+        seen[c0] = seen[c1] = true;
+    }
+    return true;
+}
+static_assert(kslot_map_ok<2, false>() && kslot_map_ok<4, false>() && kslot_map_ok<4, true>(),
+              "key slot maps");
 
 template <int BITS>
 struct CodeShift {
