@@ -890,7 +890,6 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
         // ---- scores: A = key codes (tokens gid + 8r), B = (q * s_k) hi / lo; the bias enters
         // through the hi column
         float c0[4] = {bias, 0.0f, bias, 0.0f}, c1[4] = {bias, 0.0f, bias, 0.0f};
-        float c0o[4] = {0.0f, 0.0f, 0.0f, 0.0f}, c1o[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // odd k-steps
         {
             uint32_t cw[4][KB], cws[4][KB];
 #pragma unroll
@@ -919,30 +918,27 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
 #pragma unroll
                     for (int r = 0; r < 4; ++r)
                         e4m3_pairs(((ks & 1) ? cws[r][ks >> 1] : cw[r][ks >> 1]) & 0x0F0F0F0Fu, ak[r][0], ak[r][1]);
-                    if (ks & 1) mma_f16(c0o, ak[0][0], ak[1][0], ak[0][1], ak[1][1], b0, b1);
-                    else mma_f16(c0, ak[0][0], ak[1][0], ak[0][1], ak[1][1], b0, b1);
-                    if (ks & 1) mma_f16(c1o, ak[2][0], ak[3][0], ak[2][1], ak[3][1], b0, b1);
-                    else mma_f16(c1, ak[2][0], ak[3][0], ak[2][1], ak[3][1], b0, b1);
+                    mma_f16(c0, ak[0][0], ak[1][0], ak[0][1], ak[1][1], b0, b1);
+                    mma_f16(c1, ak[2][0], ak[3][0], ak[2][1], ak[3][1], b0, b1);
                     continue;
                 }
                 a0 = code_slot<KB>(cw[0][w0], cws[0][w0], s0);
                 a1 = code_slot<KB>(cw[1][w0], cws[1][w0], s0);
                 a2 = code_slot<KB>(cw[0][w1], cws[0][w1], s1);
                 a3 = code_slot<KB>(cw[1][w1], cws[1][w1], s1);
-                if (ks & 1) mma_f16(c0o, a0, a1, a2, a3, b0, b1); else mma_f16(c0, a0, a1, a2, a3, b0, b1);
+                mma_f16(c0, a0, a1, a2, a3, b0, b1);
                 a0 = code_slot<KB>(cw[2][w0], cws[2][w0], s0);
                 a1 = code_slot<KB>(cw[3][w0], cws[3][w0], s0);
                 a2 = code_slot<KB>(cw[2][w1], cws[2][w1], s1);
                 a3 = code_slot<KB>(cw[3][w1], cws[3][w1], s1);
-                if (ks & 1) mma_f16(c1o, a0, a1, a2, a3, b0, b1); else mma_f16(c1, a0, a1, a2, a3, b0, b1);
+                mma_f16(c1, a0, a1, a2, a3, b0, b1);
             }
         }
 
         // ---- online softmax for head t over tokens gid, gid+8, gid+16, gid+24; the scores are
         // in units of the prescaled q, and qpost (a power of two) scales them exactly inside
         // the max and the exponent
-        const float S[4] = {(c0[0] + c0o[0]) + (c0[1] + c0o[1]), (c0[2] + c0o[2]) + (c0[3] + c0o[3]),
-                            (c1[0] + c1o[0]) + (c1[1] + c1o[1]), (c1[2] + c1o[2]) + (c1[3] + c1o[3])};
+        const float S[4] = {c0[0] + c0[1], c0[2] + c0[3], c1[0] + c1[1], c1[2] + c1[3]};
         float tmax = fmaxf(fmaxf(S[0], S[1]), fmaxf(S[2], S[3]));
         tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 4));
         tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
