@@ -940,12 +940,15 @@ __device__ __forceinline__ void group_segment(const DecodeArgs& a, const MmaSmem
         // the max and the exponent
         const float S[4] = {c0[0] + c0[1], c0[2] + c0[3], c1[0] + c1[1], c1[2] + c1[3]};
         float tmax = fmaxf(fmaxf(S[0], S[1]), fmaxf(S[2], S[3]));
-        tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 4));
-        tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
-        tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
         const float spost = kCvtK ? qpost * kE4m3Unit : qpost;   // exact: both powers of two
-        const float mnew = fmaxf(m_run, tmax * spost);
-        if (__any_sync(kFull, mnew > m_run)) {
+        // the head's max over the tile's 32 tokens (a reduction over the lanes of head t) is
+        // needed only when some lane's own four tokens pass its running max; otherwise it
+        // could not pass either and the state stays as it is
+        if (__any_sync(kFull, tmax * spost > m_run)) {
+            tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 4));
+            tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
+            tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
+            const float mnew = fmaxf(m_run, tmax * spost);
             const float alpha = exp2_ftz(m_run - mnew);
             l_run *= alpha;
 #pragma unroll
