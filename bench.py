@@ -96,12 +96,12 @@ def attn_bytes(wl, lengths, kb, vb):
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per (token, kv head) of one
 # decode launch, from ncu captures of the kernels in their current version on the 8-sequence
-# case of the Llama-3-8B GQA workload (2-bit, bf16): 209.29 MB for 8 x 8 x 32772 units at
+# case of the Llama-3-8B GQA workload (2-bit, bf16): 209.11 MB for 8 x 8 x 32772 units at
 # query group 4, and 415.19 MB for 16 x 8 x 32772 units at query group 8 (64 query heads).
 # Keyed by (kernel, k_bits, v_bits, G, R, query group, input dtype); a configuration without
 # an entry reports traffic as null.
 NCU_TRAFFIC_BYTES_PER_UNIT = {
-    ("decode_mma_kernel", 2, 2, 32, 128, 4, "bf16"): 209_293_312 / (8 * 8 * 32772),
+    ("decode_mma_kernel", 2, 2, 32, 128, 4, "bf16"): 209_112_832 / (8 * 8 * 32772),
     ("decode_mma_kernel", 2, 2, 32, 128, 8, "bf16"): 415_185_408 / (16 * 8 * 32772),
 }
 
